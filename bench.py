@@ -1,0 +1,373 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged-KV decode step on GB300.
+
+A step is the whole hot path over one batch: paged_kv_append of the step's
+new K/V (32 tokens) followed by paged_attention (split over a persistent grid,
+merged in-kernel) on the continuous-batch decode workload: 32 sequences,
+32 query / 8 KV heads, head_dim 128, block size 16, context lengths uniform in
+[256, 2048], bf16 K/V ~ N(0, 1), block tables from a shuffled 5,000-block pool.
+
+Prints ONE JSON line (rank 0).  `value` is KV GB/s of the whole step
+(algorithmic KV bytes / device time of append + attention), inputs resident in
+HBM, L2 flushed between timed steps.  `--impl reference` times the CPU oracle
+on the host cores instead (a deliberately slow reference).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torchrun (one rank per GPU); every rank runs its own
+replica of the workload (weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode KV GB/s (% of HBM peak) and seq-steps/s at B=32, d=128"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="named workload (default: the decode config)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attn_algorithmic_bytes(w) -> int:
+    """Bytes the attention must move once: KV (+ FP8 scales), q, out, the block
+    table entries it reads and the two length arrays."""
+    nblk = int(((w.context_lens.astype(np.int64) + 15) // 16).sum())
+    return w.kv_bytes() + 2 * w.q.nbytes + 4 * nblk + 8 * w.num_seqs
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_14_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per attention launch from a committed ncu capture, if it was
+    taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for ln in open(self.path):
+                parts = [x.strip() for x in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        except Exception:
+            return None
+        if not sms:
+            return None
+        return {"sm_mhz": float(np.median(sms)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+class OracleStepper:
+    """The CPU oracle, as it stands, on the host cores.  One sample step =
+    the oracle's append of the step's new tokens plus its attention for a
+    slice of the batch's sequences (`seqs_per_step` of them, rotating), so a
+    step stays bounded; the KV bytes of the slice give the throughput."""
+
+    def __init__(self, w, seqs_per_step: int):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.kc, self.vc = oracle.build_cache(w, with_step=False)
+        self.kd = oracle.KV_FP8 if w.kv_dtype == "fp8" else oracle.KV_BF16
+        self.threads = os.cpu_count() or 1
+        self.spp = max(1, min(seqs_per_step, w.num_seqs))
+        self.qoff = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int64)
+        self.i = 0
+
+    def step(self):
+        """Returns (KV bytes processed, seconds)."""
+        w, o = self.w, self.oracle
+        b0 = (self.i * self.spp) % w.num_seqs
+        bs = [(b0 + j) % w.num_seqs for j in range(self.spp)]
+        self.i += 1
+        rows = np.concatenate([np.arange(self.qoff[b], self.qoff[b + 1]) for b in bs])
+        L = w.context_lens[bs]
+        t0 = time.perf_counter()
+        o.paged_kv_append(self.kd, self.kc, self.vc, w.k_scales, w.v_scales, w.num_blocks, w.num_kv_heads,
+                          w.head_dim, w.k_new[rows], w.v_new[rows], w.slots[rows])
+        o.paged_attention(self.kd, self.kc, self.vc, w.k_scales, w.v_scales, w.num_blocks, w.num_kv_heads,
+                          w.head_dim, w.q[rows], w.num_q_heads, w.block_tables[bs], L, w.q_lens[bs], w.scale,
+                          self.threads)
+        el = time.perf_counter() - t0
+        kvb = int(L.astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 2 * w.elem_bytes
+        return kvb, el
+
+
+def cpu_baseline(w, seconds: float, seqs_per_step: int = 8):
+    """Oracle throughput over ~`seconds` of sample steps: (GB/s, threads, steps, s)."""
+    st = OracleStepper(w, seqs_per_step)
+    tot_b, tot_t, n = 0, 0.0, 0
+    while tot_t < seconds:
+        b, t = st.step()
+        tot_b += b
+        tot_t += t
+        n += 1
+    return tot_b / tot_t / 1e9, st.threads, n, tot_t
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from paged_kv_decode_14_gb300 import workloads as wl
+    w = wl.CONFIGS[args.config]()
+    spp = 2
+    st = OracleStepper(w, spp)
+    for _ in range(args.warmup):
+        st.step()
+    tot_b, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        b, t = st.step()
+        tot_b += b
+        tot_t += t
+    val = tot_b / tot_t / 1e9
+    # ms for a full batch step at this rate
+    ms = 1e3 * w.kv_bytes() / (val * 1e9)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": 16,
+                       "kv_bytes_per_step": w.kv_bytes()},
+            "seq_steps_per_s": w.num_seqs / (ms / 1e3),
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": st.threads, "kind": "oracle",
+                             "sample": f"each step: oracle append + attention for {spp} of the {w.num_seqs} "
+                                       f"sequences (rotating); ms_per_step scaled to the whole batch"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from paged_kv_decode_14_gb300 import _native as nat
+    from paged_kv_decode_14_gb300 import workloads as wl
+    from paged_kv_decode_14_gb300.runner import DeviceWorkload
+
+    nat.lib()
+    w = wl.CONFIGS[args.config]()
+    dw = DeviceWorkload(w, device=dev)
+    dw.prefill()
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---------------- device-resident timing
+    for _ in range(args.warmup):
+        flush.zero_()
+        dw.step()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.__enter__()
+    barrier()
+    wall0 = time.perf_counter()
+    for e0, e1, e2 in ev:
+        flush.zero_()                     # L2 flush, outside the timed events
+        e0.record(stream)
+        dw.append_step()
+        e1.record(stream)
+        dw.attend()
+        e2.record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    if clocks:
+        clocks.__exit__()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    attn_ms = [b.elapsed_time(c) for _, b, c in ev]
+    app_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    tot = float(np.sum(step_ms))
+    if world > 1:
+        t = torch.tensor([tot], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot = float(t.item())
+    kvb = w.kv_bytes()
+    ms = tot / args.steps
+    value = world * kvb * args.steps / (tot / 1e3) / 1e9
+
+    # ---------------- end to end through the public API, host buffers
+    hin, hout = w.step_io_bytes()
+    pin = {n: getattr(dw, n).cpu().pin_memory() for n in ("q", "k_new", "v_new", "slots", "block_tables",
+                                                           "context_lens", "q_lens")}
+    host_out = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        if i >= args.warmup:
+            e2e_ev[i - args.warmup][0].record(stream)
+        for n, t in pin.items():
+            getattr(dw, n).copy_(t, non_blocking=True)
+        dw.step()
+        host_out.copy_(dw.out, non_blocking=True)
+        if i >= args.warmup:
+            e2e_ev[i - args.warmup][1].record(stream)
+    barrier()
+    e2e_tot = float(sum(a.elapsed_time(b) for a, b in e2e_ev))
+    if world > 1:
+        t = torch.tensor([e2e_tot], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_tot = float(t.item())
+    e2e_val = world * kvb * args.steps / (e2e_tot / 1e3) / 1e9
+
+    # ---------------- roofline of the dominant kernel (attention)
+    peak, peak_kind = hbm_peak()
+    attn_avg_ms = float(np.mean(attn_ms))
+    achieved = attn_algorithmic_bytes(w) / (attn_avg_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": load_traffic(w.name), "peak_kind": f"{peak_kind} (copy bandwidth)",
+            "kernel": "paged attention (persistent split-KV, in-kernel merge)",
+            "algorithmic_bytes_per_launch": attn_algorithmic_bytes(w),
+            "avg_launch_us": attn_avg_ms * 1e3}
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": 16,
+                       "context_lens": "uniform [256, 2048]", "pool_blocks": w.num_blocks,
+                       "kv_bytes_per_step": kvb, "l2": "flushed before every timed step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_hbm_peak": 100.0 * value / peak,
+            "seq_steps_per_s": world * w.num_seqs * args.steps / (tot / 1e3),
+            "attention_us": attn_avg_ms * 1e3, "append_us": float(np.mean(app_ms)) * 1e3,
+            "step_us_p10_p50_p90": [float(np.percentile(step_ms, q)) * 1e3 for q in (10, 50, 90)],
+            "roofline": roof,
+            "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": hin, "d2h_bytes_per_step": hout,
+                    "ms_per_step": e2e_tot / args.steps},
+            "gpu_launches": 2 * args.steps,
+            "wall_s_timed_region": wall}
+    if clocks:
+        line["clocks"] = clocks.summary()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, threads, n, el = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{n} full decode steps (append + attention of all {w.num_seqs} "
+                                          f"sequences) in {el:.1f} s"}
+    errs = dw.errors()
+    if errs != (0, 0):
+        line["device_errors"] = list(errs)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,191 @@
+/*
+ * pagedkv.h -- C ABI of the paged-KV decode attention library (libpagedkv.so),
+ * written for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the problem the paged-KV pages state:
+ *   - inferd README, "Paged KV" phase (block allocator + page table) and the
+ *     "Paged KV equivalence" result: each sequence's K/V live in fixed-size
+ *     physical blocks addressed through a per-sequence block table, and
+ *     attention through the table equals dense attention.
+ *   - lfm25-inference README, "Paged GQA/XQA Decode Attention: zero-allocation
+ *     paged KV caching with Split-K reduction", "--page-size 16", and the
+ *     runtime principles "KV pages are managed by the engine", "temporary
+ *     device memory is reused through bounded pools", "precision and page size
+ *     are startup policies".
+ *
+ * Conventions for every entry point
+ *   - All pointers named *_cache, q, out, k_new, v_new, slot_mapping,
+ *     block_tables, context_lens, q_lens, *_scales, workspace, device_error
+ *     are DEVICE pointers on the current CUDA device.  The caller owns every
+ *     buffer; the library allocates nothing and keeps no state besides cached
+ *     device attributes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; no entry point synchronises
+ *     except pkv_read_device_error.
+ *   - Host-side argument checks run before anything is launched; a non-OK
+ *     status means nothing was enqueued (except PKV_ERR_CUDA, which reports a
+ *     failed launch).
+ *   - Indices the host cannot see (block ids, slots, lengths) are checked on
+ *     the device: an out-of-range value sets a device error word (see
+ *     pkv_read_device_error) and the access is skipped; the kernels never
+ *     trap.  Outputs of such a call are unspecified.
+ *
+ * Cache layout (fixed per cache).  K and V are each
+ *     [num_blocks][num_kv_heads][page]
+ * where a page holds the block_size = 16 tokens of one block for one kv-head,
+ * laid out as 16-byte chunks:
+ *     page = [16 / 8][head_dim / C][8][C],   C = 16 / element bytes
+ * (C = 8 for bf16, 16 for fp8): two groups of 8 tokens; inside a group, one
+ * 16-byte chunk of the head dimension after another; inside a chunk, the 8
+ * tokens of the group, each contributing C consecutive elements.  Element
+ * (token off, dim d) of a page sits at element index
+ *     ((off / 8) * (head_dim / C) + d / C) * 8 * C + (off % 8) * C + d % C.
+ * Each 8x16-byte core block of a page is one contiguous 128-byte unit, so a
+ * page copied to shared memory unchanged is directly a tensor-core operand.
+ * A token slot is  slot = block * 16 + off.
+ *
+ * FP8 cache (kv_dtype = PKV_KV_FP8_E4M3): OCP E4M3 ("fn": bias 7, no
+ * infinities, max finite 448) with one fp32 scale per (block, kv-head) for K
+ * and one for V, k_scales / v_scales = [num_blocks][num_kv_heads].  Stored
+ * code = e4m3_rne_satfinite( (float)x / scale ) (IEEE fp32 division);
+ * dequantised value = code value * scale.  Scales are inputs (the caller
+ * computes them, e.g. absmax / 448 per block).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer */
+    PKV_ERR_UNSUPPORTED = 2,   /* head_dim / block_size / dtype / group size not built */
+    PKV_ERR_WORKSPACE = 3,     /* workspace missing or too small */
+    PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    PKV_ERR_DEVICE_INDEX = 5,  /* device error word: bad block id / slot / length */
+    PKV_ERR_TIMEOUT = 6        /* device error word: a bounded wait gave up */
+} pkv_status;
+
+typedef enum pkv_kv_dtype { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
+
+/* Device error word values (bit flags, OR-ed together by the kernels). */
+#define PKV_DEVERR_BLOCK_ID 1   /* block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_LENGTH 2     /* q_len > context_len, or a negative length */
+#define PKV_DEVERR_SLOT 4       /* slot >= num_blocks * 16 in an append */
+#define PKV_DEVERR_TIMEOUT 8    /* a bounded wait inside a kernel expired */
+
+/* One paged cache ("startup policy": fixed for its lifetime). */
+typedef struct pkv_cache {
+    int64_t num_blocks;        /* physical blocks in the pool */
+    int32_t block_size;        /* must be 16 */
+    int32_t num_kv_heads;      /* Hkv >= 1 */
+    int32_t head_dim;          /* 64 or 128 */
+    int32_t kv_dtype;          /* pkv_kv_dtype */
+    void* k_cache;             /* device, layout above, 16-byte aligned */
+    void* v_cache;
+    const float* k_scales;     /* device [num_blocks][Hkv] fp32; NULL for bf16 */
+    const float* v_scales;
+} pkv_cache;
+
+/*
+ * paged_kv_append -- write one step's new K/V rows into their block slots
+ * (lfm25-inference file list, kernels/kv_cache.cu; scheduler/slots.rs).
+ *
+ *   k_new, v_new   device bf16 [num_tokens][Hkv][head_dim], row-major, 16-byte aligned
+ *   slot_mapping   device int64 [num_tokens]; slot = block * 16 + offset.
+ *                  A negative slot skips the token (padding).  A slot at or beyond
+ *                  num_blocks * 16 is skipped and sets PKV_DEVERR_SLOT.
+ *                  Two tokens with the same slot in one call: undefined.
+ *   device_error   optional device int32 error word (NULL: errors are not reported)
+ *
+ * bf16 cache: the bf16 bits are copied.  FP8 cache: each value is divided by
+ * its (block, kv-head) scale in IEEE fp32 and encoded to E4M3 with round to
+ * nearest even and saturation to +-448 (NaN stays NaN).
+ * num_tokens = 0 is a no-op.
+ */
+PKV_API pkv_status pkv_paged_kv_append(const pkv_cache* cache, const void* k_new, const void* v_new,
+                                       const int64_t* slot_mapping, int64_t num_tokens,
+                                       int32_t* device_error, void* stream);
+
+/*
+ * Workspace for pkv_paged_attention, in bytes.  The workspace holds the
+ * device error word, one merge ticket per (sequence, kv-head) and the split
+ * partial results.  It must be zeroed once before first use
+ * (pkv_workspace_init); the kernels leave it ready for the next call.
+ * num_ctas = 0 means the library's default grid for the current device.
+ */
+PKV_API size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                            int32_t num_kv_heads, int32_t head_dim,
+                                            int32_t max_q_len, int32_t num_ctas);
+
+/* Zero a workspace (cudaMemsetAsync on `stream`). */
+PKV_API pkv_status pkv_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * paged_attention -- decode / causal-verify attention over the paged cache
+ * (lfm25-inference "Paged GQA/XQA Decode Attention ... Split-K reduction";
+ * inferd "paged attention" reference and its equivalence with dense
+ * attention; the verify window of inferd's speculative decoding).
+ *
+ * For sequence b with context length L_b (it counts every resident token,
+ * including the q_lens[b] tokens just appended) and query window Q_b:
+ * query i (0 <= i < Q_b) of query head h attends to positions
+ * j = 0 .. L_b - Q_b + i of kv-head g = h / (Hq / Hkv):
+ *     out = sum_j softmax_j(scale * q . k_j) v_j,
+ * accumulated in fp32 and rounded to bf16 (nearest even).
+ *
+ *   q, out         device bf16 [sum q_lens][Hq][head_dim], packed by sequence
+ *                  (sequence b's rows start at q_lens[0] + ... + q_lens[b-1]).
+ *   block_tables   device int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                  ceil(L_b / 16) are never read.
+ *   context_lens,  device int32 [num_seqs]; 0 <= q_lens[b] <= context_lens[b].
+ *   q_lens
+ *   max_q_len      host-known upper bound of q_lens (1..16), picks the kernel.
+ *   scale          softmax scale (e.g. 1/sqrt(head_dim)).
+ *   num_ctas       grid size (0 = default); it sets how the batch's KV is
+ *                  split, so results of different grids differ by rounding only.
+ *   workspace      device, >= pkv_attention_workspace_size(...) bytes, zeroed
+ *                  once by pkv_workspace_init; not shared by concurrent calls.
+ *
+ * Supported: block_size 16, head_dim 64 or 128, Hq % Hkv == 0,
+ * (Hq / Hkv) * max_q_len <= 32.  Results are deterministic and depend only
+ * on logical positions (not on which physical blocks hold them).
+ */
+PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, int32_t num_q_heads,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, const int32_t* q_lens,
+                                       int32_t num_seqs, int32_t max_q_len, float scale, void* out,
+                                       void* workspace, size_t workspace_bytes, int32_t num_ctas,
+                                       void* stream);
+
+/*
+ * Read and clear a device error word: either the first 4 bytes of an
+ * attention workspace or an append's device_error.  Synchronises `stream`.
+ * *code receives the PKV_DEVERR_* bits; the return value is PKV_OK when no bit
+ * was set, PKV_ERR_TIMEOUT if the timeout bit was set, else
+ * PKV_ERR_DEVICE_INDEX.  For tests and debugging, not the hot path.
+ */
+PKV_API pkv_status pkv_read_device_error(void* error_word, int32_t* code, void* stream);
+
+/* Static description of a status code. */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* Library version string. */
+PKV_API const char* pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,176 @@
+"""ctypes binding of libpagedkv.so (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; this module
+turns torch tensors into device pointers, passes the current CUDA stream and
+raises on a non-OK status.  If the library is missing it raises: there is no
+fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "pagedkv.h")
+
+KV_BF16, KV_FP8_E4M3 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "workspace missing or too small",
+          4: "CUDA error", 5: "device-side index or length error", 6: "device-side wait timed out"}
+DEVERR_BLOCK_ID, DEVERR_LENGTH, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, 'unknown')} (status {status})")
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p)]
+
+
+def lib():
+    """Load libpagedkv.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libpagedkv.so not found at {LIB_PATH}: run "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            L = ctypes.CDLL(LIB_PATH)
+            c = ctypes
+            vp, i32, i64 = c.c_void_p, c.c_int32, c.c_int64
+            L.pkv_paged_kv_append.restype = c.c_int
+            L.pkv_paged_kv_append.argtypes = [c.POINTER(CacheDesc), vp, vp, vp, i64, vp, vp]
+            L.pkv_attention_workspace_size.restype = c.c_size_t
+            L.pkv_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+            L.pkv_workspace_init.restype = c.c_int
+            L.pkv_workspace_init.argtypes = [vp, c.c_size_t, vp]
+            L.pkv_paged_attention.restype = c.c_int
+            L.pkv_paged_attention.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, i32, vp, vp, i32, i32,
+                                              c.c_float, vp, vp, c.c_size_t, i32, vp]
+            L.pkv_read_device_error.restype = c.c_int
+            L.pkv_read_device_error.argtypes = [vp, c.POINTER(i32), vp]
+            L.pkv_status_string.restype = c.c_char_p
+            L.pkv_status_string.argtypes = [c.c_int]
+            L.pkv_version.restype = c.c_char_p
+            L.pkv_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class PagedKVCache:
+    """A paged K/V cache in the library's layout: two device buffers of
+    [num_blocks][num_kv_heads][16 * head_dim] elements (bf16 or e4m3 bytes),
+    plus the per-(block, kv-head) fp32 scales of an FP8 cache."""
+
+    def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, kv_dtype: str = "bf16",
+                 device="cuda", k=None, v=None, k_scales=None, v_scales=None):
+        self.num_blocks, self.num_kv_heads, self.head_dim = num_blocks, num_kv_heads, head_dim
+        self.kv_dtype = kv_dtype
+        tdt = torch.uint8 if kv_dtype == "fp8" else torch.bfloat16
+        shape = (num_blocks, num_kv_heads, 16 * head_dim)
+        self.k = k if k is not None else torch.empty(shape, dtype=tdt, device=device)
+        self.v = v if v is not None else torch.empty(shape, dtype=tdt, device=device)
+        self.k_scales, self.v_scales = k_scales, v_scales
+        if kv_dtype == "fp8" and (k_scales is None or v_scales is None):
+            raise ValueError("an FP8 cache needs k_scales and v_scales")
+
+    def desc(self) -> CacheDesc:
+        for t in (self.k, self.v):
+            if not t.is_contiguous():
+                raise ValueError("cache buffers must be contiguous")
+        for t in (self.k_scales, self.v_scales):
+            if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+                raise ValueError("scales must be contiguous float32")
+        return CacheDesc(self.num_blocks, 16, self.num_kv_heads, self.head_dim,
+                         KV_FP8_E4M3 if self.kv_dtype == "fp8" else KV_BF16,
+                         self.k.data_ptr(), self.v.data_ptr(),
+                         None if self.k_scales is None else self.k_scales.data_ptr(),
+                         None if self.v_scales is None else self.v_scales.data_ptr())
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise PagedKVError(st, what)
+
+
+def append(cache: PagedKVCache, k_new, v_new, slot_mapping, device_error=None, stream=None):
+    """pkv_paged_kv_append: k_new/v_new bf16 [T, Hkv, D], slot_mapping int64 [T]."""
+    for t in (k_new, v_new):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("k_new / v_new must be contiguous bfloat16")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    d = cache.desc()
+    st = lib().pkv_paged_kv_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                   int(slot_mapping.numel()), _ptr(device_error), _stream(stream))
+    _check(st, "pkv_paged_kv_append")
+
+
+def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_q_len, num_ctas=0) -> int:
+    n = lib().pkv_attention_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_q_len, num_ctas)
+    if n == 0:
+        raise PagedKVError(1, "pkv_attention_workspace_size")
+    return int(n)
+
+
+def make_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_q_len, num_ctas=0, device="cuda",
+                   stream=None):
+    n = workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_q_len, num_ctas)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(lib().pkv_workspace_init(_ptr(ws), n, _stream(stream)), "pkv_workspace_init")
+    return ws
+
+
+def attention(cache: PagedKVCache, q, block_tables, context_lens, q_lens, max_q_len: int, scale: float,
+              workspace, out=None, num_ctas: int = 0, stream=None):
+    """pkv_paged_attention: q bf16 [sum q_lens, Hq, D] -> out bf16 of the same shape."""
+    if q.dtype != torch.bfloat16 or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be contiguous bfloat16 [rows, Hq, D]")
+    for t, name in ((block_tables, "block_tables"), (context_lens, "context_lens"), (q_lens, "q_lens")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+    if out is None:
+        out = torch.empty_like(q)
+    d = cache.desc()
+    st = lib().pkv_paged_attention(ctypes.byref(d), _ptr(q), int(q.shape[1]), _ptr(block_tables),
+                                   int(block_tables.shape[1]), _ptr(context_lens), _ptr(q_lens),
+                                   int(context_lens.numel()), int(max_q_len), float(scale), _ptr(out),
+                                   _ptr(workspace), int(workspace.numel()), int(num_ctas), _stream(stream))
+    _check(st, "pkv_paged_attention")
+    return out
+
+
+def read_device_error(error_word, stream=None) -> int:
+    """Read and clear a device error word (workspace or append flag); syncs."""
+    code = ctypes.c_int32(0)
+    st = lib().pkv_read_device_error(_ptr(error_word), ctypes.byref(code), _stream(stream))
+    if st not in (0, 5, 6):
+        _check(st, "pkv_read_device_error")
+    return int(code.value)
+
+
+def version() -> str:
+    return lib().pkv_version().decode()

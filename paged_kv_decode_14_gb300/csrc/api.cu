@@ -1,0 +1,167 @@
+// C ABI of libpagedkv: argument checks, grid planning and kernel dispatch.
+// Declarations and contracts: include/pagedkv.h.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace pkv {
+cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_new, const int64_t* slots,
+                          int64_t num_tokens, int* err, cudaStream_t st, int num_sms);
+cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
+int simt_rows_pad(int rows);
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_num_sms[kMaxDevices] = {0};
+std::mutex g_mu;
+
+int num_sms_current() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_num_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_num_sms[dev] = n;
+    }
+    return g_num_sms[dev];
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+pkv_status check_cache(const pkv_cache* c) {
+    if (!c || !c->k_cache || !c->v_cache) return PKV_ERR_INVALID_ARG;
+    if (c->num_blocks <= 0 || c->num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
+    if (c->block_size != kBlock) return PKV_ERR_UNSUPPORTED;
+    if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+    if (c->kv_dtype == PKV_KV_FP8_E4M3 && (!c->k_scales || !c->v_scales)) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(c->k_cache) || !aligned16(c->v_cache)) return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
+// Grid of the attention kernel: a persistent set of CTAs, 4 per SM.
+int default_ctas(int num_sms) { return num_sms > 0 ? num_sms * 4 : 0; }
+
+int rows_pad_for(int group, int max_q_len) { return simt_rows_pad(group * max_q_len); }
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+PKV_API const char* pkv_version(void) { return "pagedkv 0.1 (sm_103a)"; }
+
+PKV_API const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_CUDA: return "CUDA error";
+        case PKV_ERR_DEVICE_INDEX: return "device-side index or length error";
+        case PKV_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+PKV_API pkv_status pkv_paged_kv_append(const pkv_cache* cache, const void* k_new, const void* v_new,
+                                       const int64_t* slot_mapping, int64_t num_tokens, int32_t* device_error,
+                                       void* stream) {
+    pkv_status s = check_cache(cache);
+    if (s != PKV_OK) return s;
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    cudaError_t e = launch_append(*cache, k_new, v_new, slot_mapping, num_tokens, device_error,
+                                  (cudaStream_t)stream, sms);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+PKV_API size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                            int32_t head_dim, int32_t max_q_len, int32_t num_ctas) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+    if (head_dim <= 0 || max_q_len < 1) return 0;
+    if (num_ctas <= 0) num_ctas = default_ctas(num_sms_current());
+    if (num_ctas <= 0) return 0;
+    const int rows_pad = rows_pad_for(num_q_heads / num_kv_heads, max_q_len);
+    return workspace_layout(num_seqs, num_kv_heads, head_dim, rows_pad, num_ctas).total;
+}
+
+PKV_API pkv_status pkv_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || workspace_bytes < 256) return PKV_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream) == cudaSuccess ? PKV_OK
+                                                                                              : PKV_ERR_CUDA;
+}
+
+PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, int32_t num_q_heads,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, const int32_t* q_lens, int32_t num_seqs,
+                                       int32_t max_q_len, float scale, void* out, void* workspace,
+                                       size_t workspace_bytes, int32_t num_ctas, void* stream) {
+    pkv_status s = check_cache(cache);
+    if (s != PKV_OK) return s;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !out || !block_tables || !context_lens || !q_lens || !workspace) return PKV_ERR_INVALID_ARG;
+    if (max_blocks_per_seq <= 0 || max_q_len < 1) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+    const int group = num_q_heads / cache->num_kv_heads;
+    if (max_q_len > 16 || group * max_q_len > 32) return PKV_ERR_UNSUPPORTED;
+    if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    if (num_ctas < 0) return PKV_ERR_INVALID_ARG;
+    const int ncta = num_ctas > 0 ? num_ctas : default_ctas(sms);
+    const int rows_pad = rows_pad_for(group, max_q_len);
+    const WorkspaceLayout wl = workspace_layout(num_seqs, cache->num_kv_heads, cache->head_dim, rows_pad, ncta);
+    if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
+
+    AttnParams p;
+    p.k_cache = (const uint8_t*)cache->k_cache;
+    p.v_cache = (const uint8_t*)cache->v_cache;
+    p.k_scales = cache->k_scales;
+    p.v_scales = cache->v_scales;
+    p.q = (const __nv_bfloat16*)q;
+    p.out = (__nv_bfloat16*)out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.q_lens = q_lens;
+    p.err = (int*)workspace;
+    p.tickets = (int*)((uint8_t*)workspace + wl.tickets_off);
+    p.partials = (float*)((uint8_t*)workspace + wl.partials_off);
+    p.num_blocks = cache->num_blocks;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.group = group;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_q_len = max_q_len;
+    p.rows = group * max_q_len;
+    p.rows_pad = rows_pad;
+    p.slot_floats = (int)wl.slot_floats;
+    p.scale_log2 = scale * kLog2e;
+    const int E = cache->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
+    cudaError_t e = launch_attention_simt(p, cache->head_dim, E, ncta, (cudaStream_t)stream);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+PKV_API pkv_status pkv_read_device_error(void* error_word, int32_t* code, void* stream) {
+    if (!error_word || !code) return PKV_ERR_INVALID_ARG;
+    int32_t h = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&h, error_word, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemsetAsync(error_word, 0, sizeof(h), st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PKV_ERR_CUDA;
+    *code = h;
+    if (h == 0) return PKV_OK;
+    return (h & PKV_DEVERR_TIMEOUT) ? PKV_ERR_TIMEOUT : PKV_ERR_DEVICE_INDEX;
+}
+
+}  // extern "C"

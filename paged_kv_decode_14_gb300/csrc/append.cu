@@ -1,0 +1,86 @@
+// paged_kv_append: write one step's new K/V rows into their cache slots
+// (lfm25-inference file list: kernels/kv_cache.cu, scheduler/slots.rs).
+//
+// One thread per (token, kv-head, 16-byte cache chunk, K|V).  For a bf16
+// cache the chunk is 8 bf16 values copied as one 16-byte store; for an FP8
+// cache it is 16 values, each divided by its (block, kv-head) scale in IEEE
+// fp32 (round to nearest) and converted by CUDA's E4M3 conversion with
+// round-to-nearest-even and saturation to +-448.
+#include "common.cuh"
+
+namespace pkv {
+
+template <int E>
+__global__ void __launch_bounds__(256) append_kernel(const uint8_t* __restrict__ k_new, const uint8_t* __restrict__ v_new,
+                                                     const int64_t* __restrict__ slots, int64_t num_tokens, int Hkv,
+                                                     int D, int64_t num_blocks, uint8_t* k_cache, uint8_t* v_cache,
+                                                     const float* __restrict__ k_scales,
+                                                     const float* __restrict__ v_scales, int* err) {
+    const int NCH = D * E / 16;                  // 16-byte chunks per token row in the cache
+    const int64_t per_tok = (int64_t)Hkv * NCH * 2;
+    const int64_t total = num_tokens * per_tok;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = idx / per_tok;
+        int rem = (int)(idx % per_tok);
+        const int which = rem & 1;               // 0 = K, 1 = V
+        rem >>= 1;
+        const int g = rem / NCH, ch = rem % NCH;
+        const int64_t s = slots[t];
+        if (s < 0) continue;
+        const int64_t blk = s / kBlock;
+        const int off = (int)(s % kBlock);
+        if (blk >= num_blocks) {
+            if (which == 0 && g == 0 && ch == 0) raise_error(err, PKV_DEVERR_SLOT);
+            continue;
+        }
+        const uint8_t* src = (which ? v_new : k_new) + (((size_t)t * Hkv + g) * D) * 2;
+        uint8_t* page = (which ? v_cache : k_cache) + ((size_t)blk * Hkv + g) * (size_t)(kBlock * D * E);
+        uint4* dst = reinterpret_cast<uint4*>(page + ((off >> 3) * NCH + ch) * 128 + (off & 7) * 16);
+        if constexpr (E == 2) {
+            *dst = __ldg(reinterpret_cast<const uint4*>(src + ch * 16));
+        } else {
+            const float sc = (which ? v_scales : k_scales)[(size_t)blk * Hkv + g];
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(src + ch * 32));
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(src + ch * 32 + 16));
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t packed[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t x = w[2 * j + h];
+                    const float lo = __fdiv_rn(bf16_lo(x), sc), hi = __fdiv_rn(bf16_hi(x), sc);
+                    const uint32_t c0 = __nv_cvt_float_to_fp8(lo, __NV_SATFINITE, __NV_E4M3);
+                    const uint32_t c1 = __nv_cvt_float_to_fp8(hi, __NV_SATFINITE, __NV_E4M3);
+                    word |= (c0 | (c1 << 8)) << (16 * h);
+                }
+                packed[j] = word;
+            }
+            *dst = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+    }
+}
+
+cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_new, const int64_t* slots,
+                          int64_t num_tokens, int* err, cudaStream_t st, int num_sms) {
+    const int E = c.kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
+    const int64_t total = num_tokens * c.num_kv_heads * (c.head_dim * E / 16) * 2;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (E == 2)
+        append_kernel<2><<<(unsigned)blocks, threads, 0, st>>>(
+            (const uint8_t*)k_new, (const uint8_t*)v_new, slots, num_tokens, c.num_kv_heads, c.head_dim,
+            c.num_blocks, (uint8_t*)c.k_cache, (uint8_t*)c.v_cache, nullptr, nullptr, err);
+    else
+        append_kernel<1><<<(unsigned)blocks, threads, 0, st>>>(
+            (const uint8_t*)k_new, (const uint8_t*)v_new, slots, num_tokens, c.num_kv_heads, c.head_dim,
+            c.num_blocks, (uint8_t*)c.k_cache, (uint8_t*)c.v_cache, c.k_scales, c.v_scales, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,264 @@
+// Shared device helpers of libpagedkv: number formats, the balanced work
+// partition over (sequence, kv-head, page) units and the split merge.
+//
+// Work partition ("Split-K" of the lfm25-inference README's paged GQA/XQA
+// decode attention, restated for a persistent grid).  Every (sequence b,
+// kv-head g) pair is a segment of ceil(L_b / 16) page units; segments are
+// laid end to end in (b, g) order and the W units are cut into P equal
+// ranges, one per CTA: CTA c owns units [floor(c W / P), floor((c+1) W / P)).
+// A segment that falls inside one CTA is finished there; a segment cut by a
+// range boundary leaves one partial (m, l, acc) per CTA it touches, and the
+// CTA that finishes last (a ticket per segment, no waiting) merges them in
+// CTA order.  The cut depends on lengths only, never on physical block ids.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pkv {
+
+constexpr int kBlock = 16;                 // tokens per page (block_size)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------ formats
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two E4M3 codes (low byte = first element) -> two floats, exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
+    __half2 hh = *reinterpret_cast<__half2*>(&h);
+    return __half22float2(hh);
+}
+
+__device__ __forceinline__ void raise_error(int* err, int bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// ------------------------------------------------------------------ workspace
+
+struct WorkspaceLayout {
+    size_t tickets_off;     // int32 [num_seqs * Hkv]
+    size_t partials_off;    // float [num_ctas][2][slot_floats]
+    size_t slot_floats;     // rows_pad * (head_dim + 2)
+    size_t total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ inline WorkspaceLayout workspace_layout(int num_seqs, int num_kv_heads, int head_dim,
+                                                 int rows_pad, int num_ctas) {
+    WorkspaceLayout w;
+    w.tickets_off = 256;
+    w.partials_off = align_up(w.tickets_off + sizeof(int32_t) * (size_t)num_seqs * num_kv_heads, 256);
+    w.slot_floats = (size_t)rows_pad * (head_dim + 2);
+    w.total = w.partials_off + sizeof(float) * w.slot_floats * 2 * (size_t)num_ctas;
+    return w;
+}
+
+// ------------------------------------------------------------------ parameters
+
+struct AttnParams {
+    const uint8_t* k_cache;
+    const uint8_t* v_cache;
+    const float* k_scales;
+    const float* v_scales;
+    const __nv_bfloat16* q;
+    __nv_bfloat16* out;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* q_lens;
+    int* err;                  // workspace error word
+    int* tickets;              // workspace tickets
+    float* partials;           // workspace partial slots
+    int64_t num_blocks;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                 // Hq / Hkv
+    int max_blocks_per_seq;
+    int max_q_len;             // host bound on q_lens
+    int rows;                  // group * max_q_len (rows of the widest segment)
+    int rows_pad;              // slot row capacity
+    int slot_floats;
+    float scale_log2;          // scale * log2(e)
+};
+
+// ------------------------------------------------------------------ planning
+
+// Units (pages x kv-heads) of sequence b; sequences with no query rows or
+// invalid lengths (Q > L, Q above the launch's max_q_len, more pages than a
+// block-table row holds) contribute none.
+__device__ __forceinline__ bool seq_valid(const AttnParams& p, int L, int Q) {
+    return Q > 0 && Q <= L && Q <= p.max_q_len && (L + kBlock - 1) / kBlock <= p.max_blocks_per_seq;
+}
+__device__ __forceinline__ int seq_units(const AttnParams& p, int L, int Q) {
+    return seq_valid(p, L, Q) ? ((L + kBlock - 1) / kBlock) * p.num_kv_heads : 0;
+}
+// q rows of sequence b in the packed q / out tensors.
+__device__ __forceinline__ int seq_qrows(int Q) { return Q > 0 ? Q : 0; }
+
+struct Cursor {
+    int b;          // current sequence
+    int Ub;         // units before sequence b
+    int qoff;       // first q row of sequence b
+    int L, Q, nb;   // its context length, query length, pages
+};
+
+// Block-wide inclusive scan of one int per thread (NT threads, NT % 32 == 0).
+template <int NT>
+__device__ __forceinline__ int block_scan_incl(int v, int* scratch /* NT/32 + 1 ints */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) scratch[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < NT / 32 ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        if (lane < NT / 32) scratch[lane] = w;
+    }
+    __syncthreads();
+    int add = warp > 0 ? scratch[warp - 1] : 0;
+    int total = scratch[NT / 32 - 1];
+    __syncthreads();
+    scratch[NT / 32] = total;
+    return v + add;
+}
+
+// Computes W (total units) and positions a cursor at the sequence holding
+// unit u0 of this CTA.  All NT threads must call it.  CTA 0 reports invalid
+// lengths.  Returns false when the CTA has no work.
+template <int NT>
+__device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch, Cursor* cur,
+                            int* u0_out, int* u1_out, int* W_out) {
+    const int tid = threadIdx.x;
+    // pass 1: total units
+    int total = 0;
+    for (int base = 0; base < p.num_seqs; base += NT) {
+        int b = base + tid;
+        int u = 0;
+        if (b < p.num_seqs) {
+            int L = p.context_lens[b], Q = p.q_lens[b];
+            if (cta == 0 && Q != 0 && !seq_valid(p, L, Q)) raise_error(p.err, PKV_DEVERR_LENGTH);
+            u = seq_units(p, L, Q);
+        }
+        block_scan_incl<NT>(u, scratch);
+        total += scratch[NT / 32];
+        __syncthreads();
+    }
+    const int W = total;
+    const int u0 = (int)(((int64_t)cta * W) / ncta);
+    const int u1 = (int)(((int64_t)(cta + 1) * W) / ncta);
+    *u0_out = u0;
+    *u1_out = u1;
+    *W_out = W;
+    if (u0 >= u1) return false;
+    // pass 2: find b with Ub <= u0 < Ub + units(b), and its q offset
+    __shared__ Cursor s_cur;
+    int run_u = 0, run_q = 0;
+    for (int base = 0; base < p.num_seqs; base += NT) {
+        int b = base + tid;
+        int u = 0, q = 0, L = 0, Q = 0;
+        if (b < p.num_seqs) {
+            L = p.context_lens[b];
+            Q = p.q_lens[b];
+            u = seq_units(p, L, Q);
+            q = seq_qrows(Q);
+        }
+        int iu = block_scan_incl<NT>(u, scratch);
+        int tot_u = scratch[NT / 32];
+        __syncthreads();
+        int iq = block_scan_incl<NT>(q, scratch);
+        int tot_q = scratch[NT / 32];
+        __syncthreads();
+        int Ub = run_u + iu - u;
+        if (b < p.num_seqs && u > 0 && Ub <= u0 && u0 < Ub + u) {
+            s_cur.b = b;
+            s_cur.Ub = Ub;
+            s_cur.qoff = run_q + iq - q;
+            s_cur.L = L;
+            s_cur.Q = Q;
+            s_cur.nb = (L + kBlock - 1) / kBlock;
+        }
+        run_u += tot_u;
+        run_q += tot_q;
+    }
+    __syncthreads();
+    *cur = s_cur;
+    return true;
+}
+
+// Advance the cursor to the next sequence with work (all threads, same values).
+__device__ __forceinline__ void cursor_next(const AttnParams& p, Cursor& c) {
+    c.Ub += c.nb * p.num_kv_heads;
+    c.qoff += seq_qrows(c.Q);
+    for (;;) {
+        c.b += 1;
+        if (c.b >= p.num_seqs) return;
+        c.L = p.context_lens[c.b];
+        c.Q = p.q_lens[c.b];
+        if (seq_units(p, c.L, c.Q) > 0) {
+            c.nb = (c.L + kBlock - 1) / kBlock;
+            return;
+        }
+        c.qoff += seq_qrows(c.Q);       // skipped sequence: its rows stay packed in q / out
+    }
+}
+
+// CTA owning unit u under the partition above.
+__device__ __forceinline__ int owner_cta(int u, int W, int ncta) {
+    return (int)((((int64_t)u + 1) * ncta - 1) / W);
+}
+
+// Partial slot of a piece: 0 if its segment started before this CTA's range,
+// else 1 (the segment starts here and continues in the next CTA).
+__device__ __forceinline__ float* slot_ptr(const AttnParams& p, int cta, int seg_start, int u0) {
+    int k = seg_start < u0 ? 0 : 1;
+    return p.partials + ((size_t)cta * 2 + k) * (size_t)p.slot_floats;
+}
+
+// Merge the partials of segment [S0, S1) (all rows of (b, g)) into out.
+// Called by every thread of the CTA that drew the last ticket.
+template <int NT>
+__device__ void merge_segment(const AttnParams& p, const Cursor& c, int g, int S0, int S1, int W,
+                              int ncta, int D) {
+    const int c_first = owner_cta(S0, W, ncta), c_last = owner_cta(S1 - 1, W, ncta);
+    const int R = p.group * c.Q;
+    for (int idx = threadIdx.x; idx < R * D; idx += NT) {
+        const int r = idx / D, d = idx % D;
+        float M = -INFINITY;
+        for (int cc = c_first; cc <= c_last; ++cc) {
+            const int u0c = (int)(((int64_t)cc * W) / ncta);
+            const float* s = slot_ptr(p, cc, S0, u0c);
+            M = fmaxf(M, __ldcg(s + r));
+        }
+        float den = 0.f, num = 0.f;
+        for (int cc = c_first; cc <= c_last; ++cc) {
+            const int u0c = (int)(((int64_t)cc * W) / ncta);
+            const float* s = slot_ptr(p, cc, S0, u0c);
+            const float m = __ldcg(s + r);
+            const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+            den += w * __ldcg(s + p.rows_pad + r);
+            num += w * __ldcg(s + 2 * p.rows_pad + (size_t)r * D + d);
+        }
+        const int i = r / p.group, hl = r % p.group;
+        const size_t o = ((size_t)(c.qoff + i) * p.num_q_heads + g * p.group + hl) * D + d;
+        p.out[o] = __float2bfloat16_rn(num / den);
+    }
+}
+
+}  // namespace pkv

@@ -1,0 +1,90 @@
+"""Device-side driver for one workload: upload, build the cache by append,
+run decode steps.  Used by the tests, the smoke check and the benchmark."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _native as nat
+from .workloads import BF16_NAN, FP8_NAN, Workload
+
+
+def _bf16_tensor(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+class DeviceWorkload:
+    """Holds a workload's tensors on the GPU.  The cache starts filled with the
+    NaN sentinel, so a read of an unwritten slot shows up as NaN."""
+
+    def __init__(self, w: Workload, device="cuda", num_ctas: int = 0):
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        self.q = _bf16_tensor(w.q, dev)
+        self.k_new = _bf16_tensor(w.k_new, dev)
+        self.v_new = _bf16_tensor(w.v_new, dev)
+        self.slots = torch.from_numpy(w.slots).to(dev)
+        self.block_tables = torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(dev)
+        self.context_lens = torch.from_numpy(w.context_lens).to(dev)
+        self.q_lens = torch.from_numpy(w.q_lens).to(dev)
+        ks = vs = None
+        if w.kv_dtype == "fp8":
+            ks = torch.from_numpy(w.k_scales).to(dev)
+            vs = torch.from_numpy(w.v_scales).to(dev)
+        self.cache = nat.PagedKVCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.kv_dtype, device=dev,
+                                      k_scales=ks, v_scales=vs)
+        self.reset_cache()
+        self.num_ctas = num_ctas
+        self.workspace = nat.make_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                            max(1, w.max_q_len), num_ctas, device=dev)
+        self.append_err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.q)
+
+    def reset_cache(self):
+        if self.w.kv_dtype == "fp8":
+            self.cache.k.fill_(int(FP8_NAN))
+            self.cache.v.fill_(int(FP8_NAN))
+        else:
+            self.cache.k.view(torch.int16).fill_(int(np.int16(BF16_NAN.view(np.int16))))
+            self.cache.v.view(torch.int16).fill_(int(np.int16(BF16_NAN.view(np.int16))))
+
+    def prefill(self, chunk_tokens: int = 1 << 16):
+        """Append the workload's resident tokens (the state before the step)."""
+        w = self.w
+        n = int(w.prefill_slots.shape[0])
+        for s in range(0, n, chunk_tokens):
+            e = min(n, s + chunk_tokens)
+            k = _bf16_tensor(w.prefill_k[s:e], self.device)
+            v = _bf16_tensor(w.prefill_v[s:e], self.device)
+            sl = torch.from_numpy(w.prefill_slots[s:e]).to(self.device)
+            nat.append(self.cache, k, v, sl, device_error=self.append_err)
+
+    def append_step(self, stream=None):
+        nat.append(self.cache, self.k_new, self.v_new, self.slots, device_error=self.append_err, stream=stream)
+
+    def attend(self, out=None, num_ctas=None, stream=None, workspace=None):
+        w = self.w
+        return nat.attention(self.cache, self.q, self.block_tables, self.context_lens, self.q_lens,
+                             max(1, w.max_q_len), w.scale, workspace if workspace is not None else self.workspace,
+                             out=self.out if out is None else out,
+                             num_ctas=self.num_ctas if num_ctas is None else num_ctas, stream=stream)
+
+    def step(self, stream=None):
+        """One decode step: append the new tokens, then attend."""
+        self.append_step(stream)
+        return self.attend(stream=stream)
+
+    def cache_bytes(self):
+        """(K, V) cache contents as numpy arrays in the library layout."""
+        k = self.cache.k.view(torch.uint8) if self.w.kv_dtype == "fp8" else self.cache.k.view(torch.int16)
+        v = self.cache.v.view(torch.uint8) if self.w.kv_dtype == "fp8" else self.cache.v.view(torch.int16)
+        k, v = k.cpu().numpy().reshape(-1), v.cpu().numpy().reshape(-1)
+        if self.w.kv_dtype != "fp8":
+            k, v = k.view(np.uint16), v.view(np.uint16)
+        return k, v
+
+    def errors(self):
+        """(attention workspace error bits, append error bits); clears both."""
+        return nat.read_device_error(self.workspace), nat.read_device_error(self.append_err)
