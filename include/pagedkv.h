@@ -145,7 +145,8 @@ PKV_API pkv_status pkv_workspace_init(void* workspace, size_t workspace_bytes, v
  *     out = sum_j softmax_j(scale * q . k_j) v_j,
  * accumulated in fp32 and rounded to bf16 (nearest even).
  *
- *   q, out         device bf16 [sum q_lens][Hq][head_dim], packed by sequence
+ *   q, out         device bf16 [sum q_lens][Hq][head_dim], packed by sequence; they must hold
+ *                  sum(q_lens) rows (the kernels trust this size)
  *                  (sequence b's rows start at q_lens[0] + ... + q_lens[b-1]).
  *   block_tables   device int32 [num_seqs][max_blocks_per_seq]; entries past
  *                  ceil(L_b / 16) are never read.

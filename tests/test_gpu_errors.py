@@ -69,7 +69,7 @@ def test_q_len_above_context_len_sets_error_word():
     dw = DeviceWorkload(w)
     dw.prefill()
     dw.append_step()
-    dw.q_lens[0] = 45      # > context_lens[0] = 40
+    dw.context_lens[1] = 1     # q_lens[1] = 2 > context_lens[1]; q stays packed as before
     dw.attend()
     assert dw.errors()[0] & nat.DEVERR_LENGTH
 
