@@ -104,10 +104,11 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
     __shared__ int s_ticket;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cta = blockIdx.x, ncta = gridDim.x;
+    const int cta = blockIdx.x;
     Cursor cur;
-    int u0, u1, W;
-    if (!plan_locate<kThreads>(p, cta, ncta, scratch, &cur, &u0, &u1, &W)) return;
+    int u0, u1, W, P;
+    if (!plan_locate<kThreads>(p, cta, gridDim.x, scratch, &cur, &u0, &u1, &W, &P)) return;
+    const int ncta = P;
 
     float* qs = reinterpret_cast<float*>(smem + K::OFF_Q);
     float* pb = reinterpret_cast<float*>(smem + K::OFF_P) + warp * RT * 16;

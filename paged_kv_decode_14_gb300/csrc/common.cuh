@@ -139,12 +139,12 @@ __device__ __forceinline__ int block_scan_incl(int v, int* scratch /* NT/32 + 1 
     return v + add;
 }
 
-// Computes W (total units) and positions a cursor at the sequence holding
-// unit u0 of this CTA.  All NT threads must call it.  CTA 0 reports invalid
+// Computes W (total units) and the number P = min(grid, W) of CTAs that take
+// part, and positions a cursor at the sequence holding unit u0 of this CTA.  All NT threads must call it.  CTA 0 reports invalid
 // lengths.  Returns false when the CTA has no work.
 template <int NT>
 __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch, Cursor* cur,
-                            int* u0_out, int* u1_out, int* W_out) {
+                            int* u0_out, int* u1_out, int* W_out, int* P_out) {
     const int tid = threadIdx.x;
     // pass 1: total units
     int total = 0;
@@ -161,12 +161,16 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         __syncthreads();
     }
     const int W = total;
-    const int u0 = (int)(((int64_t)cta * W) / ncta);
-    const int u1 = (int)(((int64_t)(cta + 1) * W) / ncta);
+    // With more CTAs than units, only the first W CTAs take part, so that every
+    // participating CTA owns at least one unit.
+    const int P = min(ncta, W);
+    *W_out = W;
+    *P_out = P;
+    if (cta >= P) return false;
+    const int u0 = (int)(((int64_t)cta * W) / P);
+    const int u1 = (int)(((int64_t)(cta + 1) * W) / P);
     *u0_out = u0;
     *u1_out = u1;
-    *W_out = W;
-    if (u0 >= u1) return false;
     // pass 2: find b with Ub <= u0 < Ub + units(b), and its q offset
     __shared__ Cursor s_cur;
     int run_u = 0, run_q = 0;
@@ -219,7 +223,8 @@ __device__ __forceinline__ void cursor_next(const AttnParams& p, Cursor& c) {
     }
 }
 
-// CTA owning unit u under the partition above.
+// CTA owning unit u under the partition above (P = participating CTAs <= W,
+// so every CTA in [owner(S0), owner(S1 - 1)] holds a piece of [S0, S1)).
 __device__ __forceinline__ int owner_cta(int u, int W, int ncta) {
     return (int)((((int64_t)u + 1) * ncta - 1) / W);
 }

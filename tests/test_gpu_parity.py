@@ -60,7 +60,7 @@ SWEEP = [
     # (D, Hq, Hkv, lens, q_lens, dtype)
     (64, 8, 2, [1, 15, 16, 17, 31, 32, 33, 100], [1] * 8, "bf16"),
     (128, 8, 8, [1, 15, 16, 17, 64, 257], [1] * 6, "bf16"),
-    (128, 16, 2, [5, 40, 77, 300], [5, 3, 8, 2], "bf16"),
+    (128, 8, 2, [5, 40, 77, 300], [5, 3, 8, 2], "bf16"),
     (64, 4, 4, [9, 10, 11], [8, 4, 2], "bf16"),
     (128, 32, 8, [600, 3, 1200], [1, 1, 1], "fp8"),
     (64, 8, 1, [33, 17, 129], [4, 1, 2], "fp8"),
