@@ -171,6 +171,39 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
                                        void* stream);
 
 /*
+ * pkv_paged_attention_noalloc -- pkv_paged_attention for callers that cannot
+ * allocate device memory (the pages have no counterpart of this entry point).
+ *
+ * Some callers own no device allocator: a plugin or foreign-language host
+ * that can only pass the tensors it already holds, or a serving loop whose
+ * device memory budget is fixed at start-up and must not grow on the decode
+ * path.  They cannot supply the attention workspace, so this variant keeps it
+ * in a static device array of PKV_NOALLOC_SCRATCH_BYTES inside the library
+ * (every GPU that loads the library holds that array until the process
+ * exits).  The caller still passes all inputs and outputs; the arguments mean
+ * what they mean for pkv_paged_attention.  It allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library call.
+ *
+ *   device_error   optional device int32 error word that receives the
+ *                  PKV_DEVERR_* bits (NULL: errors are not reported).
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current and caches it; make that first call before any stream
+ * capture.  Each call clears the array's error word and merge tickets on
+ * `stream` before launching.  All calls share the one array and it keeps the
+ * last call's contents, so calls whose kernels overlap on the GPU (other
+ * streams or other host threads on the same device) race: serialise them.
+ * A call whose workspace would exceed PKV_NOALLOC_SCRATCH_BYTES (too many
+ * sequences or CTAs) returns PKV_ERR_WORKSPACE and launches nothing.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+PKV_API pkv_status pkv_paged_attention_noalloc(const pkv_cache* cache, const void* q, int32_t num_q_heads,
+                                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t* context_lens, const int32_t* q_lens,
+                                               int32_t num_seqs, int32_t max_q_len, float scale, void* out,
+                                               int32_t num_ctas, int32_t* device_error, void* stream);
+
+/*
  * Read and clear a device error word: either the first 4 bytes of an
  * attention workspace or an append's device_error.  Synchronises `stream`.
  * *code receives the PKV_DEVERR_* bits; the return value is PKV_OK when no bit

@@ -60,6 +60,9 @@ def lib():
             L.pkv_paged_attention.restype = c.c_int
             L.pkv_paged_attention.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, i32, vp, vp, i32, i32,
                                               c.c_float, vp, vp, c.c_size_t, i32, vp]
+            L.pkv_paged_attention_noalloc.restype = c.c_int
+            L.pkv_paged_attention_noalloc.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, i32, vp, vp, i32, i32,
+                                                      c.c_float, vp, i32, vp, vp]
             L.pkv_read_device_error.restype = c.c_int
             L.pkv_read_device_error.argtypes = [vp, c.POINTER(i32), vp]
             L.pkv_status_string.restype = c.c_char_p
@@ -160,6 +163,27 @@ def attention(cache: PagedKVCache, q, block_tables, context_lens, q_lens, max_q_
                                    int(context_lens.numel()), int(max_q_len), float(scale), _ptr(out),
                                    _ptr(workspace), int(workspace.numel()), int(num_ctas), _stream(stream))
     _check(st, "pkv_paged_attention")
+    return out
+
+
+def attention_noalloc(cache: PagedKVCache, q, block_tables, context_lens, q_lens, max_q_len: int, scale: float,
+                      out=None, num_ctas: int = 0, device_error=None, stream=None):
+    """pkv_paged_attention_noalloc: like attention(), with the library's static
+    scratch array instead of a caller workspace (for callers that cannot
+    allocate device memory).  Calls that overlap on the GPU race."""
+    if q.dtype != torch.bfloat16 or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be contiguous bfloat16 [rows, Hq, D]")
+    for t, name in ((block_tables, "block_tables"), (context_lens, "context_lens"), (q_lens, "q_lens")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+    if out is None:
+        out = torch.empty_like(q)
+    d = cache.desc()
+    st = lib().pkv_paged_attention_noalloc(ctypes.byref(d), _ptr(q), int(q.shape[1]), _ptr(block_tables),
+                                           int(block_tables.shape[1]), _ptr(context_lens), _ptr(q_lens),
+                                           int(context_lens.numel()), int(max_q_len), float(scale), _ptr(out),
+                                           int(num_ctas), _ptr(device_error), _stream(stream))
+    _check(st, "pkv_paged_attention_noalloc")
     return out
 
 

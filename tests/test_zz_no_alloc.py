@@ -1,0 +1,61 @@
+"""pkv_paged_attention_noalloc: the attention entry point for callers that
+cannot allocate device memory (a host that can only pass the tensors it
+already holds, or a serving loop with a device budget fixed at start-up).  It
+keeps its scratch in the library's static device array instead of a
+caller-provided workspace.
+
+Checked through the C ABI against pkv_paged_attention (the entry point with a
+caller workspace), with the tolerance of the other parity tests, on two calls
+in a row: the second call reuses the array the first one left behind.  The
+file sorts last so that a run stopping at the first failure has already run
+every other test; it also passes alone in a fresh process."""
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_decode_14_gb300 import _native as nat
+from paged_kv_decode_14_gb300 import workloads as wl
+from paged_kv_decode_14_gb300.runner import DeviceWorkload
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def _f64(t):
+    return wl.bf16_to_f32(t.view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+
+
+@pytest.mark.parametrize("which", ["decode", "verify"])
+def test_noalloc_matches_workspace_entry_two_calls(which):
+    if which == "decode":
+        w = wl.decode_b32_d128()
+    else:
+        w = wl.make_workload("v", context_lens=[700, 45, 2100, 16], q_lens=[5, 5, 3, 1], num_q_heads=32,
+                             num_kv_heads=8, head_dim=128, seed=91)
+    dw = DeviceWorkload(w)
+    dw.prefill()
+    dw.append_step()
+    ref = dw.attend().clone()
+    torch.cuda.synchronize()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for call in range(2):
+        out = torch.full_like(dw.q, float("nan"))
+        nat.attention_noalloc(dw.cache, dw.q, dw.block_tables, dw.context_lens, dw.q_lens, max(1, w.max_q_len),
+                              w.scale, out=out, device_error=err)
+        torch.cuda.synchronize()
+        a, b = _f64(out), _f64(ref)
+        assert not np.isnan(a).any(), f"call {call}: NaN in output"
+        assert np.all(np.abs(a - b) <= ATOL + RTOL * np.abs(b)), f"call {call}: max err {np.abs(a - b).max()}"
+        assert nat.read_device_error(err) == 0
+
+
+def test_noalloc_rejects_sizes_beyond_its_array():
+    w = wl.tiny_decode()
+    dw = DeviceWorkload(w)
+    with pytest.raises(nat.PagedKVError) as e:
+        # a grid this large needs far more partial slots than the static array holds
+        nat.attention_noalloc(dw.cache, dw.q, dw.block_tables, dw.context_lens, dw.q_lens, 1, w.scale,
+                              num_ctas=1 << 20)
+    assert e.value.status == 3
