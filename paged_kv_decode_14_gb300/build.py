@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "api_noalloc.cu", "append.cu", "attn_simt.cu"]
+SOURCES = ["api.cu", "api_noalloc.cu", "append.cu", "attn_simt.cu", "attn_tc.cu"]
 
 
 def nvcc() -> str:

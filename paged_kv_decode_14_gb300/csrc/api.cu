@@ -8,7 +8,20 @@ namespace pkv {
 cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_new, const int64_t* slots,
                           int64_t num_tokens, int* err, cudaStream_t st, int num_sms);
 cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
+cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, int ncta, cudaStream_t st);
 int simt_rows_pad(int rows);
+
+// Kernel choice: the tensor-core kernel for bf16 caches (R = G * max_q_len <= 32),
+// the CUDA-core kernel for FP8 caches.
+bool attention_uses_tc(const pkv_cache* c, int rows) { return c->kv_dtype == PKV_KV_BF16 && rows <= 32; }
+
+// Default grid: one persistent CTA per SM for the tensor-core kernel (it
+// holds ~200 KiB of shared memory), four per SM for the CUDA-core kernel.
+int attention_default_ctas(bool tc, int num_sms) { return num_sms > 0 ? (tc ? num_sms : 4 * num_sms) : 0; }
+
+cudaError_t launch_attention(bool tc, const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st) {
+    return tc ? launch_attention_tc(p, head_dim, ncta, st) : launch_attention_simt(p, head_dim, elem_bytes, ncta, st);
+}
 
 namespace {
 
@@ -41,8 +54,8 @@ pkv_status check_cache(const pkv_cache* c) {
     return PKV_OK;
 }
 
-// Grid of the attention kernel: a persistent set of CTAs, 4 per SM.
-int default_ctas(int num_sms) { return num_sms > 0 ? num_sms * 4 : 0; }
+// Workspace sizing without a kernel choice covers the larger default grid.
+int default_ctas(int num_sms) { return attention_default_ctas(false, num_sms); }
 
 int rows_pad_for(int group, int max_q_len) { return simt_rows_pad(group * max_q_len); }
 
@@ -118,7 +131,8 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
     const int sms = num_sms_current();
     if (sms <= 0) return PKV_ERR_CUDA;
     if (num_ctas < 0) return PKV_ERR_INVALID_ARG;
-    const int ncta = num_ctas > 0 ? num_ctas : default_ctas(sms);
+    const bool tc = attention_uses_tc(cache, group * max_q_len);
+    const int ncta = num_ctas > 0 ? num_ctas : attention_default_ctas(tc, sms);
     const int rows_pad = rows_pad_for(group, max_q_len);
     const WorkspaceLayout wl = workspace_layout(num_seqs, cache->num_kv_heads, cache->head_dim, rows_pad, ncta);
     if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
@@ -148,7 +162,7 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
     p.slot_floats = (int)wl.slot_floats;
     p.scale_log2 = scale * kLog2e;
     const int E = cache->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
-    cudaError_t e = launch_attention_simt(p, cache->head_dim, E, ncta, (cudaStream_t)stream);
+    cudaError_t e = launch_attention(tc, p, cache->head_dim, E, ncta, (cudaStream_t)stream);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

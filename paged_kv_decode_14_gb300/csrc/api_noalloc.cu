@@ -20,7 +20,9 @@
 #include "common.cuh"
 
 namespace pkv {
-cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
+bool attention_uses_tc(const pkv_cache* c, int rows);
+int attention_default_ctas(bool tc, int num_sms);
+cudaError_t launch_attention(bool tc, const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
 int simt_rows_pad(int rows);
 }  // namespace pkv
 
@@ -83,7 +85,8 @@ extern "C" PKV_API pkv_status pkv_paged_attention_noalloc(
     int sms = 0;
     pkv_status s = device_setup(&scratch, &sms);
     if (s != PKV_OK) return s;
-    const int ncta = num_ctas > 0 ? num_ctas : sms * 4;
+    const bool tc = attention_uses_tc(c, group * max_q_len);
+    const int ncta = num_ctas > 0 ? num_ctas : attention_default_ctas(tc, sms);
     const int rows_pad = simt_rows_pad(group * max_q_len);
     const WorkspaceLayout wl = workspace_layout(num_seqs, c->num_kv_heads, c->head_dim, rows_pad, ncta);
     if (wl.total > (size_t)PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;   // beyond the fixed maximum
@@ -117,5 +120,5 @@ extern "C" PKV_API pkv_status pkv_paged_attention_noalloc(
     p.slot_floats = (int)wl.slot_floats;
     p.scale_log2 = scale * kLog2e;
     const int E = c->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
-    return launch_attention_simt(p, c->head_dim, E, ncta, st) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return launch_attention(tc, p, c->head_dim, E, ncta, st) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
