@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--soak-seconds", type=float, default=1.5,
+                    help="untimed steps run right before the timed region while clocks are sampled")
     return ap.parse_args()
 
 
@@ -91,7 +93,7 @@ def load_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -107,7 +109,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -229,6 +231,23 @@ def run_reference(args):
     return 0
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest per-rank value (the slowest rank's time) across the job."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(bytes_per_step: int, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job throughput: every rank moves bytes_per_step per step (weak
+    scaling, one replica per GPU), timed by the slowest rank."""
+    return world * bytes_per_step * steps / (max_ms / 1e3) / 1e9
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -268,6 +287,14 @@ def run_ours(args):
     clocks = ClockSampler(local) if not args.no_clocks else None
     if clocks:
         clocks.__enter__()
+        # keep the GPU under the same load while the sampler starts up, right
+        # before the timed region (the timed region alone is tens of ms)
+        t_end = time.perf_counter() + args.soak_seconds
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                flush.zero_()
+                dw.step()
+            torch.cuda.synchronize(dev)
     barrier()
     wall0 = time.perf_counter()
     for e0, e1, e2 in ev:
@@ -284,14 +311,10 @@ def run_ours(args):
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     attn_ms = [b.elapsed_time(c) for _, b, c in ev]
     app_ms = [a.elapsed_time(b) for a, b, _ in ev]
-    tot = float(np.sum(step_ms))
-    if world > 1:
-        t = torch.tensor([tot], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot = float(t.item())
+    tot = max_over_ranks(float(np.sum(step_ms)), world, dev)
     kvb = w.kv_bytes()
     ms = tot / args.steps
-    value = world * kvb * args.steps / (tot / 1e3) / 1e9
+    value = job_throughput_gbs(kvb, args.steps, tot, world)
 
     # ---------------- end to end through the public API, host buffers
     hin, hout = w.step_io_bytes()
@@ -311,12 +334,8 @@ def run_ours(args):
         if i >= args.warmup:
             e2e_ev[i - args.warmup][1].record(stream)
     barrier()
-    e2e_tot = float(sum(a.elapsed_time(b) for a, b in e2e_ev))
-    if world > 1:
-        t = torch.tensor([e2e_tot], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_tot = float(t.item())
-    e2e_val = world * kvb * args.steps / (e2e_tot / 1e3) / 1e9
+    e2e_tot = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in e2e_ev)), world, dev)
+    e2e_val = job_throughput_gbs(kvb, args.steps, e2e_tot, world)
 
     # ---------------- roofline of the dominant kernel (attention)
     peak, peak_kind = hbm_peak()
@@ -347,6 +366,9 @@ def run_ours(args):
             "wall_s_timed_region": wall}
     if clocks:
         line["clocks"] = clocks.summary()
+        if line["clocks"] is not None:
+            line["clocks"]["window"] = f"{args.soak_seconds:.1f} s of identical untimed steps + the timed region"
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, threads, n, el = cpu_baseline(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",

@@ -10,17 +10,25 @@ cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_n
 cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, int ncta, cudaStream_t st);
 int simt_rows_pad(int rows);
+int tc_heads_per_segment(int num_kv_heads, int rows);
 
-// Kernel choice: the tensor-core kernel for bf16 caches (R = G * max_q_len <= 32),
-// the CUDA-core kernel for FP8 caches.
-bool attention_uses_tc(const pkv_cache* c, int rows) { return c->kv_dtype == PKV_KV_BF16 && rows <= 32; }
+// Kernel choice and grid for one attention call: the tensor-core kernel for
+// bf16 caches (R = G * max_q_len <= 32; one persistent CTA per SM, all of its
+// ~227 KiB of shared memory), the CUDA-core kernel for FP8 caches (4 CTAs per
+// SM).  rows_pad: partial-slot rows (the tensor-core kernel keeps up to 32
+// columns of several kv-heads per segment).
+AttnLaunch plan_attention(const pkv_cache* c, int group, int max_q_len, int num_ctas, int num_sms) {
+    AttnLaunch L;
+    const int rows = group * max_q_len;
+    L.tc = c->kv_dtype == PKV_KV_BF16 && rows <= 32;
+    L.ncta = num_ctas > 0 ? num_ctas : (L.tc ? num_sms : 4 * num_sms);
+    L.rows_pad = L.tc ? 32 : simt_rows_pad(rows);
+    L.hg = L.tc ? tc_heads_per_segment(c->num_kv_heads, rows) : 1;
+    return L;
+}
 
-// Default grid: one persistent CTA per SM for the tensor-core kernel (it
-// holds ~200 KiB of shared memory), four per SM for the CUDA-core kernel.
-int attention_default_ctas(bool tc, int num_sms) { return num_sms > 0 ? (tc ? num_sms : 4 * num_sms) : 0; }
-
-cudaError_t launch_attention(bool tc, const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st) {
-    return tc ? launch_attention_tc(p, head_dim, ncta, st) : launch_attention_simt(p, head_dim, elem_bytes, ncta, st);
+cudaError_t launch_attention(const AttnLaunch& L, const AttnParams& p, int head_dim, int elem_bytes, cudaStream_t st) {
+    return L.tc ? launch_attention_tc(p, head_dim, L.ncta, st) : launch_attention_simt(p, head_dim, elem_bytes, L.ncta, st);
 }
 
 namespace {
@@ -54,10 +62,9 @@ pkv_status check_cache(const pkv_cache* c) {
     return PKV_OK;
 }
 
-// Workspace sizing without a kernel choice covers the larger default grid.
-int default_ctas(int num_sms) { return attention_default_ctas(false, num_sms); }
-
-int rows_pad_for(int group, int max_q_len) { return simt_rows_pad(group * max_q_len); }
+// Workspace sizing without a kernel choice covers either kernel: the larger
+// default grid and 32 slot rows.
+int default_ctas(int num_sms) { return 4 * num_sms; }
 
 }  // namespace
 }  // namespace pkv
@@ -103,7 +110,7 @@ PKV_API size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_q_head
     if (head_dim <= 0 || max_q_len < 1) return 0;
     if (num_ctas <= 0) num_ctas = default_ctas(num_sms_current());
     if (num_ctas <= 0) return 0;
-    const int rows_pad = rows_pad_for(num_q_heads / num_kv_heads, max_q_len);
+    const int rows_pad = max(32, simt_rows_pad((num_q_heads / num_kv_heads) * max_q_len));
     return workspace_layout(num_seqs, num_kv_heads, head_dim, rows_pad, num_ctas).total;
 }
 
@@ -131,10 +138,8 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
     const int sms = num_sms_current();
     if (sms <= 0) return PKV_ERR_CUDA;
     if (num_ctas < 0) return PKV_ERR_INVALID_ARG;
-    const bool tc = attention_uses_tc(cache, group * max_q_len);
-    const int ncta = num_ctas > 0 ? num_ctas : attention_default_ctas(tc, sms);
-    const int rows_pad = rows_pad_for(group, max_q_len);
-    const WorkspaceLayout wl = workspace_layout(num_seqs, cache->num_kv_heads, cache->head_dim, rows_pad, ncta);
+    const AttnLaunch L = plan_attention(cache, group, max_q_len, num_ctas, sms);
+    const WorkspaceLayout wl = workspace_layout(num_seqs, cache->num_kv_heads, cache->head_dim, L.rows_pad, L.ncta);
     if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
 
     AttnParams p;
@@ -158,11 +163,12 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.max_q_len = max_q_len;
     p.rows = group * max_q_len;
-    p.rows_pad = rows_pad;
+    p.rows_pad = L.rows_pad;
     p.slot_floats = (int)wl.slot_floats;
     p.scale_log2 = scale * kLog2e;
+    p.hg = L.hg;
     const int E = cache->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
-    cudaError_t e = launch_attention(tc, p, cache->head_dim, E, ncta, (cudaStream_t)stream);
+    cudaError_t e = launch_attention(L, p, cache->head_dim, E, (cudaStream_t)stream);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

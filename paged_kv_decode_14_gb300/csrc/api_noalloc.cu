@@ -20,10 +20,8 @@
 #include "common.cuh"
 
 namespace pkv {
-bool attention_uses_tc(const pkv_cache* c, int rows);
-int attention_default_ctas(bool tc, int num_sms);
-cudaError_t launch_attention(bool tc, const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
-int simt_rows_pad(int rows);
+AttnLaunch plan_attention(const pkv_cache* c, int group, int max_q_len, int num_ctas, int num_sms);
+cudaError_t launch_attention(const AttnLaunch& L, const AttnParams& p, int head_dim, int elem_bytes, cudaStream_t st);
 }  // namespace pkv
 
 static __device__ __align__(256) uint8_t g_pkv_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
@@ -85,10 +83,8 @@ extern "C" PKV_API pkv_status pkv_paged_attention_noalloc(
     int sms = 0;
     pkv_status s = device_setup(&scratch, &sms);
     if (s != PKV_OK) return s;
-    const bool tc = attention_uses_tc(c, group * max_q_len);
-    const int ncta = num_ctas > 0 ? num_ctas : attention_default_ctas(tc, sms);
-    const int rows_pad = simt_rows_pad(group * max_q_len);
-    const WorkspaceLayout wl = workspace_layout(num_seqs, c->num_kv_heads, c->head_dim, rows_pad, ncta);
+    const AttnLaunch L = plan_attention(c, group, max_q_len, num_ctas, sms);
+    const WorkspaceLayout wl = workspace_layout(num_seqs, c->num_kv_heads, c->head_dim, L.rows_pad, L.ncta);
     if (wl.total > (size_t)PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;   // beyond the fixed maximum
 
     cudaStream_t st = (cudaStream_t)stream;
@@ -116,9 +112,10 @@ extern "C" PKV_API pkv_status pkv_paged_attention_noalloc(
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.max_q_len = max_q_len;
     p.rows = group * max_q_len;
-    p.rows_pad = rows_pad;
+    p.rows_pad = L.rows_pad;
     p.slot_floats = (int)wl.slot_floats;
     p.scale_log2 = scale * kLog2e;
+    p.hg = L.hg;
     const int E = c->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
-    return launch_attention(tc, p, c->head_dim, E, ncta, st) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return launch_attention(L, p, c->head_dim, E, st) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t* __restrict__
                                                      int D, int64_t num_blocks, uint8_t* k_cache, uint8_t* v_cache,
                                                      const float* __restrict__ k_scales,
                                                      const float* __restrict__ v_scales, int* err) {
+    griddep_launch();                            // the attention that follows may start its set-up
     const int NCH = D * E / 16;                  // 16-byte chunks per token row in the cache
     const int64_t per_tok = (int64_t)Hkv * NCH * 2;
     const int64_t total = num_tokens * per_tok;

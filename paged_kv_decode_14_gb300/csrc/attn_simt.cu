@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x;
+    griddep_wait();       // inputs of the previous kernel on the stream are visible
     Cursor cur;
     int u0, u1, W, P;
     if (!plan_locate<kThreads>(p, cta, gridDim.x, scratch, &cur, &u0, &u1, &W, &P)) return;
@@ -333,8 +334,7 @@ static cudaError_t launch_simt_t(const AttnParams& p, int ncta, cudaStream_t st)
     auto kern = simt::attn_simt_kernel<D, E, RT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<ncta, simt::kThreads, K::SMEM, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(ncta), dim3(simt::kThreads), (size_t)K::SMEM, st, p);
 }
 
 template <int D, int E>

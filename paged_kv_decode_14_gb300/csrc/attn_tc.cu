@@ -3,34 +3,46 @@
 //
 // Computes what attn_simt.cu computes (the paged GQA/XQA attention of the
 // lfm25-inference README, equal to dense attention per the inferd
-// equivalence gate): for every (sequence b, kv-head g), rows r = i*G + hl,
-//   out_r = softmax_j(scale * q_r . k_j) v_j,  j <= L - Q + i.
+// equivalence gate): for every sequence b and query row (i, query head h),
+//   out = softmax_j(scale * q . k_j) v_j,  j <= L - Q + i,  kv-head h / G.
 //
-// Work partition and merge: the balanced page partition of common.cuh, one
-// persistent CTA per SM.  A CTA streams its pages in tiles of 8 pages = 128
-// tokens.  Per tile:
-//   S^T[128 tok, N] = K_tile[128 tok, D] . Q^T[D, N]       (MMA, M=128, K-major A and B)
+// Columns.  A segment is (sequence b, group of HG kv-heads).  Its query rows
+// sit on the MMA's N side ("swap AB"): column n = hh * R + r for kv-head
+// hh of the group and row r = i * G + hl of that head's GQA group, R = G * Q,
+// NCOL = HG * R <= 8 (P split into a bf16 high and low part on adjacent
+// columns, N = 16) or <= 32 (N = 32).  A 128-token tile holds 8 (page,
+// kv-head) units in page-major order; each token row only sees the columns of
+// its own kv-head.
+//
+// Per tile:
+//   S^T[128 tok, N] = K_tile[128 tok, D] . Q^T[D, N]        (M=128, K-major A and B)
 //   softmax on S^T rows (one thread per token, TMEM lane = token)
-//   O^T[128 d, N]   = V_tile^T[d, 128 tok] . P^T[128 tok, N] (MMA, M=128, MN-major A and B)
-//   correction acc = acc * alpha + O^T (one thread per head-dim row)
-// with N = 16 or 32 columns holding the group's R = G*Q query rows.  The
-// query group sits on the MMA's N side ("swap AB"), so G*Q rows of 4..32 do
-// not waste a 64/128-row M tile.  When 2R <= 16, P is split into a bf16 high
-// part and a bf16 low part on adjacent columns (free: N is 16 anyway), so the
-// P.V product keeps about 16 bits of P.
+//   O^T[128 d, N]  += V_tile^T[d, 128 tok] . P^T[128 tok, N] (M=128, MN-major A and B)
+// K and V pages sit in separate rings: a K slot is refilled as soon as its
+// S^T MMA has run, a V slot once its P.V MMA has.
+// O^T stays in TMEM for the whole piece; the softmax reference max of a
+// column is only raised (and O^T rescaled in TMEM) when a logit exceeds it by
+// more than 2^8, so most tiles need neither a max reduction nor a rescale.
 //
 // The cache's page layout (16-byte chunks, core matrices of 8 tokens x 16
-// bytes, see pagedkv.h) is exactly the tensor core's no-swizzle canonical
-// layout: K pages are K-major A operands and V pages MN-major A operands as
-// copied, so a page goes HBM -> shared memory in one bulk copy and is never
-// touched by the CUDA cores (except zeroing the unwritten tail rows of a
-// sequence's last page, which may hold NaN).
+// bytes, see pagedkv.h) is the tensor core's no-swizzle canonical layout: K
+// pages are K-major A operands and V pages MN-major A operands as copied, so
+// a page goes HBM -> shared memory in one bulk copy and is never touched by
+// the CUDA cores (except zeroing the unwritten tail rows of a sequence's last
+// page, which may hold NaN).
 //
-// Warp roles (192 threads): warps 0-3 softmax + correction + epilogue (their
-// TMEM lane quarters), warp 4 producer (bulk copies, q staging), warp 5 MMA
-// issuer.  Every mbarrier wait is bounded (2 s); a timeout sets
-// PKV_DEVERR_TIMEOUT and an abort flag, all roles wind down, in-flight copies
-// are drained and TMEM is freed before the CTA exits.
+// Work partition: the balanced unit partition of common.cuh, one persistent
+// CTA per SM.  A CTA takes its last piece first and then walks its range from
+// the start, so both pieces of every segment cut between two CTAs finish
+// early and their merge overlaps the rest of the work.
+//
+// Warp roles (256 threads): warps 0-3 softmax, O rescale and piece epilogue
+// (their TMEM lane quarters), warp 4 producer (bulk copies, q staging), warp
+// 5 issues the S^T MMAs, warp 7 the P.V MMAs (each blocks on its own
+// barriers, so a P.V never waits behind the next tiles' S^T), warp 6 merges
+// split segments.  Every mbarrier wait is bounded
+// (2 s); a timeout sets PKV_DEVERR_TIMEOUT and an abort flag, all roles wind
+// down, in-flight copies are drained and TMEM is freed before the CTA exits.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -39,46 +51,52 @@ namespace tc {
 
 using namespace ptx;
 
-constexpr int kTP = 8;                        // pages per tile
-constexpr int kTileTok = kTP * kBlock;        // 128 tokens = MMA M
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kTP = 8;                        // units (pages of one kv-head) per tile
+constexpr int kTileTok = kTP * kBlock;        // 128 token rows = MMA M
+constexpr int kThreads = 256;
+constexpr int kProducerWarp = 4, kMmaWarp = 5, kMergeWarp = 6, kPvWarp = 7;
 constexpr int kSoftThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxSmem = 232448;
+constexpr int NSB = 4;                        // S^T / P ring depth (tiles the MMA may run ahead)
 
-template <int D, int NPAD, bool SPLIT, int NS>
+// Online-softmax reference slack (powers of two), see the header comment.
+constexpr float kRescaleSlack = 8.f;
+
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV>
 struct Cfg {
+    static constexpr int RMAX = SPLIT ? NPAD / 2 : NPAD;  // logical columns
     static constexpr int PAGE = kBlock * D * 2;
     static constexpr int NCH = D / 8;                   // 16-byte chunks per token row
     static constexpr int TILE = kTP * PAGE;
     static constexpr int VSLACK = D == 64 ? 1024 : 0;   // M=128 PV on D=64 reads 1 KiB past a page
     static constexpr int OFF_K = 0;                     // + st * TILE
-    static constexpr int OFF_V = NS * TILE;             // + st * (TILE + VSLACK)
-    static constexpr int OFF_Q = OFF_V + NS * (TILE + VSLACK);
+    static constexpr int OFF_V = NSK * TILE;            // + st * (TILE + VSLACK)
+    static constexpr int OFF_Q = OFF_V + NSV * (TILE + VSLACK);
     static constexpr int QBUF = NPAD * D * 2;
     static constexpr int OFF_P = OFF_Q + 2 * QBUF;
     static constexpr int PBUF = NPAD * kTileTok * 2;
-    static constexpr int OFF_RED = OFF_P + 2 * PBUF;             // float [2][4][RMAX]
-    static constexpr int RMAX = SPLIT ? NPAD / 2 : NPAD;         // query rows per (b, g)
-    static constexpr int OFF_LRED = OFF_RED + 2 * 4 * RMAX * 4;  // float [4][RMAX]
+    static constexpr int OFF_RED = OFF_P + NSB * PBUF;  // float [8 slots][RMAX]
+    static constexpr int OFF_LRED = OFF_RED + 8 * RMAX * 4;   // float [4 warps][RMAX]
     static constexpr int OFF_BAR = OFF_LRED + 4 * RMAX * 4;
-    static constexpr int NBAR = 3 * NS + 11;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;          // tmem addr, abort, ticket, zero
-    static constexpr int SMEM_USED = OFF_MISC + 16 + 128;        // + base alignment slack
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 10;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem addr, abort, zero
+    static constexpr int OFF_MQ = OFF_MISC + 16;         // merge tasks: int [4][8]
+    static constexpr int SMEM_USED = OFF_MQ + 128 + 128; // + base alignment slack
     // One CTA per SM either way: take the whole per-block budget, so every
     // operand read the descriptors can form stays inside the allocation.
     static constexpr int SMEM = kMaxSmem - 1024;
-    static constexpr int TMEM_COLS = 4 * NPAD;                   // S[2], O[2]
+    static constexpr int COL_S = 0;                      // S^T buffers: NSB x NPAD columns
+    static constexpr int COL_O = NSB * NPAD;             // O^T accumulator: NPAD columns
+    static constexpr int TMEM_COLS = (NSB + 1) * NPAD <= 64 ? 64 : (NSB + 1) * NPAD <= 128 ? 128 : 256;
     static_assert(SMEM_USED <= SMEM, "shared memory budget");
-    static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation size");
 };
 
-// barrier indices
-template <int NS>
+template <int NSK, int NSV>
 struct Bars {
-    static constexpr int KFULL = 0, VFULL = NS, EMPTY = 2 * NS, SFULL = 3 * NS, PFULL = SFULL + 2,
-                         OFULL = PFULL + 2, QFULL = OFULL + 2, QEMPTY = QFULL + 2, DONE = QEMPTY + 2;
+    static constexpr int KFULL = 0, KEMPTY = NSK, VFULL = 2 * NSK, VEMPTY = 2 * NSK + NSV,
+                         SFULL = 2 * NSK + 2 * NSV, PFULL = SFULL + NSB, PEMPTY = PFULL + NSB,
+                         QFULL = PEMPTY + NSB, QEMPTY = QFULL + 2, DONE = QEMPTY + 2, MQFULL = DONE + 2;
 };
 
 struct Ctl {
@@ -114,36 +132,128 @@ __device__ __forceinline__ bool bar_red_or(int id, int n, bool v) {
     return r != 0;
 }
 
-// Iterates the pieces of a CTA's unit range (every role walks it the same way).
-struct PieceIter {
-    Cursor cur;
-    int u, u1, Hkv;
-    int g, S0, S1, pg0, npg;
-    __device__ void load(const AttnParams& p) {
-        g = (u - cur.Ub) / cur.nb;
-        S0 = cur.Ub + g * cur.nb;
-        S1 = S0 + cur.nb;
-        const int pe = min(u1, S1);
-        pg0 = u - S0;
-        npg = pe - u;
-    }
-    __device__ bool valid() const { return u < u1; }
-    __device__ void advance(const AttnParams& p) {
-        u += npg;
-        if (u < u1 && u == cur.Ub + cur.nb * Hkv) cursor_next(p, cur);
-        if (u < u1) load(p);
-    }
-};
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D, int NPAD, bool SPLIT, int NS>
+// Pieces of a CTA's unit range [u0, u1), in processing order: the piece
+// holding u1 - 1 first (when it does not start at u0), then [u0, start of
+// that piece) front to back.  Segment = (sequence, group of HG kv-heads), its
+// units = pages x HG in page-major order.  Every role walks it the same way.
+struct PieceIter {
+    Cursor cur, fcur;
+    int u, stop, u0, HG, Hkv;
+    bool tail_phase;
+    int hg, S0, S1, pg0, npg;   // current piece: group, segment [S0, S1), units [S0+pg0, S0+pg0+npg)
+
+    __device__ void load_at(int uu, int end) {
+        const int len = cur.nb * HG;
+        hg = (uu - cur.Ub) / len;
+        S0 = cur.Ub + hg * len;
+        S1 = S0 + len;
+        pg0 = uu - S0;
+        npg = min(end, S1) - uu;
+    }
+    __device__ void init(const AttnParams& p, const Cursor& c0, const Cursor& ct, int u0_, int u1) {
+        HG = p.hg;
+        Hkv = p.num_kv_heads;
+        u0 = u0_;
+        fcur = c0;
+        cur = ct;
+        const int len = ct.nb * HG;
+        const int s0t = ct.Ub + ((u1 - 1 - ct.Ub) / len) * len;
+        const int tstart = max(u0, s0t);
+        if (tstart > u0) {
+            tail_phase = true;
+            stop = tstart;          // the forward walk ends where the tail piece starts
+            u = tstart;
+            load_at(tstart, u1);
+        } else {
+            tail_phase = false;
+            stop = u1;
+            cur = c0;
+            u = u0;
+            load_at(u0, u1);
+        }
+    }
+    __device__ bool valid() const { return tail_phase || u < stop; }
+    __device__ void advance(const AttnParams& p) {
+        if (tail_phase) {
+            tail_phase = false;
+            cur = fcur;
+            u = u0;
+            load_at(u, stop);
+            return;
+        }
+        u += npg;
+        if (u < stop && u == cur.Ub + cur.nb * Hkv) cursor_next(p, cur);
+        if (u < stop) load_at(u, stop);
+    }
+};
+
+// Column n of segment (b, hg) -> element offset of its q / out row.
+__device__ __forceinline__ size_t col_row_offset(const AttnParams& p, int qoff, int R, int hg, int n, int D) {
+    const int hh = n / R, r = n % R, i = r / p.group, hl = r % p.group;
+    return ((size_t)(qoff + i) * p.num_q_heads + (hg * p.hg + hh) * p.group + hl) * D;
+}
+
+// Merge the partials of segment [S0, S1) (NCOL columns) into out; one warp,
+// one round trip of loads per piece (online merge across pieces).
+template <int D>
+__device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q, int S0, int S1, int W, int P,
+                                   int lane) {
+    constexpr int DPL = D / 32;
+    const int c_first = owner_cta(S0, W, P), c_last = owner_cta(S1 - 1, W, P);
+    const int R = p.group * Q, ncol = p.hg * R;
+    for (int n0 = 0; n0 < ncol; n0 += 8) {
+        float M[8], den[8], num[8][DPL];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            M[k] = -INFINITY;
+            den[k] = 0.f;
+#pragma unroll
+            for (int x = 0; x < DPL; ++x) num[k][x] = 0.f;
+        }
+        for (int c = c_first; c <= c_last; ++c) {
+            const float* s = slot_ptr(p, c, S0, (int)(((int64_t)c * W) / P));
+            float m[8], l[8], a[8][DPL];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int n = n0 + k;
+                m[k] = n < ncol ? __ldcg(s + n) : -INFINITY;
+                l[k] = n < ncol ? __ldcg(s + p.rows_pad + n) : 0.f;
+#pragma unroll
+                for (int x = 0; x < DPL; ++x)
+                    a[k][x] = n < ncol ? __ldcg(s + 2 * p.rows_pad + (size_t)n * D + lane + 32 * x) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float mn = fmaxf(M[k], m[k]);
+                const float wo = (M[k] == -INFINITY) ? 0.f : exp2f(M[k] - mn);
+                const float wn = (m[k] == -INFINITY) ? 0.f : exp2f(m[k] - mn);
+                M[k] = mn;
+                den[k] = den[k] * wo + l[k] * wn;
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) num[k][x] = num[k][x] * wo + a[k][x] * wn;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int n = n0 + k;
+            if (n < ncol) {
+                __nv_bfloat16* o = p.out + col_row_offset(p, qoff, R, hg, n, D);
+#pragma unroll
+                for (int x = 0; x < DPL; ++x) o[lane + 32 * x] = __float2bfloat16_rn(num[k][x] / den[k]);
+            }
+        }
+    }
+}
+
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p) {
-    using K = Cfg<D, NPAD, SPLIT, NS>;
-    using B = Bars<NS>;
+    using K = Cfg<D, NPAD, SPLIT, NSK, NSV>;
+    using B = Bars<NSK, NSV>;
     constexpr int RMAX = K::RMAX;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int scratch[kThreads / 32 + 1];
@@ -151,37 +261,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     const uint32_t sb = smem_u32(smem);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    Cursor cur0;
-    int u0, u1, W, P;
-    if (!plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P)) return;
     const int cta = blockIdx.x;
 
     auto bar = [&](int i) -> uint32_t { return sb + K::OFF_BAR + 8 * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 4);
-    volatile int* ticket_flag = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 8);
-    volatile int* never = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 12);   // stays 0
+    volatile int* never = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 8);   // stays 0
     const Ctl ctl{abort_flag, p.err};
     const Ctl drain{never, p.err};      // bounded waits that ignore the abort flag
 
+    // Q buffers start zeroed: rows past a piece's columns are never written
+    // and only feed S^T columns the softmax ignores.
+    for (int i = tid; i < 2 * K::QBUF / 16; i += kThreads)
+        reinterpret_cast<uint4*>(smem + K::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NSK; ++s) {
             mbar_init(bar(B::KFULL + s), 1);
-            mbar_init(bar(B::VFULL + s), 1);
-            mbar_init(bar(B::EMPTY + s), 1);
+            mbar_init(bar(B::KEMPTY + s), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int s = 0; s < NSV; ++s) {
+            mbar_init(bar(B::VFULL + s), 1);
+            mbar_init(bar(B::VEMPTY + s), 1);
+        }
+        for (int i = 0; i < NSB; ++i) {
             mbar_init(bar(B::SFULL + i), 1);
             mbar_init(bar(B::PFULL + i), kSoftThreads);
-            mbar_init(bar(B::OFULL + i), 1);
+            mbar_init(bar(B::PEMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B::QFULL + i), 1);
             mbar_init(bar(B::QEMPTY + i), 1);
         }
         mbar_init(bar(B::DONE), 1);
+        mbar_init(bar(B::DONE + 1), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B::MQFULL + i), 1);
         *abort_flag = 0;
         *never = 0;
         mbar_fence_init();
     }
+    // Everything above touches only this CTA's shared memory, so under a
+    // programmatic dependent launch it overlaps the previous kernel; inputs are
+    // read only after that kernel's writes are visible.
+    griddep_wait();
+    Cursor cur0, curt;
+    int u0, u1, W, P;
+    const bool has_work = plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt);
+    if (!has_work) return;       // uniform across the CTA; no TMEM held yet
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), K::TMEM_COLS);
         tmem_relinquish();
@@ -190,19 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int G = p.group, Hkv = p.num_kv_heads;
+    const int G = p.group, Hkv = p.num_kv_heads, HG = p.hg;
 
     PieceIter it;
-    it.cur = cur0;
-    it.u = u0;
-    it.u1 = u1;
-    it.Hkv = Hkv;
-    it.load(p);
+    it.init(p, cur0, curt, u0, u1);
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         const uint64_t pol = policy_evict_first();
-        int t = 0, j = 0;
+        int t = 0, j = 0, kcount = 0, vcount = 0;
         bool ok = true;
         while (ok && it.valid()) {
             const int qb = j & 1;
@@ -211,220 +333,265 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                 ok = __shfl_sync(0xffffffffu, w, 0);
                 if (!ok) break;
             }
-            // q rows of this (b, g) -> Q buffer in the K-major core-matrix layout
-            const int R = G * it.cur.Q;
-            uint8_t* qdst = smem + K::OFF_Q + qb * K::QBUF;
-            for (int idx = lane; idx < NPAD * K::NCH; idx += 32) {
-                const int r = idx / K::NCH, c = idx % K::NCH;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (r < R) {
-                    const int i = r / G, hl = r % G;
-                    v = __ldg(reinterpret_cast<const uint4*>(
-                        p.q + ((size_t)(it.cur.qoff + i) * p.num_q_heads + it.g * G + hl) * D + c * 8));
-                }
-                *reinterpret_cast<uint4*>(qdst + (r >> 3) * (K::NCH * 128) + c * 128 + (r & 7) * 16) = v;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B::QFULL + qb));
-
+            const int R = G * it.cur.Q, ncol = HG * R;
             const int32_t* table = p.block_tables + (size_t)it.cur.b * p.max_blocks_per_seq;
-            int ids = 0, ids_base = -1;
+            int ids = 0, ids_start = -1000000;      // ids: table entry of page ids_start + lane
             for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
                 const int np = min(kTP, it.npg - t0);
-                const int st = t % NS;
-                // block ids of this and the next 3 tiles, 8 per tile, one per lane
-                if ((t0 >> 5) != ids_base) {
-                    ids_base = t0 >> 5;
-                    const int pi = (ids_base << 5) + lane;
-                    ids = pi < it.npg ? table[it.pg0 + pi] : 0;
+                const int ks = t % NSK, vs = t % NSV;
+                const int qfirst = it.pg0 + t0;                       // first unit of the tile
+                const int jfirst = qfirst / HG, jlast = (qfirst + np - 1) / HG;
+                if (jfirst < ids_start || jlast >= ids_start + 32) {
+                    ids_start = jfirst;
+                    ids = ids_start + lane < it.cur.nb ? table[ids_start + lane] : 0;
                 }
-                int blk = __shfl_sync(0xffffffffu, ids, ((t0 & 31) + (lane & 7)) & 31);
-                if (t >= NS) {
-                    bool w = lane == 0 ? wait_bar(bar(B::EMPTY + st), ((t / NS) - 1) & 1, ctl) : true;
+                const int qu = qfirst + (lane & 7);
+                int blk = __shfl_sync(0xffffffffu, ids, (qu / HG - ids_start) & 31);
+                if (blk < 0 || blk >= p.num_blocks) {
+                    if (lane < np) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+                    blk = 0;
+                }
+                const size_t off = ((size_t)blk * Hkv + it.hg * HG + qu % HG) * K::PAGE;
+                if (t >= NSK) {
+                    bool w = lane == 0 ? wait_bar(bar(B::KEMPTY + ks), ((t / NSK) - 1) & 1, ctl) : true;
                     ok = __shfl_sync(0xffffffffu, w, 0);
                     if (!ok) break;
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(B::KFULL + st), np * K::PAGE);
-                    mbar_arrive_expect_tx(bar(B::VFULL + st), np * K::PAGE);
-                }
+                if (lane == 0) mbar_arrive_expect_tx(bar(B::KFULL + ks), np * K::PAGE);
                 __syncwarp();
-                if (lane < np) {
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        raise_error(p.err, PKV_DEVERR_BLOCK_ID);
-                        blk = 0;
+                if (lane < np)
+                    bulk_g2s_hint(sb + K::OFF_K + ks * K::TILE + lane * K::PAGE, p.k_cache + off, K::PAGE,
+                                  bar(B::KFULL + ks), pol);
+                ++kcount;
+                if (t0 == 0) {
+                    // q rows of the segment's columns -> Q buffer (K-major core
+                    // matrices), loaded while the first K tile is in flight
+                    uint8_t* qdst = smem + K::OFF_Q + qb * K::QBUF;
+                    constexpr int QV = (RMAX * K::NCH + 31) / 32;
+                    uint4 v[QV];
+#pragma unroll
+                    for (int k = 0; k < QV; ++k) {
+                        const int idx = lane + 32 * k;
+                        if (idx < ncol * K::NCH) {
+                            const int n = idx / K::NCH, c = idx % K::NCH;
+                            v[k] = __ldg(reinterpret_cast<const uint4*>(
+                                p.q + col_row_offset(p, it.cur.qoff, R, it.hg, n, D) + c * 8));
+                        }
                     }
-                    const size_t off = ((size_t)blk * Hkv + it.g) * K::PAGE;
-                    bulk_g2s_hint(sb + K::OFF_K + st * K::TILE + lane * K::PAGE, p.k_cache + off, K::PAGE,
-                                  bar(B::KFULL + st), pol);
-                    bulk_g2s_hint(sb + K::OFF_V + st * (K::TILE + K::VSLACK) + lane * K::PAGE, p.v_cache + off,
-                                  K::PAGE, bar(B::VFULL + st), pol);
+#pragma unroll
+                    for (int k = 0; k < QV; ++k) {
+                        const int idx = lane + 32 * k;
+                        if (idx < ncol * K::NCH) {
+                            const int n = idx / K::NCH, c = idx % K::NCH;
+                            *reinterpret_cast<uint4*>(qdst + (n >> 3) * (K::NCH * 128) + c * 128 + (n & 7) * 16) = v[k];
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B::QFULL + qb));
                 }
+                if (t >= NSV) {
+                    bool w = lane == 0 ? wait_bar(bar(B::VEMPTY + vs), ((t / NSV) - 1) & 1, ctl) : true;
+                    ok = __shfl_sync(0xffffffffu, w, 0);
+                    if (!ok) break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + vs), np * K::PAGE);
+                __syncwarp();
+                if (lane < np)
+                    bulk_g2s_hint(sb + K::OFF_V + vs * (K::TILE + K::VSLACK) + lane * K::PAGE, p.v_cache + off,
+                                  K::PAGE, bar(B::VFULL + vs), pol);
+                ++vcount;
                 __syncwarp();
             }
             ++j;
-            it.advance(p);
+            if (ok) it.advance(p);
         }
-        // drain: the last fill of every stage has landed before the CTA exits
+        // drain: every copy issued has landed before the CTA exits
         if (lane == 0) {
-            for (int tt = max(0, t - NS); tt < t; ++tt) {
-                const int st = tt % NS;
-                wait_bar(bar(B::KFULL + st), (tt / NS) & 1, drain);
-                wait_bar(bar(B::VFULL + st), (tt / NS) & 1, drain);
-            }
+            for (int tt = max(0, kcount - NSK); tt < kcount; ++tt)
+                wait_bar(bar(B::KFULL + tt % NSK), (tt / NSK) & 1, drain);
+            for (int tt = max(0, vcount - NSV); tt < vcount; ++tt)
+                wait_bar(bar(B::VFULL + tt % NSV), (tt / NSV) & 1, drain);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ S^T issuer
+        // S^T of tile t once its K and its piece's q have landed and the
+        // softmax has released S^T buffer t % NSB (P of tile t - NSB written).
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(128, NPAD, false, false);
-            constexpr uint32_t idPV = idesc_bf16_f32(128, NPAD, true, true);
             int t = 0, j = 0;
-            int pend = -1, pend_np = 0;
             bool ok = true;
-            auto issue_pv = [&](int tt, int np) -> bool {
-                const int st = tt % NS;
-                if (!wait_bar(bar(B::VFULL + st), (tt / NS) & 1, ctl)) return false;
-                if (!wait_bar(bar(B::PFULL + (tt & 1)), (tt >> 1) & 1, ctl)) return false;
-                tc_fence_after();
-                const uint32_t vbase = sb + K::OFF_V + st * (K::TILE + K::VSLACK);
-                const uint32_t pbase = sb + K::OFF_P + (tt & 1) * K::PBUF;
-                for (int pg = 0; pg < np; ++pg) {
-                    const uint64_t a = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
-                    const uint64_t b = smem_desc(pbase + pg * 256, 128, 16 * 128);
-                    mma_bf16(tmem + 2 * NPAD + (tt & 1) * NPAD, a, b, idPV, pg > 0);
-                }
-                mma_commit(bar(B::OFULL + (tt & 1)));
-                mma_commit(bar(B::EMPTY + st));
-                return true;
-            };
             while (ok && it.valid()) {
                 const int qb = j & 1;
                 if (!(ok = wait_bar(bar(B::QFULL + qb), (j >> 1) & 1, ctl))) break;
-                tc_fence_after();
                 const uint32_t qbase = sb + K::OFF_Q + qb * K::QBUF;
                 for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
-                    const int np = min(kTP, it.npg - t0);
-                    const int st = t % NS;
-                    if (!(ok = wait_bar(bar(B::KFULL + st), (t / NS) & 1, ctl))) break;
+                    const int ks = t % NSK;
+                    if (t >= NSB && !(ok = wait_bar(bar(B::PFULL + t % NSB), ((t / NSB) - 1) & 1, ctl))) break;
+                    if (!(ok = wait_bar(bar(B::KFULL + ks), (t / NSK) & 1, ctl))) break;
                     tc_fence_after();
-                    const uint32_t kbase = sb + K::OFF_K + st * K::TILE;
+                    const uint32_t kbase = sb + K::OFF_K + ks * K::TILE;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint64_t a = smem_desc(kbase + k * 256, 128, K::NCH * 128);
                         const uint64_t b = smem_desc(qbase + k * 256, 128, K::NCH * 128);
-                        mma_bf16(tmem + (t & 1) * NPAD, a, b, idS, k > 0);
+                        mma_bf16(tmem + K::COL_S + (t % NSB) * NPAD, a, b, idS, k > 0);
                     }
-                    mma_commit(bar(B::SFULL + (t & 1)));
+                    mma_commit(bar(B::SFULL + t % NSB));
+                    mma_commit(bar(B::KEMPTY + ks));
                     if (t0 + kTP >= it.npg) mma_commit(bar(B::QEMPTY + qb));
-                    if (pend >= 0 && !(ok = issue_pv(pend, pend_np))) break;
-                    pend = t;
-                    pend_np = np;
                 }
                 ++j;
                 if (ok) it.advance(p);
             }
-            if (ok && pend >= 0) issue_pv(pend, pend_np);
             mma_commit(bar(B::DONE));
             wait_bar(bar(B::DONE), 0, drain);
         }
         __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------ P.V issuer
+        // O^T += V^T P^T of tile t once its P is written and its V has landed;
+        // the first tile of a piece starts O^T afresh.
+        if (lane == 0) {
+            constexpr uint32_t idPV = idesc_bf16_f32(128, NPAD, true, true);
+            int t = 0;
+            bool ok = true;
+            while (ok && it.valid()) {
+                for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
+                    const int np = min(kTP, it.npg - t0);
+                    const int vs = t % NSV;
+                    if (!(ok = wait_bar(bar(B::PFULL + t % NSB), (t / NSB) & 1, ctl))) break;
+                    if (!(ok = wait_bar(bar(B::VFULL + vs), (t / NSV) & 1, ctl))) break;
+                    tc_fence_after();
+                    const uint32_t vbase = sb + K::OFF_V + vs * (K::TILE + K::VSLACK);
+                    const uint32_t pbase = sb + K::OFF_P + (t % NSB) * K::PBUF;
+                    for (int pg = 0; pg < np; ++pg) {
+                        const uint64_t a = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
+                        const uint64_t b = smem_desc(pbase + pg * 256, 128, 16 * 128);
+                        mma_bf16(tmem + K::COL_O, a, b, idPV, (pg > 0 || t0 > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar(B::PEMPTY + t % NSB));
+                    mma_commit(bar(B::VEMPTY + vs));
+                }
+                if (ok) it.advance(p);
+            }
+            mma_commit(bar(B::DONE + 1));
+            wait_bar(bar(B::DONE + 1), 0, drain);
+        }
+        __syncwarp();
+    } else if (warp == kMergeWarp) {
+        // ------------------------------------------------------------ merges of split segments
+        int* mq = reinterpret_cast<int*>(smem + K::OFF_MQ);
+        for (int n = 0;; ++n) {
+            bool w = lane == 0 ? wait_bar(bar(B::MQFULL + (n & 3)), (n >> 2) & 1, ctl) : true;
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            const int* task = mq + (n & 3) * 8;
+            if (task[0] < 0) break;                     // sentinel: the softmax warps are done
+            __threadfence();
+            merge_segment_warp<D>(p, task[1], task[2], task[3], task[4], task[5], W, P, lane);
+        }
+        __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax / correction / epilogue
+        // ------------------------------------------------------------ softmax / rescale / epilogue
         const int tt = tid;                                   // token row of S^T, d row of O^T
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         float* red = reinterpret_cast<float*>(smem + K::OFF_RED);
         float* lred = reinterpret_cast<float*>(smem + K::OFF_LRED);
-        int t = 0;
+        int t = 0, n_tasks = 0;
         bool aborted = false;
-        float m_run[RMAX], l_part[RMAX], acc[RMAX], alpha_prev[RMAX];
-
-        auto correct = [&](int tix) {
-            bool w = wait_bar(bar(B::OFULL + (tix & 1)), (tix >> 1) & 1, ctl);
-            (void)w;
-            tc_fence_after();
-            float o[NPAD];
-#pragma unroll
-            for (int c = 0; c < NPAD; c += 16) {
-                float tmp[16];
-                tmem_ld16(tmem + lane_base + 2 * NPAD + (tix & 1) * NPAD + c, tmp);
-#pragma unroll
-                for (int x = 0; x < 16; ++x) o[c + x] = tmp[x];
-            }
-#pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-                const float add = SPLIT ? (o[2 * r] + o[2 * r + 1]) : o[r];
-                acc[r] = acc[r] * alpha_prev[r] + add;
-            }
-            tc_fence_before();
-        };
+        float m_ref[RMAX], l_part[RMAX];
 
         while (!aborted && it.valid()) {
-            const int Q = it.cur.Q, R = G * Q, L = it.cur.L, lim0 = L - Q;
-            const int st_b = it.cur.b;
+            const int Q = it.cur.Q, R = G * Q, L = it.cur.L, lim0 = L - Q, ncol = HG * R;
+            const int seg_b = it.cur.b;
 #pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-                m_run[r] = -INFINITY;
-                l_part[r] = 0.f;
-                acc[r] = 0.f;
-                alpha_prev[r] = 1.f;
+            for (int n = 0; n < RMAX; ++n) {
+                m_ref[n] = -INFINITY;
+                l_part[n] = 0.f;
             }
             const int ntile = (it.npg + kTP - 1) / kTP;
             for (int jt = 0; jt < ntile; ++jt, ++t) {
                 const int np = min(kTP, it.npg - jt * kTP);
-                const int st = t % NS;
-                bool okw = wait_bar(bar(B::SFULL + (t & 1)), (t >> 1) & 1, ctl);
+                const int vs = t % NSV;
+                // this thread's token: unit slot k of the tile -> (page, kv-head), position
+                const int k = tt >> 4;
+                const int qu = it.pg0 + jt * kTP + k;
+                const int hh = qu % HG;
+                const int pos = (qu / HG) * kBlock + (tt & 15);
+                const bool tok_ok = k < np && pos < L;
+                // visible columns: [lo, hi) of this head's R rows (causal within the window)
+                const int lo = hh * R + max(0, pos - lim0) * G, hi = hh * R + R;
+
+                const bool okw = wait_bar(bar(B::SFULL + t % NSB), (t / NSB) & 1, ctl);
                 tc_fence_after();
-                float s[NPAD];
+                float s[RMAX];
 #pragma unroll
-                for (int c = 0; c < NPAD; c += 16) {
+                for (int c = 0; c < RMAX; c += 16) {
                     float tmp[16];
-                    tmem_ld16(tmem + lane_base + (t & 1) * NPAD + c, tmp);
+                    tmem_ld16(tmem + lane_base + K::COL_S + (t % NSB) * NPAD + c, tmp);
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) s[c + x] = tmp[x];
+                    for (int x = 0; x < 16 && c + x < RMAX; ++x) s[c + x] = tmp[x];
                 }
-                const int pgi = tt >> 4;
-                const int pos = (it.pg0 + jt * kTP + pgi) * kBlock + (tt & 15);
-                const bool tok_ok = pgi < np && pos < L;
-                float x[RMAX];
+                bool need = false;
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r) {
-                    const bool vis = r < R && tok_ok && pos <= lim0 + r / G;
-                    x[r] = vis ? s[r] * p.scale_log2 : -INFINITY;
+                for (int n = 0; n < RMAX; ++n) {
+                    const bool vis = tok_ok && n >= lo && n < hi;
+                    s[n] = vis ? s[n] * p.scale_log2 : -INFINITY;
+                    need |= s[n] > m_ref[n] + kRescaleSlack;
                 }
-                // tile max per row over the 128 tokens
-                float* rd = red + (t & 1) * 4 * RMAX;
+                if (bar_red_or(1, kSoftThreads, need || !okw)) {
+                    // raise the reference to this tile's max (first tile of a piece, or a big jump):
+                    // per (unit slot, column) maxima over the slot's 16 tokens, then per column
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r) {
-                    if (r < R) {
-                        float mx = x[r];
+                    for (int n = 0; n < RMAX; ++n) {
+                        float mx = s[n];
 #pragma unroll
-                        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                        if (lane == 0) rd[warp * RMAX + r] = mx;
+                        for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                        if ((tt & 15) == 0) red[k * RMAX + n] = mx;
                     }
-                }
-                if (bar_red_or(1, kSoftThreads, !okw || *abort_flag)) {
-                    aborted = true;
-                    break;
-                }
-                float alpha[RMAX], pr[RMAX];
-#pragma unroll
-                for (int r = 0; r < RMAX; ++r) {
-                    if (r < R) {
-                        const float tm = fmaxf(fmaxf(rd[r], rd[RMAX + r]), fmaxf(rd[2 * RMAX + r], rd[3 * RMAX + r]));
-                        const float mn = fmaxf(m_run[r], tm);
-                        alpha[r] = (m_run[r] == -INFINITY) ? 0.f : exp2f(m_run[r] - mn);
-                        m_run[r] = mn;
-                        pr[r] = (x[r] == -INFINITY) ? 0.f : exp2f(x[r] - mn);
-                        l_part[r] = l_part[r] * alpha[r] + pr[r];
-                    } else {
-                        alpha[r] = 1.f;
-                        pr[r] = 0.f;
+                    if (bar_red_or(1, kSoftThreads, !okw || *abort_flag)) {
+                        aborted = true;
+                        break;
                     }
+                    float alpha[RMAX];
+                    bool any_scale = false;
+#pragma unroll
+                    for (int n = 0; n < RMAX; ++n) {
+                        float tm = -INFINITY;
+#pragma unroll
+                        for (int kk = 0; kk < kTP; ++kk) tm = fmaxf(tm, red[kk * RMAX + n]);
+                        const float mn = fmaxf(m_ref[n], tm);
+                        alpha[n] = (m_ref[n] == -INFINITY) ? 0.f : exp2f(m_ref[n] - mn);
+                        any_scale |= (alpha[n] != 1.f) && (m_ref[n] != -INFINITY);
+                        m_ref[n] = mn;
+                        l_part[n] *= alpha[n];
+                    }
+                    if (jt > 0 && any_scale) {
+                        // O^T (TMEM) *= alpha once the previous tile's P.V has landed
+                        wait_bar(bar(B::PEMPTY + (t - 1) % NSB), ((t - 1) / NSB) & 1, ctl);
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < NPAD; c += 16) {
+                            float o[16];
+                            tmem_ld16(tmem + lane_base + K::COL_O + c, o);
+#pragma unroll
+                            for (int x = 0; x < 16; ++x) o[x] *= alpha[SPLIT ? (c + x) / 2 : (c + x)];
+                            tmem_st16(tmem + lane_base + K::COL_O + c, o);
+                        }
+                    }
+                    // keep red[] stable until every thread has read it
+                    named_bar_sync(1, kSoftThreads);
                 }
-                // P^T row of this token: NPAD bf16 columns, MN-major core-matrix layout
-                uint8_t* pdst = smem + K::OFF_P + (t & 1) * K::PBUF + tt * 16;
+                float pr[RMAX];
+#pragma unroll
+                for (int n = 0; n < RMAX; ++n) {
+                    pr[n] = (s[n] == -INFINITY) ? 0.f : exp2f(s[n] - m_ref[n]);
+                    l_part[n] += pr[n];
+                }
+                // P buffer t % NSB is free once the P.V of tile t - NSB has completed
+                if (t >= NSB) wait_bar(bar(B::PEMPTY + t % NSB), ((t / NSB) - 1) & 1, ctl);
+                uint8_t* pdst = smem + K::OFF_P + (t % NSB) * K::PBUF + tt * 16;
 #pragma unroll
                 for (int cc = 0; cc < NPAD / 8; ++cc) {
                     uint32_t w4[4];
@@ -432,10 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                     for (int h = 0; h < 4; ++h) {
                         float a, b;
                         if constexpr (SPLIT) {
-                            const int r = cc * 4 + h;          // columns 2r (high) and 2r+1 (low)
-                            const float hi = __bfloat162float(__float2bfloat16_rn(pr[r]));
+                            const int n = cc * 4 + h;          // physical columns 2n (high) and 2n+1 (low)
+                            const float hi = __bfloat162float(__float2bfloat16_rn(pr[n]));
                             a = hi;
-                            b = pr[r] - hi;
+                            b = pr[n] - hi;
                         } else {
                             a = pr[cc * 8 + 2 * h];
                             b = pr[cc * 8 + 2 * h + 1];
@@ -445,80 +612,98 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                     *reinterpret_cast<uint4*>(pdst + cc * (16 * 128)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
                 // unwritten tail slots of the sequence's last page: zero their V rows (they may hold NaN)
-                if (pgi < np && pos >= L) {
-                    wait_bar(bar(B::VFULL + st), (t / NS) & 1, ctl);
-                    uint8_t* vrow = smem + K::OFF_V + st * (K::TILE + K::VSLACK) + pgi * K::PAGE +
+                if (k < np && pos >= L) {
+                    wait_bar(bar(B::VFULL + vs), (t / NSV) & 1, ctl);
+                    uint8_t* vrow = smem + K::OFF_V + vs * (K::TILE + K::VSLACK) + k * K::PAGE +
                                     ((tt & 15) >> 3) * (K::NCH * 128) + (tt & 7) * 16;
 #pragma unroll
                     for (int c = 0; c < K::NCH; ++c) *reinterpret_cast<uint4*>(vrow + c * 128) = make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(bar(B::PFULL + (t & 1)));
-                if (jt > 0) correct(t - 1);
-#pragma unroll
-                for (int r = 0; r < RMAX; ++r) alpha_prev[r] = alpha[r];
+                mbar_arrive(bar(B::PFULL + t % NSB));
             }
             if (aborted) break;
-            correct(t - 1);
 
-            // ---- epilogue of the piece: row sums, then output or partial
+            // ---- epilogue of the piece: column sums (while the last P.V runs), O^T from
+            // TMEM, then output or partial
 #pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-                if (r < R) {
-                    float v = l_part[r];
+            for (int n = 0; n < RMAX; ++n) {
+                if (n < ncol) {
+                    float v = l_part[n];
 #pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0) lred[warp * RMAX + r] = v;
+                    for (int o2 = 16; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
+                    if (lane == 0) lred[warp * RMAX + n] = v;
                 }
             }
             named_bar_sync(1, kSoftThreads);
             float Lsum[RMAX];
 #pragma unroll
-            for (int r = 0; r < RMAX; ++r)
-                Lsum[r] = (r < R) ? lred[r] + lred[RMAX + r] + lred[2 * RMAX + r] + lred[3 * RMAX + r] : 1.f;
-            named_bar_sync(1, kSoftThreads);
+            for (int n = 0; n < RMAX; ++n)
+                Lsum[n] = n < ncol ? lred[n] + lred[RMAX + n] + lred[2 * RMAX + n] + lred[3 * RMAX + n] : 1.f;
+            wait_bar(bar(B::PEMPTY + (t - 1) % NSB), ((t - 1) / NSB) & 1, ctl);
+            tc_fence_after();
+            float o[NPAD];
+#pragma unroll
+            for (int c = 0; c < NPAD; c += 16) {
+                float tmp[16];
+                tmem_ld16(tmem + lane_base + K::COL_O + c, tmp);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) o[c + x] = tmp[x];
+            }
+            tc_fence_before();
+            float acc[RMAX];
+#pragma unroll
+            for (int n = 0; n < RMAX; ++n) acc[n] = SPLIT ? (o[2 * n] + o[2 * n + 1]) : o[n];
+            named_bar_sync(1, kSoftThreads);     // lred may be reused by the next piece
             const bool complete = (it.S0 >= u0) && (it.S1 <= u1);
             if (complete) {
                 if (tt < D) {
 #pragma unroll
-                    for (int r = 0; r < RMAX; ++r) {
-                        if (r < R) {
-                            const int i = r / G, hl = r % G;
-                            p.out[((size_t)(it.cur.qoff + i) * p.num_q_heads + it.g * G + hl) * D + tt] =
-                                __float2bfloat16_rn(acc[r] / Lsum[r]);
-                        }
-                    }
+                    for (int n = 0; n < RMAX; ++n)
+                        if (n < ncol)
+                            p.out[col_row_offset(p, it.cur.qoff, R, it.hg, n, D) + tt] =
+                                __float2bfloat16_rn(acc[n] / Lsum[n]);
                 }
             } else {
                 float* slot = slot_ptr(p, cta, it.S0, u0);
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r) {
-                    if (r < R) {
-                        if (tt == r) {
-                            slot[r] = m_run[r];
-                            slot[p.rows_pad + r] = Lsum[r];
+                for (int n = 0; n < RMAX; ++n) {
+                    if (n < ncol) {
+                        if (tt == n) {
+                            slot[n] = m_ref[n];
+                            slot[p.rows_pad + n] = Lsum[n];
                         }
-                        if (tt < D) slot[2 * p.rows_pad + (size_t)r * D + tt] = acc[r];
+                        if (tt < D) slot[2 * p.rows_pad + (size_t)n * D + tt] = acc[n];
                     }
                 }
                 __threadfence();
                 named_bar_sync(1, kSoftThreads);
                 if (tt == 0) {
                     const int need = owner_cta(it.S1 - 1, W, P) - owner_cta(it.S0, W, P) + 1;
-                    const int old = atomicAdd(p.tickets + st_b * Hkv + it.g, 1);
-                    const int last = (old == need - 1);
-                    if (last) p.tickets[st_b * Hkv + it.g] = 0;
-                    *ticket_flag = last;
+                    const int tix = seg_b * Hkv + it.hg;
+                    const int old = atomicAdd(p.tickets + tix, 1);
+                    if (old == need - 1) {
+                        // last piece of this segment: hand the merge to the merge warp
+                        p.tickets[tix] = 0;
+                        __threadfence();
+                        int* task = reinterpret_cast<int*>(smem + K::OFF_MQ) + (n_tasks & 3) * 8;
+                        task[0] = seg_b;
+                        task[1] = it.hg;
+                        task[2] = it.cur.qoff;
+                        task[3] = Q;
+                        task[4] = it.S0;
+                        task[5] = it.S1;
+                        mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
+                        ++n_tasks;
+                    }
                 }
-                named_bar_sync(1, kSoftThreads);
-                if (*ticket_flag) {
-                    __threadfence();
-                    merge_segment<kSoftThreads>(p, it.cur, it.g, it.S0, it.S1, W, P, D);
-                }
-                named_bar_sync(1, kSoftThreads);
             }
             it.advance(p);
+        }
+        if (tt == 0) {   // sentinel for the merge warp
+            reinterpret_cast<int*>(smem + K::OFF_MQ)[(n_tasks & 3) * 8] = -1;
+            mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
         }
     }
 
@@ -531,24 +716,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     }
 }
 
-template <int D, int NPAD, bool SPLIT, int NS>
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV>
 static cudaError_t launch_t(const AttnParams& p, int ncta, cudaStream_t st) {
-    using K = Cfg<D, NPAD, SPLIT, NS>;
-    auto kern = attn_tc_kernel<D, NPAD, SPLIT, NS>;
+    using K = Cfg<D, NPAD, SPLIT, NSK, NSV>;
+    auto kern = attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<ncta, kThreads, K::SMEM, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(ncta), dim3(kThreads), K::SMEM, st, p);
 }
 
 }  // namespace tc
 
+// Columns per segment for the tensor-core kernel: up to 8 (with the bf16
+// high/low split of P, N = 16) when the rows of one kv-head fit, else up to 32.
+static int tc_col_limit(int rows) { return rows <= 8 ? 8 : 32; }
+
+// kv-heads per segment: the largest divisor of Hkv whose columns
+// (heads x G x max_q_len) fit the column limit.
+int tc_heads_per_segment(int num_kv_heads, int rows) {
+    const int lim = tc_col_limit(rows);
+    int hg = 1;
+    for (int h = 1; h <= num_kv_heads; ++h)
+        if (num_kv_heads % h == 0 && h * rows <= lim) hg = h;
+    return hg;
+}
+
 // bf16 cache, head_dim 64/128, R = G * max_q_len <= 32.
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, int ncta, cudaStream_t st) {
-    const bool small = p.rows <= 8;
+    const bool split = tc_col_limit(p.rows) == 8;
     if (head_dim == 128)
-        return small ? tc::launch_t<128, 16, true, 3>(p, ncta, st) : tc::launch_t<128, 32, false, 3>(p, ncta, st);
-    return small ? tc::launch_t<64, 16, true, 6>(p, ncta, st) : tc::launch_t<64, 32, false, 6>(p, ncta, st);
+        return split ? tc::launch_t<128, 16, true, 2, 4>(p, ncta, st) : tc::launch_t<128, 32, false, 2, 3>(p, ncta, st);
+    return split ? tc::launch_t<64, 16, true, 4, 6>(p, ncta, st) : tc::launch_t<64, 32, false, 4, 6>(p, ncta, st);
 }
 
 }  // namespace pkv

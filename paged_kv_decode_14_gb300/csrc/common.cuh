@@ -41,6 +41,30 @@ __device__ __forceinline__ void raise_error(int* err, int bits) {
     if (err) atomicOr(err, bits);
 }
 
+// Programmatic dependent launch: a kernel launched with
+// programmaticStreamSerialization may start while the previous kernel on the
+// stream runs; griddep_wait() blocks until that kernel has completed and its
+// memory is visible (a no-op for a normal launch).  griddep_launch() lets the
+// next kernel on the stream start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+template <typename... Args>
+__host__ inline cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ------------------------------------------------------------------ workspace
 
 struct WorkspaceLayout {
@@ -88,6 +112,15 @@ struct AttnParams {
     int rows_pad;              // slot row capacity
     int slot_floats;
     float scale_log2;          // scale * log2(e)
+    int hg;                    // kv-heads per segment (tensor-core kernel; 1 elsewhere)
+};
+
+// Kernel choice and grid of one attention call (see plan_attention in api.cu).
+struct AttnLaunch {
+    bool tc;        // tensor-core kernel
+    int ncta;       // grid size
+    int rows_pad;   // partial-slot rows
+    int hg;         // kv-heads per segment
 };
 
 // ------------------------------------------------------------------ planning
@@ -140,12 +173,85 @@ __device__ __forceinline__ int block_scan_incl(int v, int* scratch /* NT/32 + 1 
 }
 
 // Computes W (total units) and the number P = min(grid, W) of CTAs that take
-// part, and positions a cursor at the sequence holding unit u0 of this CTA.  All NT threads must call it.  CTA 0 reports invalid
-// lengths.  Returns false when the CTA has no work.
+// part, and positions a cursor at the sequence holding unit u0 of this CTA
+// (and, if tail != nullptr, one at the sequence holding its last unit u1 - 1).
+// All NT threads must call it.  CTA 0 reports invalid lengths.  Returns false
+// when the CTA has no work.
+// Block-wide inclusive scan of two ints per thread (one pass for both).
+template <int NT>
+__device__ __forceinline__ int2 block_scan2_incl(int2 v, int2* scratch /* NT/32 + 1 */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int nx = __shfl_up_sync(0xffffffffu, v.x, o), ny = __shfl_up_sync(0xffffffffu, v.y, o);
+        if (lane >= o) {
+            v.x += nx;
+            v.y += ny;
+        }
+    }
+    if (lane == 31) scratch[warp] = v;
+    __syncthreads();
+    int2 add = make_int2(0, 0), tot = make_int2(0, 0);
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const int2 x = scratch[w];
+        if (w < warp) {
+            add.x += x.x;
+            add.y += x.y;
+        }
+        tot.x += x.x;
+        tot.y += x.y;
+    }
+    scratch[NT / 32] = tot;      // every thread writes the same value
+    return make_int2(v.x + add.x, v.y + add.y);
+}
+
 template <int NT>
 __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch, Cursor* cur,
-                            int* u0_out, int* u1_out, int* W_out, int* P_out) {
+                            int* u0_out, int* u1_out, int* W_out, int* P_out, Cursor* tail = nullptr) {
     const int tid = threadIdx.x;
+    if (p.num_seqs <= NT) {
+        // one chunk: a single load of the lengths and a single two-value scan
+        __shared__ int2 s2[NT / 32 + 1];
+        __shared__ Cursor s_cur1, s_tail1;
+        const int b = tid;
+        int L = 0, Q = 0, u = 0, q = 0;
+        if (b < p.num_seqs) {
+            L = p.context_lens[b];
+            Q = p.q_lens[b];
+            if (cta == 0 && Q != 0 && !seq_valid(p, L, Q)) raise_error(p.err, PKV_DEVERR_LENGTH);
+            u = seq_units(p, L, Q);
+            q = seq_qrows(Q);
+        }
+        const int2 inc = block_scan2_incl<NT>(make_int2(u, q), s2);
+        const int W = s2[NT / 32].x;
+        const int P = min(ncta, W);
+        *W_out = W;
+        *P_out = P;
+        if (cta >= P) return false;
+        const int u0 = (int)(((int64_t)cta * W) / P);
+        const int u1 = (int)(((int64_t)(cta + 1) * W) / P);
+        *u0_out = u0;
+        *u1_out = u1;
+        const int Ub = inc.x - u;
+        if (b < p.num_seqs && u > 0) {
+            Cursor c;
+            c.b = b;
+            c.Ub = Ub;
+            c.qoff = inc.y - q;
+            c.L = L;
+            c.Q = Q;
+            c.nb = (L + kBlock - 1) / kBlock;
+            if (Ub <= u0 && u0 < Ub + u) s_cur1 = c;
+            if (Ub <= u1 - 1 && u1 - 1 < Ub + u) s_tail1 = c;
+        }
+        __syncthreads();
+        *cur = s_cur1;
+        if (tail) *tail = s_tail1;
+        return true;
+    }
+    const bool one_chunk = p.num_seqs <= NT;      // lengths stay in registers between the passes
+    int Lc = 0, Qc = 0;
     // pass 1: total units
     int total = 0;
     for (int base = 0; base < p.num_seqs; base += NT) {
@@ -155,6 +261,8 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
             int L = p.context_lens[b], Q = p.q_lens[b];
             if (cta == 0 && Q != 0 && !seq_valid(p, L, Q)) raise_error(p.err, PKV_DEVERR_LENGTH);
             u = seq_units(p, L, Q);
+            Lc = L;
+            Qc = Q;
         }
         block_scan_incl<NT>(u, scratch);
         total += scratch[NT / 32];
@@ -171,15 +279,20 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
     const int u1 = (int)(((int64_t)(cta + 1) * W) / P);
     *u0_out = u0;
     *u1_out = u1;
-    // pass 2: find b with Ub <= u0 < Ub + units(b), and its q offset
-    __shared__ Cursor s_cur;
+    // pass 2: find b with Ub <= u0 < Ub + units(b) (and the one holding u1 - 1), with q offsets
+    __shared__ Cursor s_cur, s_tail;
     int run_u = 0, run_q = 0;
     for (int base = 0; base < p.num_seqs; base += NT) {
         int b = base + tid;
         int u = 0, q = 0, L = 0, Q = 0;
         if (b < p.num_seqs) {
-            L = p.context_lens[b];
-            Q = p.q_lens[b];
+            if (one_chunk) {
+                L = Lc;
+                Q = Qc;
+            } else {
+                L = p.context_lens[b];
+                Q = p.q_lens[b];
+            }
             u = seq_units(p, L, Q);
             q = seq_qrows(Q);
         }
@@ -190,19 +303,23 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         int tot_q = scratch[NT / 32];
         __syncthreads();
         int Ub = run_u + iu - u;
-        if (b < p.num_seqs && u > 0 && Ub <= u0 && u0 < Ub + u) {
-            s_cur.b = b;
-            s_cur.Ub = Ub;
-            s_cur.qoff = run_q + iq - q;
-            s_cur.L = L;
-            s_cur.Q = Q;
-            s_cur.nb = (L + kBlock - 1) / kBlock;
+        if (b < p.num_seqs && u > 0) {
+            Cursor c;
+            c.b = b;
+            c.Ub = Ub;
+            c.qoff = run_q + iq - q;
+            c.L = L;
+            c.Q = Q;
+            c.nb = (L + kBlock - 1) / kBlock;
+            if (Ub <= u0 && u0 < Ub + u) s_cur = c;
+            if (Ub <= u1 - 1 && u1 - 1 < Ub + u) s_tail = c;
         }
         run_u += tot_u;
         run_q += tot_q;
     }
     __syncthreads();
     *cur = s_cur;
+    if (tail) *tail = s_tail;
     return true;
 }
 
