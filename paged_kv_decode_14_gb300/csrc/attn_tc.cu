@@ -238,11 +238,13 @@ __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q,
                 for (int x = 0; x < DPL; ++x) num[k][x] = num[k][x] * wo + a[k][x] * wn;
             }
         }
+        const size_t my_off = n0 + lane < ncol ? col_row_offset(p, qoff, R, hg, n0 + lane, D) : 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int n = n0 + k;
+            const size_t off = __shfl_sync(0xffffffffu, my_off, k);
             if (n < ncol) {
-                __nv_bfloat16* o = p.out + col_row_offset(p, qoff, R, hg, n, D);
+                __nv_bfloat16* o = p.out + off;
 #pragma unroll
                 for (int x = 0; x < DPL; ++x) o[lane + 32 * x] = __float2bfloat16_rn(num[k][x] / den[k]);
             }
@@ -658,12 +660,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
             named_bar_sync(1, kSoftThreads);     // lred may be reused by the next piece
             const bool complete = (it.S0 >= u0) && (it.S1 <= u1);
             if (complete) {
-                if (tt < D) {
+                // column n's output row offset, computed by lane n and broadcast
+                const size_t my_off = lane < ncol ? col_row_offset(p, it.cur.qoff, R, it.hg, lane, D) : 0;
 #pragma unroll
-                    for (int n = 0; n < RMAX; ++n)
-                        if (n < ncol)
-                            p.out[col_row_offset(p, it.cur.qoff, R, it.hg, n, D) + tt] =
-                                __float2bfloat16_rn(acc[n] / Lsum[n]);
+                for (int n = 0; n < RMAX; ++n) {
+                    const size_t off = __shfl_sync(0xffffffffu, my_off, n);
+                    if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(acc[n] / Lsum[n]);
                 }
             } else {
                 float* slot = slot_ptr(p, cta, it.S0, u0);
