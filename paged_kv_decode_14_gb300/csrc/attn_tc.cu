@@ -20,9 +20,16 @@
 //   O^T[128 d, N]  += V_tile^T[d, 128 tok] . P^T[128 tok, N] (M=128, MN-major A and B)
 // K and V pages sit in separate rings: a K slot is refilled as soon as its
 // S^T MMA has run, a V slot once its P.V MMA has.
-// O^T stays in TMEM for the whole piece; the softmax reference max of a
-// column is only raised (and O^T rescaled in TMEM) when a logit exceeds it by
-// more than 2^8, so most tiles need neither a max reduction nor a rescale.
+//
+// Softmax warpgroups.  With NWG = 2, two warpgroups take the tiles in turn,
+// each with its own online-softmax state and its own O^T accumulator, so the
+// latency of one tile's softmax overlaps the next tile's; the piece epilogue
+// brings the two parts to a common reference and adds them.  O^T stays in
+// TMEM for the whole piece (pieces alternate between two sets of
+// accumulators, so a piece's epilogue overlaps the next piece's first tiles).
+// The softmax reference max of a column is only raised (and O^T rescaled in
+// TMEM) when a logit exceeds it by more than 2^8, so most tiles need neither a
+// max reduction nor a rescale.
 //
 // The cache's page layout (16-byte chunks, core matrices of 8 tokens x 16
 // bytes, see pagedkv.h) is the tensor core's no-swizzle canonical layout: K
@@ -36,13 +43,19 @@
 // the start, so both pieces of every segment cut between two CTAs finish
 // early and their merge overlaps the rest of the work.
 //
-// Warp roles (256 threads): warps 0-3 softmax, O rescale and piece epilogue
-// (their TMEM lane quarters), warp 4 producer (bulk copies, q staging), warp
-// 5 issues the S^T MMAs, warp 7 the P.V MMAs (each blocks on its own
-// barriers, so a P.V never waits behind the next tiles' S^T), warp 6 merges
-// split segments.  Every mbarrier wait is bounded
-// (2 s); a timeout sets PKV_DEVERR_TIMEOUT and an abort flag, all roles wind
-// down, in-flight copies are drained and TMEM is freed before the CTA exits.
+// Split segments: a split piece's epilogue stores its partial (m, l, acc) and
+// hands it to the merge warp, which reads the segment's ticket: when every
+// other piece is already published it merges at once; otherwise it publishes
+// the partial (fence, ticket increment) and merges if its ticket was the last.
+//
+// Warp roles (128 NWG + 128 threads): warps 0 .. 4 NWG - 1 softmax, O rescale
+// and piece epilogue (each warp its TMEM lane quarter), then the producer
+// (bulk copies, q staging, one piece ahead on q and the block table), the
+// S^T issuer, the merge warp and the P.V issuer (the two issuers block on
+// their own barriers, so a P.V never waits behind the next tiles' S^T).
+// Every mbarrier wait is bounded (2 s); a timeout sets PKV_DEVERR_TIMEOUT and
+// an abort flag, all roles wind down, in-flight copies are drained and TMEM
+// is freed before the CTA exits.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -53,9 +66,7 @@ using namespace ptx;
 
 constexpr int kTP = 8;                        // units (pages of one kv-head) per tile
 constexpr int kTileTok = kTP * kBlock;        // 128 token rows = MMA M
-constexpr int kThreads = 256;
-constexpr int kProducerWarp = 4, kMmaWarp = 5, kMergeWarp = 6, kPvWarp = 7;
-constexpr int kSoftThreads = 128;
+constexpr int kSoftThreads = 128;             // one softmax warpgroup (the 128 TMEM lanes)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxSmem = 232448;
 constexpr int NSB = 4;                        // S^T / P ring depth (tiles the MMA may run ahead)
@@ -63,7 +74,16 @@ constexpr int NSB = 4;                        // S^T / P ring depth (tiles the M
 // Online-softmax reference slack (powers of two), see the header comment.
 constexpr float kRescaleSlack = 8.f;
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV>
+// NWG softmax warpgroups (warps 0 .. 4 NWG - 1) take the tiles in turn, then
+// four single-warp roles.
+template <int NWG>
+struct Roles {
+    static constexpr int kThreads = kSoftThreads * NWG + 128;
+    static constexpr int kProducerWarp = 4 * NWG, kMmaWarp = 4 * NWG + 1, kMergeWarp = 4 * NWG + 2,
+                         kPvWarp = 4 * NWG + 3;
+};
+
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, int NWG>
 struct Cfg {
     static constexpr int RMAX = SPLIT ? NPAD / 2 : NPAD;  // logical columns
     static constexpr int PAGE = kBlock * D * 2;
@@ -76,19 +96,25 @@ struct Cfg {
     static constexpr int QBUF = NPAD * D * 2;
     static constexpr int OFF_P = OFF_Q + 2 * QBUF;
     static constexpr int PBUF = NPAD * kTileTok * 2;
-    static constexpr int OFF_RED = OFF_P + NSB * PBUF;  // float [8 slots][RMAX]
-    static constexpr int OFF_LRED = OFF_RED + 8 * RMAX * 4;   // float [4 warps][RMAX]
-    static constexpr int OFF_BAR = OFF_LRED + 4 * RMAX * 4;
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 10;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem addr, abort, zero
+    static constexpr int OFF_RED = OFF_P + NSB * PBUF;                 // float [NWG][8 slots][RMAX]
+    static constexpr int OFF_LRED = OFF_RED + NWG * 8 * RMAX * 4;      // float [2][NWG][4 warps][RMAX]
+    static constexpr int OFF_EM = OFF_LRED + 2 * NWG * 4 * RMAX * 4;   // float [2][NWG][RMAX]
+    static constexpr int OFF_BAR = OFF_EM + 2 * NWG * RMAX * 4;
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 13;
+    static constexpr int OFF_MISC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // tmem addr, abort, zero
     static constexpr int OFF_MQ = OFF_MISC + 16;         // merge tasks: int [4][8]
-    static constexpr int SMEM_USED = OFF_MQ + 128 + 128; // + base alignment slack
+    static constexpr int OFF_SEQ = OFF_MQ + 128;         // int4 [threads]: per-sequence (L, Q, Ub, qoff)
+    static constexpr int SMEM_USED = OFF_SEQ + Roles<NWG>::kThreads * 16 + 128;  // + base alignment slack
     // One CTA per SM either way: take the whole per-block budget, so every
     // operand read the descriptors can form stays inside the allocation.
     static constexpr int SMEM = kMaxSmem - 1024;
     static constexpr int COL_S = 0;                      // S^T buffers: NSB x NPAD columns
-    static constexpr int COL_O = NSB * NPAD;             // O^T accumulator: NPAD columns
-    static constexpr int TMEM_COLS = (NSB + 1) * NPAD <= 64 ? 64 : (NSB + 1) * NPAD <= 128 ? 128 : 256;
+    // O^T accumulators: [piece parity][warpgroup] x NPAD columns
+    static constexpr int COL_O = NSB * NPAD;
+    static constexpr int NCOLS = (NSB + 2 * NWG) * NPAD;
+    static constexpr int TMEM_COLS = NCOLS <= 64 ? 64 : NCOLS <= 128 ? 128 : 256;
+    static_assert(NCOLS <= 256, "TMEM budget");
+    static_assert(OFF_BAR % 8 == 0 && OFF_SEQ % 16 == 0 && OFF_RED % 16 == 0, "shared memory alignment");
     static_assert(SMEM_USED <= SMEM, "shared memory budget");
 };
 
@@ -96,7 +122,9 @@ template <int NSK, int NSV>
 struct Bars {
     static constexpr int KFULL = 0, KEMPTY = NSK, VFULL = 2 * NSK, VEMPTY = 2 * NSK + NSV,
                          SFULL = 2 * NSK + 2 * NSV, PFULL = SFULL + NSB, PEMPTY = PFULL + NSB,
-                         QFULL = PEMPTY + NSB, QEMPTY = QFULL + 2, DONE = QEMPTY + 2, MQFULL = DONE + 2;
+                         QFULL = PEMPTY + NSB, QEMPTY = QFULL + 2, DONE = QEMPTY + 2, MQFULL = DONE + 2,
+                         ODONE = MQFULL + 4,      // [2]: last P.V of a piece of that parity done
+                         PEND = ODONE + 2;        // every softmax thread finished its part of a piece
 };
 
 struct Ctl {
@@ -106,20 +134,31 @@ struct Ctl {
 
 // Bounded wait: spins on try_wait; gives up after kWaitLimitNs or once the
 // CTA's abort flag is set.  A timeout raises PKV_DEVERR_TIMEOUT and the flag.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The spin loop is out of line: only the first try sits in the callers' code.
+__device__ __noinline__ bool wait_bar_spin(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 0) {
-            if (*c.abort) return false;
+            if (*abort) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                raise_error(c.err, PKV_DEVERR_TIMEOUT);
-                *c.abort = 1;
+                raise_error(err, PKV_DEVERR_TIMEOUT);
+                *abort = 1;
                 return false;
             }
         }
     }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_spin(bar, parity, c.abort, c.err);
+}
+
+// 2^x by the SFU (flushes subnormal results to zero, 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ bool bar_red_or(int id, int n, bool v) {
@@ -142,6 +181,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // that piece) front to back.  Segment = (sequence, group of HG kv-heads), its
 // units = pages x HG in page-major order.  Every role walks it the same way.
 struct PieceIter {
+    const int4* tab;            // per-sequence table in shared memory, or nullptr
     Cursor cur, fcur;
     int u, stop, u0, HG, Hkv;
     bool tail_phase;
@@ -187,7 +227,7 @@ struct PieceIter {
             return;
         }
         u += npg;
-        if (u < stop && u == cur.Ub + cur.nb * Hkv) cursor_next(p, cur);
+        if (u < stop && u == cur.Ub + cur.nb * Hkv) cursor_next(p, cur, tab);
         if (u < stop) load_at(u, stop);
     }
 };
@@ -198,8 +238,22 @@ __device__ __forceinline__ size_t col_row_offset(const AttnParams& p, int qoff, 
     return ((size_t)(qoff + i) * p.num_q_heads + (hg * p.hg + hh) * p.group + hl) * D;
 }
 
+// One step of the online merge of split partials (m, l, a): the running
+// (M, den, num) and the new piece are both brought to the larger reference.
+// Written with explicit roundings so the merge gives the same bits wherever
+// it is inlined.
+__device__ __forceinline__ void merge_weights(float& M, float m, float& wo, float& wn) {
+    const float mn = fmaxf(M, m);
+    wo = (M == -INFINITY) ? 0.f : fast_exp2(M - mn);
+    wn = (m == -INFINITY) ? 0.f : fast_exp2(m - mn);
+    M = mn;
+}
+__device__ __forceinline__ float merge_acc(float x, float wo, float y, float wn) {
+    return __fmaf_rn(y, wn, __fmul_rn(x, wo));
+}
+
 // Merge the partials of segment [S0, S1) (NCOL columns) into out; one warp,
-// one round trip of loads per piece (online merge across pieces).
+// one round trip of loads per piece, pieces in CTA order.
 template <int D>
 __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q, int S0, int S1, int W, int P,
                                    int lane) {
@@ -229,13 +283,11 @@ __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q,
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const float mn = fmaxf(M[k], m[k]);
-                const float wo = (M[k] == -INFINITY) ? 0.f : exp2f(M[k] - mn);
-                const float wn = (m[k] == -INFINITY) ? 0.f : exp2f(m[k] - mn);
-                M[k] = mn;
-                den[k] = den[k] * wo + l[k] * wn;
+                float wo, wn;
+                merge_weights(M[k], m[k], wo, wn);
+                den[k] = merge_acc(den[k], wo, l[k], wn);
 #pragma unroll
-                for (int x = 0; x < DPL; ++x) num[k][x] = num[k][x] * wo + a[k][x] * wn;
+                for (int x = 0; x < DPL; ++x) num[k][x] = merge_acc(num[k][x], wo, a[k][x], wn);
             }
         }
         const size_t my_off = n0 + lane < ncol ? col_row_offset(p, qoff, R, hg, n0 + lane, D) : 0;
@@ -246,17 +298,20 @@ __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q,
             if (n < ncol) {
                 __nv_bfloat16* o = p.out + off;
 #pragma unroll
-                for (int x = 0; x < DPL; ++x) o[lane + 32 * x] = __float2bfloat16_rn(num[k][x] / den[k]);
+                for (int x = 0; x < DPL; ++x) o[lane + 32 * x] = __float2bfloat16_rn(__fdividef(num[k][x], den[k]));
             }
         }
     }
 }
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV>
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p) {
-    using K = Cfg<D, NPAD, SPLIT, NSK, NSV>;
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, int NWG>
+__global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const AttnParams p) {
+    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, NWG>;
     using B = Bars<NSK, NSV>;
     constexpr int RMAX = K::RMAX;
+    constexpr int kThreads = Roles<NWG>::kThreads;
+    constexpr int kProducerWarp = Roles<NWG>::kProducerWarp, kMmaWarp = Roles<NWG>::kMmaWarp,
+                  kMergeWarp = Roles<NWG>::kMergeWarp, kPvWarp = Roles<NWG>::kPvWarp;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int scratch[kThreads / 32 + 1];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -297,7 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         }
         mbar_init(bar(B::DONE), 1);
         mbar_init(bar(B::DONE + 1), 1);
-        for (int i = 0; i < 4; ++i) mbar_init(bar(B::MQFULL + i), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B::MQFULL + i), kSoftThreads);
+        mbar_init(bar(B::ODONE), 1);
+        mbar_init(bar(B::ODONE + 1), 1);
+        mbar_init(bar(B::PEND), kSoftThreads * NWG);
         *abort_flag = 0;
         *never = 0;
         mbar_fence_init();
@@ -308,7 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     griddep_wait();
     Cursor cur0, curt;
     int u0, u1, W, P;
-    const bool has_work = plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt);
+    int4* seqtab = reinterpret_cast<int4*>(smem + K::OFF_SEQ);
+    const bool has_work =
+        plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt, seqtab);
     if (!has_work) return;       // uniform across the CTA; no TMEM held yet
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), K::TMEM_COLS);
@@ -321,14 +381,55 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     const int G = p.group, Hkv = p.num_kv_heads, HG = p.hg;
 
     PieceIter it;
+    it.tab = p.num_seqs <= kThreads ? seqtab : nullptr;
     it.init(p, cur0, curt, u0, u1);
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
+        // Runs one piece ahead on its inputs: while piece j streams, the q rows
+        // and the first block-table window of piece j + 1 are in flight, and
+        // within a piece the next 32-page window of the block table is loaded
+        // while the current one is used, so no copy waits on a table read.
         const uint64_t pol = policy_evict_first();
+        constexpr int QV = (RMAX * K::NCH + 31) / 32;
+        constexpr bool kQAhead = QV <= 4;         // wide pieces load their q at the piece start
         int t = 0, j = 0, kcount = 0, vcount = 0;
         bool ok = true;
+        // q rows of piece `pi` in column order, 16 bytes per lane and step
+        auto load_q = [&](const PieceIter& pi, uint4 (&v)[QV]) {
+            const int R = G * pi.cur.Q, ncol = HG * R;
+#pragma unroll
+            for (int k = 0; k < QV; ++k) {
+                const int idx = lane + 32 * k;
+                v[k] = make_uint4(0, 0, 0, 0);
+                if (idx < ncol * K::NCH) {
+                    const int n = idx / K::NCH, c = idx % K::NCH;
+                    v[k] = __ldg(reinterpret_cast<const uint4*>(p.q + col_row_offset(p, pi.cur.qoff, R, pi.hg, n, D) +
+                                                                c * 8));
+                }
+            }
+        };
+        // block-table entries [ws, ws + 32) of piece `pi`'s sequence, entry ws + lane per lane
+        auto load_win = [&](const PieceIter& pi, int ws) -> int {
+            const int32_t* table = p.block_tables + (size_t)pi.cur.b * p.max_blocks_per_seq;
+            return ws + lane < pi.cur.nb ? __ldg(table + ws + lane) : 0;
+        };
+        uint4 qv[QV];
+        int win = 0;
+        if (it.valid()) {
+            if constexpr (kQAhead) load_q(it, qv);
+            win = load_win(it, it.pg0 / HG);
+        }
         while (ok && it.valid()) {
+            PieceIter nx = it;
+            nx.advance(p);
+            uint4 qn[kQAhead ? QV : 1];
+            int winn = 0;
+            if (nx.valid()) {
+                if constexpr (kQAhead) load_q(nx, qn);
+                winn = load_win(nx, nx.pg0 / HG);
+            }
+            if constexpr (!kQAhead) load_q(it, qv);
             const int qb = j & 1;
             if (j >= 2) {
                 bool w = lane == 0 ? wait_bar(bar(B::QEMPTY + qb), ((j >> 1) - 1) & 1, ctl) : true;
@@ -336,19 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                 if (!ok) break;
             }
             const int R = G * it.cur.Q, ncol = HG * R;
-            const int32_t* table = p.block_tables + (size_t)it.cur.b * p.max_blocks_per_seq;
-            int ids = 0, ids_start = -1000000;      // ids: table entry of page ids_start + lane
+            int ws = it.pg0 / HG;                         // win: entries [ws, ws + 32); win2: the next 32
+            int win2 = load_win(it, ws + 32);
             for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
                 const int np = min(kTP, it.npg - t0);
                 const int ks = t % NSK, vs = t % NSV;
                 const int qfirst = it.pg0 + t0;                       // first unit of the tile
-                const int jfirst = qfirst / HG, jlast = (qfirst + np - 1) / HG;
-                if (jfirst < ids_start || jlast >= ids_start + 32) {
-                    ids_start = jfirst;
-                    ids = ids_start + lane < it.cur.nb ? table[ids_start + lane] : 0;
-                }
                 const int qu = qfirst + (lane & 7);
-                int blk = __shfl_sync(0xffffffffu, ids, (qu / HG - ids_start) & 31);
+                const int pg = qu / HG - ws;                          // in [0, 40) for the tile's units
+                const int e1 = __shfl_sync(0xffffffffu, win, pg & 31);
+                const int e2 = __shfl_sync(0xffffffffu, win2, pg & 31);
+                int blk = pg < 32 ? e1 : e2;
                 if (blk < 0 || blk >= p.num_blocks) {
                     if (lane < np) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
                     blk = 0;
@@ -366,26 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                                   bar(B::KFULL + ks), pol);
                 ++kcount;
                 if (t0 == 0) {
-                    // q rows of the segment's columns -> Q buffer (K-major core
-                    // matrices), loaded while the first K tile is in flight
+                    // the piece's q rows -> Q buffer (K-major core matrices)
                     uint8_t* qdst = smem + K::OFF_Q + qb * K::QBUF;
-                    constexpr int QV = (RMAX * K::NCH + 31) / 32;
-                    uint4 v[QV];
 #pragma unroll
                     for (int k = 0; k < QV; ++k) {
                         const int idx = lane + 32 * k;
                         if (idx < ncol * K::NCH) {
                             const int n = idx / K::NCH, c = idx % K::NCH;
-                            v[k] = __ldg(reinterpret_cast<const uint4*>(
-                                p.q + col_row_offset(p, it.cur.qoff, R, it.hg, n, D) + c * 8));
-                        }
-                    }
-#pragma unroll
-                    for (int k = 0; k < QV; ++k) {
-                        const int idx = lane + 32 * k;
-                        if (idx < ncol * K::NCH) {
-                            const int n = idx / K::NCH, c = idx % K::NCH;
-                            *reinterpret_cast<uint4*>(qdst + (n >> 3) * (K::NCH * 128) + c * 128 + (n & 7) * 16) = v[k];
+                            *reinterpret_cast<uint4*>(qdst + (n >> 3) * (K::NCH * 128) + c * 128 + (n & 7) * 16) = qv[k];
                         }
                     }
                     fence_proxy_async_smem();
@@ -404,9 +491,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                                   K::PAGE, bar(B::VFULL + vs), pol);
                 ++vcount;
                 __syncwarp();
+                // slide the table window once a tile has reached the next one
+                if ((qfirst + np - 1) / HG - ws >= 32 && t0 + kTP < it.npg) {
+                    ws += 32;
+                    win = win2;
+                    win2 = load_win(it, ws + 32);
+                }
             }
             ++j;
-            if (ok) it.advance(p);
+            it = nx;
+            if constexpr (kQAhead) {
+#pragma unroll
+                for (int k = 0; k < QV; ++k) qv[k] = qn[k];
+            }
+            win = winn;
         }
         // drain: every copy issued has landed before the CTA exits
         if (lane == 0) {
@@ -453,16 +551,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         __syncwarp();
     } else if (warp == kPvWarp) {
         // ------------------------------------------------------------ P.V issuer
-        // O^T += V^T P^T of tile t once its P is written and its V has landed;
-        // the first tile of a piece starts O^T afresh.
+        // O^T += V^T P^T of tile t once its P is written and its V has landed.
         if (lane == 0) {
             constexpr uint32_t idPV = idesc_bf16_f32(128, NPAD, true, true);
-            int t = 0;
+            int t = 0, pc = 0;
             bool ok = true;
             while (ok && it.valid()) {
                 for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
                     const int np = min(kTP, it.npg - t0);
                     const int vs = t % NSV;
+                    // the tile's warpgroup accumulates into its own O^T; its first tile of the piece starts afresh
+                    const uint32_t ocol = tmem + K::COL_O + ((pc & 1) * NWG + t % NWG) * NPAD;
+                    const bool fresh = t0 < NWG * kTP;
                     if (!(ok = wait_bar(bar(B::PFULL + t % NSB), (t / NSB) & 1, ctl))) break;
                     if (!(ok = wait_bar(bar(B::VFULL + vs), (t / NSV) & 1, ctl))) break;
                     tc_fence_after();
@@ -471,11 +571,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                     for (int pg = 0; pg < np; ++pg) {
                         const uint64_t a = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
                         const uint64_t b = smem_desc(pbase + pg * 256, 128, 16 * 128);
-                        mma_bf16(tmem + K::COL_O, a, b, idPV, (pg > 0 || t0 > 0) ? 1u : 0u);
+                        mma_bf16(ocol, a, b, idPV, (pg > 0 || !fresh) ? 1u : 0u);
                     }
                     mma_commit(bar(B::PEMPTY + t % NSB));
                     mma_commit(bar(B::VEMPTY + vs));
+                    if (t0 + kTP >= it.npg) mma_commit(bar(B::ODONE + (pc & 1)));
                 }
+                ++pc;
                 if (ok) it.advance(p);
             }
             mma_commit(bar(B::DONE + 1));
@@ -483,39 +585,69 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         }
         __syncwarp();
     } else if (warp == kMergeWarp) {
-        // ------------------------------------------------------------ merges of split segments
+        // ------------------------------------------------------------ ticket and merge of published partials
+        // A task is a split piece whose partial the softmax warps have stored;
+        // this warp reads the segment's ticket: when every other piece is
+        // published it merges at once, else it makes the partial visible
+        // GPU-wide, draws a ticket and merges if that ticket is the last one.
         int* mq = reinterpret_cast<int*>(smem + K::OFF_MQ);
         for (int n = 0;; ++n) {
             bool w = lane == 0 ? wait_bar(bar(B::MQFULL + (n & 3)), (n >> 2) & 1, ctl) : true;
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            __syncwarp();
             const int* task = mq + (n & 3) * 8;
             if (task[0] < 0) break;                     // sentinel: the softmax warps are done
-            __threadfence();
-            merge_segment_warp<D>(p, task[1], task[2], task[3], task[4], task[5], W, P, lane);
+            const int seg_b = task[0], hg = task[1], S0 = task[4], S1 = task[5];
+            int last = 0;
+            if (lane == 0) {
+                const int need = owner_cta(S1 - 1, W, P) - owner_cta(S0, W, P) + 1;
+                int* ticket = p.tickets + seg_b * p.num_kv_heads + hg;
+                if (ld_acquire_gpu(ticket) == need - 1) {
+                    // every other piece is published (and visible): merge without publishing this one
+                    last = 1;
+                } else {
+                    __threadfence();                    // the partial (stored before the arrive) first
+                    last = atomicAdd(ticket, 1) == need - 1;
+                    __threadfence();
+                }
+                if (last) *ticket = 0;                  // ready for the next launch
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            __syncwarp();
+            if (last) merge_segment_warp<D>(p, hg, task[2], task[3], S0, S1, W, P, lane);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax / rescale / epilogue
-        const int tt = tid;                                   // token row of S^T, d row of O^T
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        float* red = reinterpret_cast<float*>(smem + K::OFF_RED);
-        float* lred = reinterpret_cast<float*>(smem + K::OFF_LRED);
-        int t = 0, n_tasks = 0;
+        // Warpgroup wg takes the tiles t with t % NWG == wg.  A piece's epilogue
+        // (the warpgroups' parts combined, then the output or a partial) runs in
+        // the warpgroup of the next piece's first tile, right after that tile.
+        const int wg = warp >> 2;
+        const int tt = tid & (kSoftThreads - 1);              // token row of S^T, d row of O^T
+        const int bwg = 1 + wg;                               // named barrier of this warpgroup
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        float* red = reinterpret_cast<float*>(smem + K::OFF_RED) + wg * (kTP * RMAX);
+        float* lred = reinterpret_cast<float*>(smem + K::OFF_LRED);   // [2][NWG][4][RMAX]
+        float* emref = reinterpret_cast<float*>(smem + K::OFF_EM);    // [2][NWG][RMAX]
+        int t = 0, n_tasks = 0, pc = 0, jt = 0, t_first = 0;
         bool aborted = false;
         float m_ref[RMAX], l_part[RMAX];
-
-        while (!aborted && it.valid()) {
-            const int Q = it.cur.Q, R = G * Q, L = it.cur.L, lim0 = L - Q, ncol = HG * R;
-            const int seg_b = it.cur.b;
+        // the finished piece whose epilogue is pending
+        bool pend = false;
+        int e_b = 0, e_hg = 0, e_qoff = 0, e_Q = 0, e_S0 = 0, e_S1 = 0, e_tfirst = 0, e_ntile = 0, e_pc = 0;
 #pragma unroll
-            for (int n = 0; n < RMAX; ++n) {
-                m_ref[n] = -INFINITY;
-                l_part[n] = 0.f;
-            }
-            const int ntile = (it.npg + kTP - 1) / kTP;
-            for (int jt = 0; jt < ntile; ++jt, ++t) {
+        for (int n = 0; n < RMAX; ++n) {
+            m_ref[n] = -INFINITY;
+            l_part[n] = 0.f;
+        }
+        bool in_piece = it.valid();
+
+        for (;;) {
+            if (in_piece && t % NWG == wg) {
+                const int Q = it.cur.Q, R = G * Q, L = it.cur.L, lim0 = L - Q;
                 const int np = min(kTP, it.npg - jt * kTP);
                 const int vs = t % NSV;
+                const uint32_t ocol = K::COL_O + ((pc & 1) * NWG + wg) * NPAD;
                 // this thread's token: unit slot k of the tile -> (page, kv-head), position
                 const int k = tt >> 4;
                 const int qu = it.pg0 + jt * kTP + k;
@@ -542,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                     s[n] = vis ? s[n] * p.scale_log2 : -INFINITY;
                     need |= s[n] > m_ref[n] + kRescaleSlack;
                 }
-                if (bar_red_or(1, kSoftThreads, need || !okw)) {
+                if (bar_red_or(bwg, kSoftThreads, need || !okw)) {
                     // raise the reference to this tile's max (first tile of a piece, or a big jump):
                     // per (unit slot, column) maxima over the slot's 16 tokens, then per column
 #pragma unroll
@@ -552,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                         for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                         if ((tt & 15) == 0) red[k * RMAX + n] = mx;
                     }
-                    if (bar_red_or(1, kSoftThreads, !okw || *abort_flag)) {
+                    if (bar_red_or(bwg, kSoftThreads, !okw || *abort_flag)) {
                         aborted = true;
                         break;
                     }
@@ -564,31 +696,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 #pragma unroll
                         for (int kk = 0; kk < kTP; ++kk) tm = fmaxf(tm, red[kk * RMAX + n]);
                         const float mn = fmaxf(m_ref[n], tm);
-                        alpha[n] = (m_ref[n] == -INFINITY) ? 0.f : exp2f(m_ref[n] - mn);
+                        alpha[n] = (m_ref[n] == -INFINITY) ? 0.f : fast_exp2(m_ref[n] - mn);
                         any_scale |= (alpha[n] != 1.f) && (m_ref[n] != -INFINITY);
                         m_ref[n] = mn;
                         l_part[n] *= alpha[n];
                     }
-                    if (jt > 0 && any_scale) {
-                        // O^T (TMEM) *= alpha once the previous tile's P.V has landed
-                        wait_bar(bar(B::PEMPTY + (t - 1) % NSB), ((t - 1) / NSB) & 1, ctl);
+                    if (jt >= NWG && any_scale) {
+                        // O^T (TMEM) *= alpha once this warpgroup's previous P.V has landed
+                        wait_bar(bar(B::PEMPTY + (t - NWG) % NSB), ((t - NWG) / NSB) & 1, ctl);
                         tc_fence_after();
 #pragma unroll
                         for (int c = 0; c < NPAD; c += 16) {
                             float o[16];
-                            tmem_ld16(tmem + lane_base + K::COL_O + c, o);
+                            tmem_ld16(tmem + lane_base + ocol + c, o);
 #pragma unroll
                             for (int x = 0; x < 16; ++x) o[x] *= alpha[SPLIT ? (c + x) / 2 : (c + x)];
-                            tmem_st16(tmem + lane_base + K::COL_O + c, o);
+                            tmem_st16(tmem + lane_base + ocol + c, o);
                         }
                     }
                     // keep red[] stable until every thread has read it
-                    named_bar_sync(1, kSoftThreads);
+                    named_bar_sync(bwg, kSoftThreads);
                 }
                 float pr[RMAX];
 #pragma unroll
                 for (int n = 0; n < RMAX; ++n) {
-                    pr[n] = (s[n] == -INFINITY) ? 0.f : exp2f(s[n] - m_ref[n]);
+                    pr[n] = (s[n] == -INFINITY) ? 0.f : fast_exp2(s[n] - m_ref[n]);
                     l_part[n] += pr[n];
                 }
                 // P buffer t % NSB is free once the P.V of tile t - NSB has completed
@@ -625,86 +757,147 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
                 tc_fence_before();
                 mbar_arrive(bar(B::PFULL + t % NSB));
             }
-            if (aborted) break;
+            if (in_piece) ++t;
 
-            // ---- epilogue of the piece: column sums (while the last P.V runs), O^T from
-            // TMEM, then output or partial
+            if (pend && (!in_piece || jt == 0)) {
+                // ---- epilogue of the previous piece, in the warpgroup of the tile just taken
+                // (or, after the last piece, of the tile that would come next)
+                pend = false;
+                const bool complete = (e_S0 >= u0) && (e_S1 <= u1);
+                if ((in_piece ? t - 1 : t) % NWG == wg) {
+                    const int R = G * e_Q, ncol = HG * R, par = e_pc & 1;
+                    named_bar_sync(bwg, kSoftThreads);     // (one warpgroup: its piece-end sums)
+                    // this piece's O^T accumulators are final once its last P.V is done
+                    wait_bar(bar(B::ODONE + par), (e_pc >> 1) & 1, ctl);
+                    tc_fence_after();
+                    float acc[RMAX], Lsum[RMAX], Mx[RMAX];
 #pragma unroll
-            for (int n = 0; n < RMAX; ++n) {
-                if (n < ncol) {
-                    float v = l_part[n];
+                    for (int n = 0; n < RMAX; ++n) {
+                        acc[n] = 0.f;
+                        Lsum[n] = 0.f;
+                        Mx[n] = -INFINITY;
+                    }
+                    // common reference: the max over the warpgroups that had tiles in the piece
 #pragma unroll
-                    for (int o2 = 16; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
-                    if (lane == 0) lred[warp * RMAX + n] = v;
+                    for (int w2 = 0; w2 < NWG; ++w2) {
+                        if (e_ntile >= NWG || e_tfirst % NWG == w2) {
+#pragma unroll
+                            for (int n = 0; n < RMAX; ++n) Mx[n] = fmaxf(Mx[n], emref[(par * NWG + w2) * RMAX + n]);
+                        }
+                    }
+#pragma unroll
+                    for (int w2 = 0; w2 < NWG; ++w2) {
+                        if (e_ntile >= NWG || e_tfirst % NWG == w2) {
+                            float o[NPAD];
+#pragma unroll
+                            for (int c = 0; c < NPAD; c += 16) {
+                                float tmp[16];
+                                tmem_ld16(tmem + lane_base + K::COL_O + (par * NWG + w2) * NPAD + c, tmp);
+#pragma unroll
+                                for (int x = 0; x < 16; ++x) o[c + x] = tmp[x];
+                            }
+                            const float* lw = lred + (par * NWG + w2) * 4 * RMAX;
+#pragma unroll
+                            for (int n = 0; n < RMAX; ++n) {
+                                const float mw = emref[(par * NWG + w2) * RMAX + n];
+                                // this warpgroup's part, brought to the common reference
+                                const float a = NWG == 1 ? 1.f : (mw == -INFINITY ? 0.f : fast_exp2(mw - Mx[n]));
+                                const float lsum = lw[n] + lw[RMAX + n] + lw[2 * RMAX + n] + lw[3 * RMAX + n];
+                                const float ow = SPLIT ? (o[2 * n] + o[2 * n + 1]) : o[n];
+                                Lsum[n] = __fmaf_rn(lsum, a, Lsum[n]);
+                                acc[n] = __fmaf_rn(ow, a, acc[n]);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    // column n's output row offset, computed by lane n and broadcast
+                    const size_t my_off = lane < ncol ? col_row_offset(p, e_qoff, R, e_hg, lane, D) : 0;
+                    if (complete) {
+#pragma unroll
+                        for (int n = 0; n < RMAX; ++n) {
+                            const size_t off = __shfl_sync(0xffffffffu, my_off, n);
+                            if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(acc[n], Lsum[n]));
+                        }
+                    } else {
+                        // this piece's partial; the merge warp publishes it and merges when last
+                        float* slot = slot_ptr(p, cta, e_S0, u0);
+#pragma unroll
+                        for (int n = 0; n < RMAX; ++n) {
+                            if (n < ncol) {
+                                if (tt == n) {
+                                    slot[n] = Mx[n];
+                                    slot[p.rows_pad + n] = Lsum[n];
+                                }
+                                if (tt < D) slot[2 * p.rows_pad + (size_t)n * D + tt] = acc[n];
+                            }
+                        }
+                        // (a CTA range cuts at most two segments, so the 4-entry task ring
+                        // never wraps onto a pending task)
+                        if (tt == 0) {
+                            int* task = reinterpret_cast<int*>(smem + K::OFF_MQ) + (n_tasks & 3) * 8;
+                            task[0] = e_b;
+                            task[1] = e_hg;
+                            task[2] = e_qoff;
+                            task[3] = e_Q;
+                            task[4] = e_S0;
+                            task[5] = e_S1;
+                        }
+                        mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
+                    }
                 }
+                if (!complete) ++n_tasks;                  // every warpgroup counts the tasks
             }
-            named_bar_sync(1, kSoftThreads);
-            float Lsum[RMAX];
-#pragma unroll
-            for (int n = 0; n < RMAX; ++n)
-                Lsum[n] = n < ncol ? lred[n] + lred[RMAX + n] + lred[2 * RMAX + n] + lred[3 * RMAX + n] : 1.f;
-            wait_bar(bar(B::PEMPTY + (t - 1) % NSB), ((t - 1) / NSB) & 1, ctl);
-            tc_fence_after();
-            float o[NPAD];
-#pragma unroll
-            for (int c = 0; c < NPAD; c += 16) {
-                float tmp[16];
-                tmem_ld16(tmem + lane_base + K::COL_O + c, tmp);
-#pragma unroll
-                for (int x = 0; x < 16; ++x) o[c + x] = tmp[x];
-            }
-            tc_fence_before();
-            float acc[RMAX];
-#pragma unroll
-            for (int n = 0; n < RMAX; ++n) acc[n] = SPLIT ? (o[2 * n] + o[2 * n + 1]) : o[n];
-            named_bar_sync(1, kSoftThreads);     // lred may be reused by the next piece
-            const bool complete = (it.S0 >= u0) && (it.S1 <= u1);
-            if (complete) {
-                // column n's output row offset, computed by lane n and broadcast
-                const size_t my_off = lane < ncol ? col_row_offset(p, it.cur.qoff, R, it.hg, lane, D) : 0;
-#pragma unroll
-                for (int n = 0; n < RMAX; ++n) {
-                    const size_t off = __shfl_sync(0xffffffffu, my_off, n);
-                    if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(acc[n] / Lsum[n]);
-                }
-            } else {
-                float* slot = slot_ptr(p, cta, it.S0, u0);
+            if (!in_piece) break;
+
+            if (++jt * kTP >= it.npg) {
+                // piece end, in every warpgroup: its column sums and reference max for
+                // the epilogue (double-buffered by piece parity)
+                const int par = pc & 1;
+                const int ncol = HG * G * it.cur.Q;
+                float* lw = lred + ((par * NWG + wg) * 4 + (warp & 3)) * RMAX;
 #pragma unroll
                 for (int n = 0; n < RMAX; ++n) {
                     if (n < ncol) {
-                        if (tt == n) {
-                            slot[n] = m_ref[n];
-                            slot[p.rows_pad + n] = Lsum[n];
-                        }
-                        if (tt < D) slot[2 * p.rows_pad + (size_t)n * D + tt] = acc[n];
+                        float v = l_part[n];
+#pragma unroll
+                        for (int o2 = 16; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
+                        if (lane == 0) lw[n] = v;
+                    }
+                    if (tt == 0) emref[(par * NWG + wg) * RMAX + n] = m_ref[n];
+                }
+                if constexpr (NWG > 1) {
+                    // every warpgroup's part of this piece is written (bounded wait)
+                    mbar_arrive(bar(B::PEND));
+                    const bool okp = wait_bar(bar(B::PEND), pc & 1, ctl);
+                    if (bar_red_or(bwg, kSoftThreads, !okp)) {   // the warpgroup leaves together
+                        aborted = true;
+                        break;
                     }
                 }
-                __threadfence();
-                named_bar_sync(1, kSoftThreads);
-                if (tt == 0) {
-                    const int need = owner_cta(it.S1 - 1, W, P) - owner_cta(it.S0, W, P) + 1;
-                    const int tix = seg_b * Hkv + it.hg;
-                    const int old = atomicAdd(p.tickets + tix, 1);
-                    if (old == need - 1) {
-                        // last piece of this segment: hand the merge to the merge warp
-                        p.tickets[tix] = 0;
-                        __threadfence();
-                        int* task = reinterpret_cast<int*>(smem + K::OFF_MQ) + (n_tasks & 3) * 8;
-                        task[0] = seg_b;
-                        task[1] = it.hg;
-                        task[2] = it.cur.qoff;
-                        task[3] = Q;
-                        task[4] = it.S0;
-                        task[5] = it.S1;
-                        mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
-                        ++n_tasks;
-                    }
+                pend = true;
+                e_b = it.cur.b;
+                e_hg = it.hg;
+                e_qoff = it.cur.qoff;
+                e_Q = it.cur.Q;
+                e_S0 = it.S0;
+                e_S1 = it.S1;
+                e_tfirst = t_first;
+                e_ntile = jt;
+                e_pc = pc;
+#pragma unroll
+                for (int n = 0; n < RMAX; ++n) {
+                    m_ref[n] = -INFINITY;
+                    l_part[n] = 0.f;
                 }
+                ++pc;
+                jt = 0;
+                t_first = t;
+                it.advance(p);
+                in_piece = it.valid();
             }
-            it.advance(p);
         }
-        if (tt == 0) {   // sentinel for the merge warp
-            reinterpret_cast<int*>(smem + K::OFF_MQ)[(n_tasks & 3) * 8] = -1;
+        if (!aborted && t % NWG == wg) {   // sentinel for the merge warp, after the last epilogue
+            if (tt == 0) reinterpret_cast<int*>(smem + K::OFF_MQ)[(n_tasks & 3) * 8] = -1;
             mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
         }
     }
@@ -718,13 +911,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     }
 }
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV>
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, int NWG>
 static cudaError_t launch_t(const AttnParams& p, int ncta, cudaStream_t st) {
-    using K = Cfg<D, NPAD, SPLIT, NSK, NSV>;
-    auto kern = attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV>;
+    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, NWG>;
+    auto kern = attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV, NWG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(ncta), dim3(kThreads), K::SMEM, st, p);
+    return launch_pdl(kern, dim3(ncta), dim3(Roles<NWG>::kThreads), K::SMEM, st, p);
 }
 
 }  // namespace tc
@@ -743,12 +936,14 @@ int tc_heads_per_segment(int num_kv_heads, int rows) {
     return hg;
 }
 
-// bf16 cache, head_dim 64/128, R = G * max_q_len <= 32.
+// bf16 cache, head_dim 64/128, R = G * max_q_len <= 32.  Narrow segments (N =
+// 16) run two softmax warpgroups; wide ones (N = 32) one, for its registers.
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, int ncta, cudaStream_t st) {
     const bool split = tc_col_limit(p.rows) == 8;
     if (head_dim == 128)
-        return split ? tc::launch_t<128, 16, true, 2, 4>(p, ncta, st) : tc::launch_t<128, 32, false, 2, 3>(p, ncta, st);
-    return split ? tc::launch_t<64, 16, true, 4, 6>(p, ncta, st) : tc::launch_t<64, 32, false, 4, 6>(p, ncta, st);
+        return split ? tc::launch_t<128, 16, true, 2, 4, 2>(p, ncta, st)
+                     : tc::launch_t<128, 32, false, 2, 3, 1>(p, ncta, st);
+    return split ? tc::launch_t<64, 16, true, 4, 6, 2>(p, ncta, st) : tc::launch_t<64, 32, false, 4, 6, 1>(p, ncta, st);
 }
 
 }  // namespace pkv

@@ -206,9 +206,13 @@ __device__ __forceinline__ int2 block_scan2_incl(int2 v, int2* scratch /* NT/32 
     return make_int2(v.x + add.x, v.y + add.y);
 }
 
+// With seqtab != nullptr and num_seqs <= NT, seqtab[b] receives (L, Q, units
+// before b, first q row of b) for every sequence, so that cursors can move on
+// without reading global memory (cursor_next with the table).
 template <int NT>
 __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch, Cursor* cur,
-                            int* u0_out, int* u1_out, int* W_out, int* P_out, Cursor* tail = nullptr) {
+                            int* u0_out, int* u1_out, int* W_out, int* P_out, Cursor* tail = nullptr,
+                            int4* seqtab = nullptr) {
     const int tid = threadIdx.x;
     if (p.num_seqs <= NT) {
         // one chunk: a single load of the lengths and a single two-value scan
@@ -224,6 +228,7 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
             q = seq_qrows(Q);
         }
         const int2 inc = block_scan2_incl<NT>(make_int2(u, q), s2);
+        if (seqtab && b < p.num_seqs) seqtab[b] = make_int4(L, Q, inc.x - u, inc.y - q);
         const int W = s2[NT / 32].x;
         const int P = min(ncta, W);
         *W_out = W;
@@ -323,15 +328,23 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
     return true;
 }
 
-// Advance the cursor to the next sequence with work (all threads, same values).
-__device__ __forceinline__ void cursor_next(const AttnParams& p, Cursor& c) {
+// Advance the cursor to the next sequence with work (all threads, same
+// values).  tab: the per-sequence table of plan_locate, or nullptr to read the
+// lengths from global memory.
+__device__ __forceinline__ void cursor_next(const AttnParams& p, Cursor& c, const int4* tab = nullptr) {
     c.Ub += c.nb * p.num_kv_heads;
     c.qoff += seq_qrows(c.Q);
     for (;;) {
         c.b += 1;
         if (c.b >= p.num_seqs) return;
-        c.L = p.context_lens[c.b];
-        c.Q = p.q_lens[c.b];
+        if (tab) {
+            const int4 e = tab[c.b];
+            c.L = e.x;
+            c.Q = e.y;
+        } else {
+            c.L = p.context_lens[c.b];
+            c.Q = p.q_lens[c.b];
+        }
         if (seq_units(p, c.L, c.Q) > 0) {
             c.nb = (c.L + kBlock - 1) / kBlock;
             return;

@@ -83,6 +83,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 
 // ------------------------------------------------------------------ fences
 
+// Load with acquire semantics at GPU scope: accesses after it are ordered
+// after it, so data published before a matching release is visible.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
