@@ -270,7 +270,7 @@ __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q,
             for (int x = 0; x < DPL; ++x) num[k][x] = 0.f;
         }
         for (int c = c_first; c <= c_last; ++c) {
-            const float* s = slot_ptr(p, c, S0, (int)(((int64_t)c * W) / P));
+            const float* s = slot_ptr(p, c, S0, cta_start(c, W, P));
             float m[8], l[8], a[8][DPL];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -360,19 +360,26 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
         *never = 0;
         mbar_fence_init();
     }
-    // Everything above touches only this CTA's shared memory, so under a
-    // programmatic dependent launch it overlaps the previous kernel; inputs are
-    // read only after that kernel's writes are visible.
+    // The tensor memory is taken before the dependency wait too.
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), K::TMEM_COLS);
+        tmem_relinquish();
+    }
+    // Everything above touches only this CTA's shared memory and TMEM, so
+    // under a programmatic dependent launch it overlaps the previous kernel;
+    // inputs are read only after that kernel's writes are visible.
     griddep_wait();
     Cursor cur0, curt;
     int u0, u1, W, P;
     int4* seqtab = reinterpret_cast<int4*>(smem + K::OFF_SEQ);
     const bool has_work =
         plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt, seqtab);
-    if (!has_work) return;       // uniform across the CTA; no TMEM held yet
-    if (warp == 0) {
-        tmem_alloc(smem_u32(tmem_slot), K::TMEM_COLS);
-        tmem_relinquish();
+    if (!has_work) {             // uniform across the CTA
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (warp == 0) tmem_dealloc(*tmem_slot, K::TMEM_COLS);
+        return;
     }
     tc_fence_before();
     __syncthreads();
@@ -386,10 +393,11 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
-        // Runs one piece ahead on its inputs: while piece j streams, the q rows
-        // and the first block-table window of piece j + 1 are in flight, and
-        // within a piece the next 32-page window of the block table is loaded
-        // while the current one is used, so no copy waits on a table read.
+        // Runs one piece ahead on its inputs: once a piece's first tile is on
+        // its way, the q rows and the first block-table window of the next piece
+        // are loaded, and within a piece the next 32-page window of the block
+        // table is loaded while the current one is used, so no copy waits on a
+        // table read after the first.
         const uint64_t pol = policy_evict_first();
         constexpr int QV = (RMAX * K::NCH + 31) / 32;
         constexpr bool kQAhead = QV <= 4;         // wide pieces load their q at the piece start
@@ -422,13 +430,8 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
         }
         while (ok && it.valid()) {
             PieceIter nx = it;
-            nx.advance(p);
             uint4 qn[kQAhead ? QV : 1];
             int winn = 0;
-            if (nx.valid()) {
-                if constexpr (kQAhead) load_q(nx, qn);
-                winn = load_win(nx, nx.pg0 / HG);
-            }
             if constexpr (!kQAhead) load_q(it, qv);
             const int qb = j & 1;
             if (j >= 2) {
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
             }
             const int R = G * it.cur.Q, ncol = HG * R;
             int ws = it.pg0 / HG;                         // win: entries [ws, ws + 32); win2: the next 32
-            int win2 = load_win(it, ws + 32);
+            int win2 = 0;                                 // (loaded after the first tile, which stays in win)
             for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
                 const int np = min(kTP, it.npg - t0);
                 const int ks = t % NSK, vs = t % NSV;
@@ -491,6 +494,15 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                                   K::PAGE, bar(B::VFULL + vs), pol);
                 ++vcount;
                 __syncwarp();
+                if (t0 == 0) {
+                    // look-ahead, once the piece's first tile is on its way
+                    win2 = load_win(it, ws + 32);
+                    nx.advance(p);
+                    if (nx.valid()) {
+                        if constexpr (kQAhead) load_q(nx, qn);
+                        winn = load_win(nx, nx.pg0 / HG);
+                    }
+                }
                 // slide the table window once a tile has reached the next one
                 if ((qfirst + np - 1) / HG - ws >= 32 && t0 + kTP < it.npg) {
                     ws += 32;
@@ -597,6 +609,7 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
             __syncwarp();
             const int* task = mq + (n & 3) * 8;
             if (task[0] < 0) break;                     // sentinel: the softmax warps are done
+            if (task[6] != 0) continue;                 // merged by the softmax warps already
             const int seg_b = task[0], hg = task[1], S0 = task[4], S1 = task[5];
             int last = 0;
             if (lane == 0) {
@@ -766,6 +779,11 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                 const bool complete = (e_S0 >= u0) && (e_S1 <= u1);
                 if ((in_piece ? t - 1 : t) % NWG == wg) {
                     const int R = G * e_Q, ncol = HG * R, par = e_pc & 1;
+                    // a split piece reads its segment's ticket first: the load's latency
+                    // overlaps the wait for the piece's last P.V
+                    int* ticket = p.tickets + e_b * Hkv + e_hg;
+                    int tk = -1;
+                    if (!complete && tt == 0) tk = ld_acquire_gpu(ticket);
                     named_bar_sync(bwg, kSoftThreads);     // (one warpgroup: its piece-end sums)
                     // this piece's O^T accumulators are final once its last P.V is done
                     wait_bar(bar(B::ODONE + par), (e_pc >> 1) & 1, ctl);
@@ -819,33 +837,111 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                             if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(acc[n], Lsum[n]));
                         }
                     } else {
-                        // this piece's partial; the merge warp publishes it and merges when last
-                        float* slot = slot_ptr(p, cta, e_S0, u0);
+                        const int c_first = owner_cta(e_S0, W, P), c_last = owner_cta(e_S1 - 1, W, P);
+                        // Every other piece published already (early ticket read): merge here.
+                        // Otherwise store the partial; a later piece hands it to the merge warp,
+                        // while the CTA's last piece publishes it and draws its ticket here.
+                        bool direct = bar_red_or(bwg, kSoftThreads, tk == c_last - c_first);
+                        bool handed = false;
+                        if (!direct) {
+                            float* slot = slot_ptr(p, cta, e_S0, u0);
 #pragma unroll
-                        for (int n = 0; n < RMAX; ++n) {
-                            if (n < ncol) {
-                                if (tt == n) {
-                                    slot[n] = Mx[n];
-                                    slot[p.rows_pad + n] = Lsum[n];
+                            for (int n = 0; n < RMAX; ++n) {
+                                if (n < ncol) {
+                                    if (tt == n) {
+                                        slot[n] = Mx[n];
+                                        slot[p.rows_pad + n] = Lsum[n];
+                                    }
+                                    if (tt < D) slot[2 * p.rows_pad + (size_t)n * D + tt] = acc[n];
                                 }
-                                if (tt < D) slot[2 * p.rows_pad + (size_t)n * D + tt] = acc[n];
+                            }
+                            if (in_piece) {
+                                // (a CTA range cuts at most two segments, so the 4-entry task ring
+                                // never wraps onto a pending task)
+                                if (tt == 0) {
+                                    int* task = reinterpret_cast<int*>(smem + K::OFF_MQ) + (n_tasks & 3) * 8;
+                                    task[0] = e_b;
+                                    task[1] = e_hg;
+                                    task[2] = e_qoff;
+                                    task[3] = e_Q;
+                                    task[4] = e_S0;
+                                    task[5] = e_S1;
+                                    task[6] = 0;
+                                }
+                                mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
+                                handed = true;
+                            } else {
+                                named_bar_sync(bwg, kSoftThreads);     // every thread's part is stored
+                                int lst = 0;
+                                if (tt == 0) {
+                                    __threadfence();
+                                    lst = atomicAdd(ticket, 1) == c_last - c_first;
+                                    __threadfence();
+                                }
+                                direct = bar_red_or(bwg, kSoftThreads, lst != 0);
                             }
                         }
-                        // (a CTA range cuts at most two segments, so the 4-entry task ring
-                        // never wraps onto a pending task)
-                        if (tt == 0) {
-                            int* task = reinterpret_cast<int*>(smem + K::OFF_MQ) + (n_tasks & 3) * 8;
-                            task[0] = e_b;
-                            task[1] = e_hg;
-                            task[2] = e_qoff;
-                            task[3] = e_Q;
-                            task[4] = e_S0;
-                            task[5] = e_S1;
+                        if (direct) {
+                            // merge in CTA order, this piece from registers (the same steps as
+                            // merge_segment_warp, so either place gives the same bits)
+#pragma unroll
+                            for (int n0 = 0; n0 < RMAX; n0 += 8) {
+                                if (n0 >= ncol) break;
+                                float M[8], den[8], num[8];
+#pragma unroll
+                                for (int x = 0; x < 8; ++x) {
+                                    M[x] = -INFINITY;
+                                    den[x] = 0.f;
+                                    num[x] = 0.f;
+                                }
+                                for (int c = c_first; c <= c_last; ++c) {
+                                    float m[8], l[8], a[8];
+                                    if (c == cta) {
+#pragma unroll
+                                        for (int x = 0; x < 8; ++x) {
+                                            m[x] = Mx[n0 + x];
+                                            l[x] = Lsum[n0 + x];
+                                            a[x] = acc[n0 + x];
+                                        }
+                                    } else {
+                                        const float* sl = slot_ptr(p, c, e_S0, cta_start(c, W, P));
+#pragma unroll
+                                        for (int x = 0; x < 8; ++x) {
+                                            const int n = n0 + x;
+                                            m[x] = n < ncol ? __ldcg(sl + n) : -INFINITY;
+                                            l[x] = n < ncol ? __ldcg(sl + p.rows_pad + n) : 0.f;
+                                            a[x] = (n < ncol && tt < D) ? __ldcg(sl + 2 * p.rows_pad + (size_t)n * D + tt) : 0.f;
+                                        }
+                                    }
+#pragma unroll
+                                    for (int x = 0; x < 8; ++x) {
+                                        float wo, wn;
+                                        merge_weights(M[x], m[x], wo, wn);
+                                        den[x] = merge_acc(den[x], wo, l[x], wn);
+                                        num[x] = merge_acc(num[x], wo, a[x], wn);
+                                    }
+                                }
+#pragma unroll
+                                for (int x = 0; x < 8; ++x) {
+                                    const int n = n0 + x;
+                                    const size_t off = __shfl_sync(0xffffffffu, my_off, n);
+                                    if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(num[x], den[x]));
+                                }
+                            }
+                            if (tt == 0) *ticket = 0;              // ready for the next launch
                         }
-                        mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
+                        if (!handed) {
+                            // its ring entry: nothing left for the merge warp (which walks the ring in order)
+                            if (tt == 0) {
+                                int* task = reinterpret_cast<int*>(smem + K::OFF_MQ) + (n_tasks & 3) * 8;
+                                task[0] = e_b;                      // (not a sentinel)
+                                task[6] = 1;
+                            }
+                            mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
+                        }
                     }
                 }
-                if (!complete) ++n_tasks;                  // every warpgroup counts the tasks
+                if (!complete) ++n_tasks;                  // every warpgroup counts the ring entries
             }
             if (!in_piece) break;
 

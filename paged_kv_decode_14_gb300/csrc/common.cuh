@@ -125,6 +125,30 @@ struct AttnLaunch {
 
 // ------------------------------------------------------------------ planning
 
+// floor(num / den) for 0 <= num < 2^47 and 0 < den < 2^31 with a quotient
+// below 2^31, without a 64-bit division: a float estimate (relative error near
+// 2^-22), a second estimate on the remainder (now within one of the quotient)
+// and one exact integer correction step.
+__device__ __forceinline__ int floor_div_small(long long num, int den) {
+    int q = (int)__fdividef((float)num, (float)den);
+    long long r = num - (long long)q * den;
+    q += (int)__fdividef((float)r, (float)den);
+    r = num - (long long)q * den;
+    if (r < 0) --q;
+    else if (r >= den) ++q;
+    return q;
+}
+
+// CTA owning unit u under the partition above (P = participating CTAs <= W,
+// so every CTA in [owner(S0), owner(S1 - 1)] holds a piece of [S0, S1)).
+__device__ __forceinline__ int owner_cta(int u, int W, int ncta) {
+    return floor_div_small((long long)(u + 1) * ncta - 1, W);
+}
+// First unit of CTA c, floor(c W / P).
+__device__ __forceinline__ int cta_start(int c, int W, int ncta) {
+    return floor_div_small((long long)c * W, ncta);
+}
+
 // Units (pages x kv-heads) of sequence b; sequences with no query rows or
 // invalid lengths (Q > L, Q above the launch's max_q_len, more pages than a
 // block-table row holds) contribute none.
@@ -234,8 +258,8 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         *W_out = W;
         *P_out = P;
         if (cta >= P) return false;
-        const int u0 = (int)(((int64_t)cta * W) / P);
-        const int u1 = (int)(((int64_t)(cta + 1) * W) / P);
+        const int u0 = cta_start(cta, W, P);
+        const int u1 = cta_start(cta + 1, W, P);
         *u0_out = u0;
         *u1_out = u1;
         const int Ub = inc.x - u;
@@ -280,8 +304,8 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
     *W_out = W;
     *P_out = P;
     if (cta >= P) return false;
-    const int u0 = (int)(((int64_t)cta * W) / P);
-    const int u1 = (int)(((int64_t)(cta + 1) * W) / P);
+    const int u0 = cta_start(cta, W, P);
+    const int u1 = cta_start(cta + 1, W, P);
     *u0_out = u0;
     *u1_out = u1;
     // pass 2: find b with Ub <= u0 < Ub + units(b) (and the one holding u1 - 1), with q offsets
@@ -353,11 +377,6 @@ __device__ __forceinline__ void cursor_next(const AttnParams& p, Cursor& c, cons
     }
 }
 
-// CTA owning unit u under the partition above (P = participating CTAs <= W,
-// so every CTA in [owner(S0), owner(S1 - 1)] holds a piece of [S0, S1)).
-__device__ __forceinline__ int owner_cta(int u, int W, int ncta) {
-    return (int)((((int64_t)u + 1) * ncta - 1) / W);
-}
 
 // Partial slot of a piece: 0 if its segment started before this CTA's range,
 // else 1 (the segment starts here and continues in the next CTA).
@@ -377,13 +396,13 @@ __device__ void merge_segment(const AttnParams& p, const Cursor& c, int g, int S
         const int r = idx / D, d = idx % D;
         float M = -INFINITY;
         for (int cc = c_first; cc <= c_last; ++cc) {
-            const int u0c = (int)(((int64_t)cc * W) / ncta);
+            const int u0c = cta_start(cc, W, ncta);
             const float* s = slot_ptr(p, cc, S0, u0c);
             M = fmaxf(M, __ldcg(s + r));
         }
         float den = 0.f, num = 0.f;
         for (int cc = c_first; cc <= c_last; ++cc) {
-            const int u0c = (int)(((int64_t)cc * W) / ncta);
+            const int u0c = cta_start(cc, W, ncta);
             const float* s = slot_ptr(p, cc, S0, u0c);
             const float m = __ldcg(s + r);
             const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
