@@ -160,7 +160,9 @@ PKV_API pkv_status pkv_workspace_init(void* workspace, size_t workspace_bytes, v
  *                  once by pkv_workspace_init; not shared by concurrent calls.
  *
  * Supported: block_size 16, head_dim 64 or 128, Hq % Hkv == 0,
- * (Hq / Hkv) * max_q_len <= 32.  Results are deterministic and depend only
+ * (Hq / Hkv) * max_q_len <= 32, max_blocks_per_seq * Hkv < 2^20 (contexts
+ * below 2^24 / Hkv tokens); otherwise PKV_ERR_UNSUPPORTED, nothing launched.
+ * Results are deterministic and depend only
  * on logical positions (not on which physical blocks hold them).
  */
 PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, int32_t num_q_heads,

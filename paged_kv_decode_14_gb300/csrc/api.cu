@@ -134,6 +134,7 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
     if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / cache->num_kv_heads;
     if (max_q_len > 16 || group * max_q_len > 32) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * cache->num_kv_heads >= (1 << 20)) return PKV_ERR_UNSUPPORTED;   // unit indices stay below 2^20
     if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
     const int sms = num_sms_current();
     if (sms <= 0) return PKV_ERR_CUDA;

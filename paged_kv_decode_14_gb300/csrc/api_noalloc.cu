@@ -77,6 +77,7 @@ extern "C" PKV_API pkv_status pkv_paged_attention_noalloc(
     if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / c->num_kv_heads;
     if (max_q_len > 16 || group * max_q_len > 32) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * c->num_kv_heads >= (1 << 20)) return PKV_ERR_UNSUPPORTED;   // unit indices stay below 2^20
     if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
 
     void* scratch = nullptr;

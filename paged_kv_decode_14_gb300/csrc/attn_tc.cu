@@ -189,7 +189,7 @@ struct PieceIter {
 
     __device__ void load_at(int uu, int end) {
         const int len = cur.nb * HG;
-        hg = (uu - cur.Ub) / len;
+        hg = div_small(uu - cur.Ub, len);
         S0 = cur.Ub + hg * len;
         S1 = S0 + len;
         pg0 = uu - S0;
@@ -202,7 +202,7 @@ struct PieceIter {
         fcur = c0;
         cur = ct;
         const int len = ct.nb * HG;
-        const int s0t = ct.Ub + ((u1 - 1 - ct.Ub) / len) * len;
+        const int s0t = ct.Ub + div_small(u1 - 1 - ct.Ub, len) * len;
         const int tstart = max(u0, s0t);
         if (tstart > u0) {
             tail_phase = true;
@@ -234,7 +234,7 @@ struct PieceIter {
 
 // Column n of segment (b, hg) -> element offset of its q / out row.
 __device__ __forceinline__ size_t col_row_offset(const AttnParams& p, int qoff, int R, int hg, int n, int D) {
-    const int hh = n / R, r = n % R, i = r / p.group, hl = r % p.group;
+    const int hh = div_small(n, R), r = n - hh * R, i = div_small(r, p.group), hl = r - i * p.group;
     return ((size_t)(qoff + i) * p.num_q_heads + (hg * p.hg + hh) * p.group + hl) * D;
 }
 
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
         int win = 0;
         if (it.valid()) {
             if constexpr (kQAhead) load_q(it, qv);
-            win = load_win(it, it.pg0 / HG);
+            win = load_win(it, div_small(it.pg0, HG));
         }
         while (ok && it.valid()) {
             PieceIter nx = it;
@@ -440,14 +440,15 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                 if (!ok) break;
             }
             const int R = G * it.cur.Q, ncol = HG * R;
-            int ws = it.pg0 / HG;                         // win: entries [ws, ws + 32); win2: the next 32
+            int ws = div_small(it.pg0, HG);                        // win: entries [ws, ws + 32); win2: the next 32
             int win2 = 0;                                 // (loaded after the first tile, which stays in win)
             for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
                 const int np = min(kTP, it.npg - t0);
                 const int ks = t % NSK, vs = t % NSV;
                 const int qfirst = it.pg0 + t0;                       // first unit of the tile
                 const int qu = qfirst + (lane & 7);
-                const int pg = qu / HG - ws;                          // in [0, 40) for the tile's units
+                const int qpg = div_small(qu, HG);                    // page of the lane's unit
+                const int pg = qpg - ws;                          // in [0, 40) for the tile's units
                 const int e1 = __shfl_sync(0xffffffffu, win, pg & 31);
                 const int e2 = __shfl_sync(0xffffffffu, win2, pg & 31);
                 int blk = pg < 32 ? e1 : e2;
@@ -455,7 +456,7 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                     if (lane < np) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
                     blk = 0;
                 }
-                const size_t off = ((size_t)blk * Hkv + it.hg * HG + qu % HG) * K::PAGE;
+                const size_t off = ((size_t)blk * Hkv + it.hg * HG + (qu - qpg * HG)) * K::PAGE;
                 if (t >= NSK) {
                     bool w = lane == 0 ? wait_bar(bar(B::KEMPTY + ks), ((t / NSK) - 1) & 1, ctl) : true;
                     ok = __shfl_sync(0xffffffffu, w, 0);
@@ -500,11 +501,11 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                     nx.advance(p);
                     if (nx.valid()) {
                         if constexpr (kQAhead) load_q(nx, qn);
-                        winn = load_win(nx, nx.pg0 / HG);
+                        winn = load_win(nx, div_small(nx.pg0, HG));
                     }
                 }
                 // slide the table window once a tile has reached the next one
-                if ((qfirst + np - 1) / HG - ws >= 32 && t0 + kTP < it.npg) {
+                if (div_small(qfirst + np - 1, HG) - ws >= 32 && t0 + kTP < it.npg) {
                     ws += 32;
                     win = win2;
                     win2 = load_win(it, ws + 32);
@@ -664,8 +665,9 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                 // this thread's token: unit slot k of the tile -> (page, kv-head), position
                 const int k = tt >> 4;
                 const int qu = it.pg0 + jt * kTP + k;
-                const int hh = qu % HG;
-                const int pos = (qu / HG) * kBlock + (tt & 15);
+                const int qpg = div_small(qu, HG);
+                const int hh = qu - qpg * HG;
+                const int pos = qpg * kBlock + (tt & 15);
                 const bool tok_ok = k < np && pos < L;
                 // visible columns: [lo, hi) of this head's R rows (causal within the window)
                 const int lo = hh * R + max(0, pos - lim0) * G, hi = hh * R + R;

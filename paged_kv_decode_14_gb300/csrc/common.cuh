@@ -139,6 +139,14 @@ __device__ __forceinline__ int floor_div_small(long long num, int den) {
     return q;
 }
 
+// floor(n / d) for 0 <= n < 2^20 and d >= 1 by one approximate float
+// division: the quotient of n + 1/2 lies at least 1 / (2 d) from an integer,
+// and the division's relative error (a few units of 2^-24) keeps it on the
+// right side for numerators this small.
+__device__ __forceinline__ int div_small(int n, int d) {
+    return (int)__fdividef((float)n + 0.5f, (float)d);
+}
+
 // CTA owning unit u under the partition above (P = participating CTAs <= W,
 // so every CTA in [owner(S0), owner(S1 - 1)] holds a piece of [S0, S1)).
 __device__ __forceinline__ int owner_cta(int u, int W, int ncta) {

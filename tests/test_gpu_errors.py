@@ -38,6 +38,10 @@ def test_host_checks_return_status():
     with pytest.raises(nat.PagedKVError) as e:      # max_q_len above the supported window
         nat.attention(c, dw.q, dw.block_tables, dw.context_lens, dw.q_lens, 17, 0.1, dw.workspace)
     assert e.value.status == 2
+    wide = torch.full((2, (1 << 20) // c.num_kv_heads), -1, dtype=torch.int32, device="cuda")
+    with pytest.raises(nat.PagedKVError) as e:      # max_blocks_per_seq * Hkv beyond 2^20 units per sequence
+        nat.attention(c, dw.q, wide, dw.context_lens, dw.q_lens, 2, 0.1, dw.workspace)
+    assert e.value.status == 2
 
 
 def test_bad_block_id_sets_error_word_then_recovers():
