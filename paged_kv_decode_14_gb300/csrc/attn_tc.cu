@@ -21,15 +21,11 @@
 // K and V pages sit in separate rings: a K slot is refilled as soon as its
 // S^T MMA has run, a V slot once its P.V MMA has.
 //
-// Softmax warpgroups.  With NWG = 2, two warpgroups take the tiles in turn,
-// each with its own online-softmax state and its own O^T accumulator, so the
-// latency of one tile's softmax overlaps the next tile's; the piece epilogue
-// brings the two parts to a common reference and adds them.  O^T stays in
-// TMEM for the whole piece (pieces alternate between two sets of
-// accumulators, so a piece's epilogue overlaps the next piece's first tiles).
-// The softmax reference max of a column is only raised (and O^T rescaled in
-// TMEM) when a logit exceeds it by more than 2^8, so most tiles need neither a
-// max reduction nor a rescale.
+// O^T stays in TMEM for the whole piece; pieces alternate between two
+// accumulators, so a piece's epilogue overlaps the next piece's tiles.  The
+// softmax reference max of a column is only raised (and O^T rescaled in TMEM)
+// when a logit exceeds it by more than 2^8, so most tiles need neither a max
+// reduction nor a rescale.
 //
 // The cache's page layout (16-byte chunks, core matrices of 8 tokens x 16
 // bytes, see pagedkv.h) is the tensor core's no-swizzle canonical layout: K
@@ -48,14 +44,16 @@
 // other piece is already published it merges at once; otherwise it publishes
 // the partial (fence, ticket increment) and merges if its ticket was the last.
 //
-// Warp roles (128 NWG + 128 threads): warps 0 .. 4 NWG - 1 softmax, O rescale
-// and piece epilogue (each warp its TMEM lane quarter), then the producer
-// (bulk copies, q staging, one piece ahead on q and the block table), the
-// S^T issuer, the merge warp and the P.V issuer (the two issuers block on
-// their own barriers, so a P.V never waits behind the next tiles' S^T).
-// Every mbarrier wait is bounded (2 s); a timeout sets PKV_DEVERR_TIMEOUT and
-// an abort flag, all roles wind down, in-flight copies are drained and TMEM
-// is freed before the CTA exits.
+// Warp roles: warps 0-3 softmax and O rescale (each warp its TMEM lane
+// quarter), warp 4 producer (bulk copies, q staging, one piece ahead on q and
+// the block table), warp 5 the S^T issuer, warp 6 the merge warp, warp 7 the
+// P.V issuer (the two issuers block on their own barriers, so a P.V never
+// waits behind the next tiles' S^T), and for narrow segments warps 8-11, the
+// epilogue warpgroup: piece epilogues run there, off the softmax's path
+// (wide segments run them in the softmax warps, after the next piece's first
+// tile).  Every mbarrier wait is bounded (2 s); a timeout sets
+// PKV_DEVERR_TIMEOUT and an abort flag, all roles wind down, in-flight copies
+// are drained and TMEM is freed before the CTA exits.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -66,24 +64,22 @@ using namespace ptx;
 
 constexpr int kTP = 8;                        // units (pages of one kv-head) per tile
 constexpr int kTileTok = kTP * kBlock;        // 128 token rows = MMA M
-constexpr int kSoftThreads = 128;             // one softmax warpgroup (the 128 TMEM lanes)
+constexpr int kSoftThreads = 128;             // one warpgroup (the 128 TMEM lanes)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxSmem = 232448;
 constexpr int NSB = 4;                        // S^T / P ring depth (tiles the MMA may run ahead)
+// warps 0-3 softmax; 4 producer, 5 S^T issuer, 6 merge, 7 P.V issuer; with
+// EWG, 8-11 the epilogue warpgroup.  Named barriers: 1 softmax, 2 epilogue.
+constexpr int kProducerWarp = 4, kMmaWarp = 5, kMergeWarp = 6, kPvWarp = 7, kEpiWarp0 = 8;
+constexpr int kBarSoft = 1, kBarEpi = 2;
+template <bool EWG>
+__host__ __device__ constexpr int threads_of() { return EWG ? 384 : 256; }
+constexpr int kSeqTab = 256;                  // sequences the shared-memory table holds
 
 // Online-softmax reference slack (powers of two), see the header comment.
 constexpr float kRescaleSlack = 8.f;
 
-// NWG softmax warpgroups (warps 0 .. 4 NWG - 1) take the tiles in turn, then
-// four single-warp roles.
-template <int NWG>
-struct Roles {
-    static constexpr int kThreads = kSoftThreads * NWG + 128;
-    static constexpr int kProducerWarp = 4 * NWG, kMmaWarp = 4 * NWG + 1, kMergeWarp = 4 * NWG + 2,
-                         kPvWarp = 4 * NWG + 3;
-};
-
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV, int NWG>
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG>
 struct Cfg {
     static constexpr int RMAX = SPLIT ? NPAD / 2 : NPAD;  // logical columns
     static constexpr int PAGE = kBlock * D * 2;
@@ -96,22 +92,25 @@ struct Cfg {
     static constexpr int QBUF = NPAD * D * 2;
     static constexpr int OFF_P = OFF_Q + 2 * QBUF;
     static constexpr int PBUF = NPAD * kTileTok * 2;
-    static constexpr int OFF_RED = OFF_P + NSB * PBUF;                 // float [NWG][8 slots][RMAX]
-    static constexpr int OFF_LRED = OFF_RED + NWG * 8 * RMAX * 4;      // float [2][NWG][4 warps][RMAX]
-    static constexpr int OFF_EM = OFF_LRED + 2 * NWG * 4 * RMAX * 4;   // float [2][NWG][RMAX]
-    static constexpr int OFF_BAR = OFF_EM + 2 * NWG * RMAX * 4;
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 13;
-    static constexpr int OFF_MISC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // tmem addr, abort, zero
+    static constexpr int OFF_RED = OFF_P + NSB * PBUF;                 // float [8 slots][RMAX]
+    static constexpr int OFF_LRED = OFF_RED + 8 * RMAX * 4;            // float [2][4 warps][RMAX]
+    static constexpr int OFF_EM = OFF_LRED + 2 * 4 * RMAX * 4;         // float [2][RMAX]
+    static constexpr int OFF_PD = OFF_EM + 2 * RMAX * 4;               // int [2][8]: piece descriptors
+    static constexpr int OFF_BAR = OFF_PD + 2 * 8 * 4;
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 16;   // the barriers of Bars
+    static constexpr int OFF_MISC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // tmem addr, abort, zero, gather state
     static constexpr int OFF_MQ = OFF_MISC + 16;         // merge tasks: int [4][8]
-    static constexpr int OFF_SEQ = OFF_MQ + 128;         // int4 [threads]: per-sequence (L, Q, Ub, qoff)
-    static constexpr int SMEM_USED = OFF_SEQ + Roles<NWG>::kThreads * 16 + 128;  // + base alignment slack
+    static constexpr int OFF_SEQ = OFF_MQ + 128;         // int4 [kSeqTab]: per-sequence (L, Q, Ub, qoff)
+    // pre-merged earlier pieces of the CTA's last segment: M[RMAX], den[RMAX], num[RMAX][D]
+    static constexpr int OFF_GATHER = OFF_SEQ + kSeqTab * 16;
+    static constexpr int GATHER = SPLIT ? RMAX * (D + 2) * 4 : 0;
+    static constexpr int SMEM_USED = OFF_GATHER + GATHER + 128;  // + base alignment slack
     // One CTA per SM either way: take the whole per-block budget, so every
     // operand read the descriptors can form stays inside the allocation.
     static constexpr int SMEM = kMaxSmem - 1024;
     static constexpr int COL_S = 0;                      // S^T buffers: NSB x NPAD columns
-    // O^T accumulators: [piece parity][warpgroup] x NPAD columns
-    static constexpr int COL_O = NSB * NPAD;
-    static constexpr int NCOLS = (NSB + 2 * NWG) * NPAD;
+    static constexpr int COL_O = NSB * NPAD;             // O^T accumulators: [piece parity] x NPAD columns
+    static constexpr int NCOLS = (NSB + 2) * NPAD;
     static constexpr int TMEM_COLS = NCOLS <= 64 ? 64 : NCOLS <= 128 ? 128 : 256;
     static_assert(NCOLS <= 256, "TMEM budget");
     static_assert(OFF_BAR % 8 == 0 && OFF_SEQ % 16 == 0 && OFF_RED % 16 == 0, "shared memory alignment");
@@ -124,7 +123,14 @@ struct Bars {
                          SFULL = 2 * NSK + 2 * NSV, PFULL = SFULL + NSB, PEMPTY = PFULL + NSB,
                          QFULL = PEMPTY + NSB, QEMPTY = QFULL + 2, DONE = QEMPTY + 2, MQFULL = DONE + 2,
                          ODONE = MQFULL + 4,      // [2]: last P.V of a piece of that parity done
-                         PEND = ODONE + 2;        // every softmax thread finished its part of a piece
+                         PREADY = ODONE + 2,      // [2]: a piece of that parity handed to the epilogue
+                         OFREE = PREADY + 2;      // [2]: its epilogue has read O^T, lred and emref
+};
+
+// A finished piece, as its epilogue needs it.
+struct PieceDesc {
+    int b, hg, qoff, Q, S0, S1, pc;
+    bool last;
 };
 
 struct Ctl {
@@ -304,14 +310,13 @@ __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q,
     }
 }
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV, int NWG>
-__global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const AttnParams p) {
-    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, NWG>;
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG>
+__global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const AttnParams p) {
+    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG>;
     using B = Bars<NSK, NSV>;
+    static_assert(B::OFREE + 2 == K::NBAR, "barrier count");
     constexpr int RMAX = K::RMAX;
-    constexpr int kThreads = Roles<NWG>::kThreads;
-    constexpr int kProducerWarp = Roles<NWG>::kProducerWarp, kMmaWarp = Roles<NWG>::kMmaWarp,
-                  kMergeWarp = Roles<NWG>::kMergeWarp, kPvWarp = Roles<NWG>::kPvWarp;
+    constexpr int kThreads = threads_of<EWG>();
     extern __shared__ uint8_t smem_raw[];
     __shared__ int scratch[kThreads / 32 + 1];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -324,6 +329,13 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 4);
     volatile int* never = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 8);   // stays 0
+    // pre-merge of the last piece's segment: 0 open, 1 the merge warp gathers, 2 gathered,
+    // 3 the epilogue went its own way
+    volatile int* gstate = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 12);
+    float* gbuf = reinterpret_cast<float*>(smem + K::OFF_GATHER);
+    float* lred = reinterpret_cast<float*>(smem + K::OFF_LRED);   // [2][4][RMAX]
+    float* emref = reinterpret_cast<float*>(smem + K::OFF_EM);    // [2][RMAX]
+    int* pdesc = reinterpret_cast<int*>(smem + K::OFF_PD);        // [2][8]
     const Ctl ctl{abort_flag, p.err};
     const Ctl drain{never, p.err};      // bounded waits that ignore the abort flag
 
@@ -349,15 +361,16 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B::QFULL + i), 1);
             mbar_init(bar(B::QEMPTY + i), 1);
+            mbar_init(bar(B::ODONE + i), 1);
+            mbar_init(bar(B::PREADY + i), kSoftThreads);
+            mbar_init(bar(B::OFREE + i), kSoftThreads);
         }
         mbar_init(bar(B::DONE), 1);
         mbar_init(bar(B::DONE + 1), 1);
         for (int i = 0; i < 4; ++i) mbar_init(bar(B::MQFULL + i), kSoftThreads);
-        mbar_init(bar(B::ODONE), 1);
-        mbar_init(bar(B::ODONE + 1), 1);
-        mbar_init(bar(B::PEND), kSoftThreads * NWG);
         *abort_flag = 0;
         *never = 0;
+        *gstate = 0;
         mbar_fence_init();
     }
     // The tensor memory is taken before the dependency wait too.
@@ -371,7 +384,7 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
     griddep_wait();
     Cursor cur0, curt;
     int u0, u1, W, P;
-    int4* seqtab = reinterpret_cast<int4*>(smem + K::OFF_SEQ);
+    int4* seqtab = p.num_seqs <= kSeqTab ? reinterpret_cast<int4*>(smem + K::OFF_SEQ) : nullptr;
     const bool has_work =
         plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt, seqtab);
     if (!has_work) {             // uniform across the CTA
@@ -388,8 +401,188 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
     const int G = p.group, Hkv = p.num_kv_heads, HG = p.hg;
 
     PieceIter it;
-    it.tab = p.num_seqs <= kThreads ? seqtab : nullptr;
+    it.tab = seqtab;
     it.init(p, cur0, curt, u0, u1);
+
+    // ---------------------------------------------------------------- piece epilogue
+    // Run by one warpgroup (thread tt = TMEM lane = d row, named barrier bid)
+    // once piece d's column sums and reference max are in lred / emref (parity
+    // d.pc & 1): waits for the piece's last P.V, reads O^T, then writes the
+    // output (complete segment), or hands the partial to the merge warp (a
+    // split piece before the CTA's last), or closes the segment (the last
+    // piece: the merge warp's pre-merge, a direct merge when every other piece
+    // is published, else publish and draw the ticket).  With EWG the O^T and
+    // smem reads end with an arrive on OFREE, which frees them for piece d.pc + 2.
+    int n_tasks = 0;
+    auto piece_epilogue = [&](const PieceDesc& d, int tt, int bid) {
+        const int lanee = tt & 31;
+        const uint32_t lbase = (uint32_t)((tt >> 5) * 32) << 16;
+        const bool complete = (d.S0 >= u0) && (d.S1 <= u1);
+        const int R = G * d.Q, ncol = HG * R, par = d.pc & 1;
+        int* ticket = p.tickets + d.b * Hkv + d.hg;
+        // the CTA's last piece, ending its segment: take the merge warp's pre-merge
+        // when it is there (or about to be), else close the pre-merge to it
+        const bool gather_ok = SPLIT && !complete && d.last && d.S0 < u0 && d.S1 <= u1;
+        int tk = -1, gs = 0;
+        if (!complete && d.last && tt == 0) {
+            if (gather_ok) {
+                gs = atomicCAS(const_cast<int*>(gstate), 0, 3);
+                if (gs == 1) {
+                    const uint64_t g0 = globaltimer_ns();
+                    while ((gs = *gstate) == 1 && !*abort_flag) {
+                        if (globaltimer_ns() - g0 > kWaitLimitNs) {
+                            raise_error(p.err, PKV_DEVERR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                    }
+                }
+                __threadfence_block();
+            }
+            // the segment's ticket: its latency overlaps the wait for the piece's last P.V
+            if (gs != 2) tk = ld_acquire_gpu(ticket);
+        }
+        named_bar_sync(bid, kSoftThreads);          // (the piece-end sums of all four warps)
+        wait_bar(bar(B::ODONE + par), (d.pc >> 1) & 1, ctl);
+        tc_fence_after();
+        float acc[RMAX], Lsum[RMAX], Mx[RMAX];
+        {
+            float o[NPAD];
+#pragma unroll
+            for (int c = 0; c < NPAD; c += 16) {
+                float tmp[16];
+                tmem_ld16(tmem + lbase + K::COL_O + par * NPAD + c, tmp);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) o[c + x] = tmp[x];
+            }
+            const float* lw = lred + par * 4 * RMAX;
+#pragma unroll
+            for (int n = 0; n < RMAX; ++n) {
+                Mx[n] = emref[par * RMAX + n];
+                Lsum[n] = lw[n] + lw[RMAX + n] + lw[2 * RMAX + n] + lw[3 * RMAX + n];
+                acc[n] = SPLIT ? (o[2 * n] + o[2 * n + 1]) : o[n];
+            }
+        }
+        tc_fence_before();
+        if constexpr (EWG) mbar_arrive(bar(B::OFREE + par));   // O^T, lred and emref of this parity are read
+        // column n's output row offset, computed by lane n and broadcast
+        const size_t my_off = lanee < ncol ? col_row_offset(p, d.qoff, R, d.hg, lanee, D) : 0;
+        if (complete) {
+#pragma unroll
+            for (int n = 0; n < RMAX; ++n) {
+                const size_t off = __shfl_sync(0xffffffffu, my_off, n);
+                if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(acc[n], Lsum[n]));
+            }
+            return;
+        }
+        if constexpr (SPLIT) {
+            if (bar_red_or(bid, kSoftThreads, gs == 2)) {
+                // the earlier pieces arrive pre-merged; add this one, the last in CTA order
+#pragma unroll
+                for (int n = 0; n < RMAX; ++n) {
+                    float M = gbuf[n], den = gbuf[RMAX + n];
+                    float num = tt < D ? gbuf[2 * RMAX + n * D + tt] : 0.f;
+                    float wo, wn;
+                    merge_weights(M, Mx[n], wo, wn);
+                    den = merge_acc(den, wo, Lsum[n], wn);
+                    num = merge_acc(num, wo, acc[n], wn);
+                    const size_t off = __shfl_sync(0xffffffffu, my_off, n);
+                    if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(num, den));
+                }
+                return;
+            }
+        }
+        const int c_first = d.last ? owner_cta(d.S0, W, P) : 0;
+        const int c_last = d.last ? owner_cta(d.S1 - 1, W, P) : 0;
+        // the last piece merges here when every other piece is published already
+        bool direct = d.last && bar_red_or(bid, kSoftThreads, tk == c_last - c_first);
+        if (!direct) {
+            float* slot = slot_ptr(p, cta, d.S0, u0);
+#pragma unroll
+            for (int n = 0; n < RMAX; ++n) {
+                if (n < ncol) {
+                    if (tt == n) {
+                        slot[n] = Mx[n];
+                        slot[p.rows_pad + n] = Lsum[n];
+                    }
+                    if (tt < D) slot[2 * p.rows_pad + (size_t)n * D + tt] = acc[n];
+                }
+            }
+            if (!d.last) {
+                // hand it to the merge warp (a CTA range cuts at most two segments, so the
+                // 4-entry task ring never wraps onto a pending task)
+                if (tt == 0) {
+                    int* task = reinterpret_cast<int*>(smem + K::OFF_MQ) + (n_tasks & 3) * 8;
+                    task[0] = d.b;
+                    task[1] = d.hg;
+                    task[2] = d.qoff;
+                    task[3] = d.Q;
+                    task[4] = d.S0;
+                    task[5] = d.S1;
+                }
+                mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
+                ++n_tasks;
+                return;
+            }
+            // the last piece: publish here and draw the ticket
+            named_bar_sync(bid, kSoftThreads);     // every thread's part is stored
+            int lst = 0;
+            if (tt == 0) {
+                __threadfence();
+                lst = atomicAdd(ticket, 1) == c_last - c_first;
+                __threadfence();
+            }
+            direct = bar_red_or(bid, kSoftThreads, lst != 0);
+        }
+        if (direct) {
+            // merge in CTA order, this piece from registers (the same steps as
+            // merge_segment_warp, so either place gives the same bits)
+#pragma unroll
+            for (int n0 = 0; n0 < RMAX; n0 += 8) {
+                if (n0 >= ncol) break;
+                float M[8], den[8], num[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    M[x] = -INFINITY;
+                    den[x] = 0.f;
+                    num[x] = 0.f;
+                }
+                for (int c = c_first; c <= c_last; ++c) {
+                    float m[8], l[8], a[8];
+                    if (c == cta) {
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            m[x] = Mx[n0 + x];
+                            l[x] = Lsum[n0 + x];
+                            a[x] = acc[n0 + x];
+                        }
+                    } else {
+                        const float* sl = slot_ptr(p, c, d.S0, cta_start(c, W, P));
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            const int n = n0 + x;
+                            m[x] = n < ncol ? __ldcg(sl + n) : -INFINITY;
+                            l[x] = n < ncol ? __ldcg(sl + p.rows_pad + n) : 0.f;
+                            a[x] = (n < ncol && tt < D) ? __ldcg(sl + 2 * p.rows_pad + (size_t)n * D + tt) : 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        float wo, wn;
+                        merge_weights(M[x], m[x], wo, wn);
+                        den[x] = merge_acc(den[x], wo, l[x], wn);
+                        num[x] = merge_acc(num[x], wo, a[x], wn);
+                    }
+                }
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const int n = n0 + x;
+                    const size_t off = __shfl_sync(0xffffffffu, my_off, n);
+                    if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(num[x], den[x]));
+                }
+            }
+            if (tt == 0) *ticket = 0;              // ready for the next launch
+        }
+    };
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
@@ -564,18 +757,20 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
         __syncwarp();
     } else if (warp == kPvWarp) {
         // ------------------------------------------------------------ P.V issuer
-        // O^T += V^T P^T of tile t once its P is written and its V has landed.
+        // O^T += V^T P^T of tile t once its P is written and its V has landed;
+        // pieces alternate between two accumulators, and a piece's first tile
+        // starts its accumulator afresh once the epilogue of the piece two
+        // before has read it.
         if (lane == 0) {
             constexpr uint32_t idPV = idesc_bf16_f32(128, NPAD, true, true);
             int t = 0, pc = 0;
             bool ok = true;
             while (ok && it.valid()) {
+                const uint32_t ocol = tmem + K::COL_O + (pc & 1) * NPAD;
+                if (EWG && pc >= 2 && !(ok = wait_bar(bar(B::OFREE + (pc & 1)), ((pc >> 1) - 1) & 1, ctl))) break;
                 for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
                     const int np = min(kTP, it.npg - t0);
                     const int vs = t % NSV;
-                    // the tile's warpgroup accumulates into its own O^T; its first tile of the piece starts afresh
-                    const uint32_t ocol = tmem + K::COL_O + ((pc & 1) * NWG + t % NWG) * NPAD;
-                    const bool fresh = t0 < NWG * kTP;
                     if (!(ok = wait_bar(bar(B::PFULL + t % NSB), (t / NSB) & 1, ctl))) break;
                     if (!(ok = wait_bar(bar(B::VFULL + vs), (t / NSV) & 1, ctl))) break;
                     tc_fence_after();
@@ -584,7 +779,7 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                     for (int pg = 0; pg < np; ++pg) {
                         const uint64_t a = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
                         const uint64_t b = smem_desc(pbase + pg * 256, 128, 16 * 128);
-                        mma_bf16(ocol, a, b, idPV, (pg > 0 || !fresh) ? 1u : 0u);
+                        mma_bf16(ocol, a, b, idPV, (pg > 0 || t0 > 0) ? 1u : 0u);
                     }
                     mma_commit(bar(B::PEMPTY + t % NSB));
                     mma_commit(bar(B::VEMPTY + vs));
@@ -598,19 +793,31 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
         }
         __syncwarp();
     } else if (warp == kMergeWarp) {
-        // ------------------------------------------------------------ ticket and merge of published partials
-        // A task is a split piece whose partial the softmax warps have stored;
-        // this warp reads the segment's ticket: when every other piece is
-        // published it merges at once, else it makes the partial visible
-        // GPU-wide, draws a ticket and merges if that ticket is the last one.
+        // ------------------------------------------------------------ hand-offs and the last piece's pre-merge
+        // The split pieces before the CTA's last piece come here in order (the
+        // softmax warps store a partial; this warp reads the segment's ticket:
+        // when every other piece is published it merges at once, else it makes
+        // the partial visible GPU-wide, draws a ticket and merges if that ticket
+        // is the last).  Then, when the last piece is split and ends its
+        // segment, this warp waits for the segment's earlier pieces to be
+        // published and merges them into shared memory, so that the last
+        // epilogue only adds its own part.
+        int n_expect = 0;
+        PieceIter w = it;                 // -> the last piece
+        for (;;) {
+            PieceIter nx = w;
+            nx.advance(p);
+            if (!nx.valid()) break;
+            if (w.S0 < u0 || w.S1 > u1) ++n_expect;
+            w = nx;
+        }
         int* mq = reinterpret_cast<int*>(smem + K::OFF_MQ);
-        for (int n = 0;; ++n) {
-            bool w = lane == 0 ? wait_bar(bar(B::MQFULL + (n & 3)), (n >> 2) & 1, ctl) : true;
-            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+        bool ok = true;
+        for (int n = 0; n < n_expect; ++n) {
+            bool wv = lane == 0 ? wait_bar(bar(B::MQFULL + (n & 3)), (n >> 2) & 1, ctl) : true;
+            if (!(ok = __shfl_sync(0xffffffffu, wv, 0))) break;
             __syncwarp();
             const int* task = mq + (n & 3) * 8;
-            if (task[0] < 0) break;                     // sentinel: the softmax warps are done
-            if (task[6] != 0) continue;                 // merged by the softmax warps already
             const int seg_b = task[0], hg = task[1], S0 = task[4], S1 = task[5];
             int last = 0;
             if (lane == 0) {
@@ -630,25 +837,86 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
             __syncwarp();
             if (last) merge_segment_warp<D>(p, hg, task[2], task[3], S0, S1, W, P, lane);
         }
+        if constexpr (SPLIT) {
+            if (ok && w.S0 < u0 && w.S1 <= u1) {
+                const int c_first = owner_cta(w.S0, W, P);          // this CTA is the segment's last
+                int* ticket = p.tickets + w.cur.b * Hkv + w.hg;
+                const int ncol = HG * G * w.cur.Q;
+                const uint64_t t0 = globaltimer_ns();
+                while (*gstate == 0 && !*abort_flag && globaltimer_ns() - t0 < kWaitLimitNs) {
+                    int v = 0;
+                    if (lane == 0) v = ld_acquire_gpu(ticket);
+                    v = __shfl_sync(0xffffffffu, v, 0);
+                    if (v == cta - c_first) {
+                        int claimed = 0;
+                        if (lane == 0) claimed = atomicCAS(const_cast<int*>(gstate), 0, 1) == 0;
+                        claimed = __shfl_sync(0xffffffffu, claimed, 0);
+                        __syncwarp();
+                        if (claimed) {
+                            // the earlier pieces in CTA order, the same steps as merge_segment_warp
+                            constexpr int DPL = D / 32;
+                            float M[RMAX], den[RMAX], num[RMAX][DPL];
+#pragma unroll
+                            for (int k = 0; k < RMAX; ++k) {
+                                M[k] = -INFINITY;
+                                den[k] = 0.f;
+#pragma unroll
+                                for (int x = 0; x < DPL; ++x) num[k][x] = 0.f;
+                            }
+                            for (int c = c_first; c < cta; ++c) {
+                                const float* sl = slot_ptr(p, c, w.S0, cta_start(c, W, P));
+#pragma unroll
+                                for (int k = 0; k < RMAX; ++k) {
+                                    const bool ld = k < ncol;
+                                    const float m = ld ? __ldcg(sl + k) : -INFINITY;
+                                    const float l = ld ? __ldcg(sl + p.rows_pad + k) : 0.f;
+                                    float wo, wn;
+                                    merge_weights(M[k], m, wo, wn);
+                                    den[k] = merge_acc(den[k], wo, l, wn);
+#pragma unroll
+                                    for (int x = 0; x < DPL; ++x) {
+                                        const float a = ld ? __ldcg(sl + 2 * p.rows_pad + (size_t)k * D + lane + 32 * x) : 0.f;
+                                        num[k][x] = merge_acc(num[k][x], wo, a, wn);
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int k = 0; k < RMAX; ++k) {
+                                if (lane == 0) {
+                                    gbuf[k] = M[k];
+                                    gbuf[RMAX + k] = den[k];
+                                }
+#pragma unroll
+                                for (int x = 0; x < DPL; ++x) gbuf[2 * RMAX + k * D + lane + 32 * x] = num[k][x];
+                            }
+                            __threadfence_block();
+                            __syncwarp();
+                            if (lane == 0) {
+                                *ticket = 0;                    // ready for the next launch
+                                *gstate = 2;
+                            }
+                        }
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+            }
+        }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ softmax / rescale / epilogue
-        // Warpgroup wg takes the tiles t with t % NWG == wg.  A piece's epilogue
-        // (the warpgroups' parts combined, then the output or a partial) runs in
-        // the warpgroup of the next piece's first tile, right after that tile.
-        const int wg = warp >> 2;
-        const int tt = tid & (kSoftThreads - 1);              // token row of S^T, d row of O^T
-        const int bwg = 1 + wg;                               // named barrier of this warpgroup
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        float* red = reinterpret_cast<float*>(smem + K::OFF_RED) + wg * (kTP * RMAX);
-        float* lred = reinterpret_cast<float*>(smem + K::OFF_LRED);   // [2][NWG][4][RMAX]
-        float* emref = reinterpret_cast<float*>(smem + K::OFF_EM);    // [2][NWG][RMAX]
-        int t = 0, n_tasks = 0, pc = 0, jt = 0, t_first = 0;
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ softmax / rescale
+        // One thread per token row of S^T (TMEM lane).  At a piece's end its
+        // column sums and reference max go to lred / emref (double-buffered by
+        // piece parity); the piece's epilogue then runs in the epilogue
+        // warpgroup (EWG), or here after the next piece's first tile.
+        const int tt = tid;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float* red = reinterpret_cast<float*>(smem + K::OFF_RED);
+        int t = 0, pc = 0, jt = 0;
         bool aborted = false;
         float m_ref[RMAX], l_part[RMAX];
-        // the finished piece whose epilogue is pending
-        bool pend = false;
-        int e_b = 0, e_hg = 0, e_qoff = 0, e_Q = 0, e_S0 = 0, e_S1 = 0, e_tfirst = 0, e_ntile = 0, e_pc = 0;
+        bool pend = false;                   // (without EWG) the finished piece whose epilogue is pending
+        PieceDesc pd{};
 #pragma unroll
         for (int n = 0; n < RMAX; ++n) {
             m_ref[n] = -INFINITY;
@@ -657,11 +925,11 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
         bool in_piece = it.valid();
 
         for (;;) {
-            if (in_piece && t % NWG == wg) {
+            if (in_piece) {
                 const int Q = it.cur.Q, R = G * Q, L = it.cur.L, lim0 = L - Q;
                 const int np = min(kTP, it.npg - jt * kTP);
                 const int vs = t % NSV;
-                const uint32_t ocol = K::COL_O + ((pc & 1) * NWG + wg) * NPAD;
+                const uint32_t ocol = K::COL_O + (pc & 1) * NPAD;
                 // this thread's token: unit slot k of the tile -> (page, kv-head), position
                 const int k = tt >> 4;
                 const int qu = it.pg0 + jt * kTP + k;
@@ -689,7 +957,7 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                     s[n] = vis ? s[n] * p.scale_log2 : -INFINITY;
                     need |= s[n] > m_ref[n] + kRescaleSlack;
                 }
-                if (bar_red_or(bwg, kSoftThreads, need || !okw)) {
+                if (bar_red_or(kBarSoft, kSoftThreads, need || !okw)) {
                     // raise the reference to this tile's max (first tile of a piece, or a big jump):
                     // per (unit slot, column) maxima over the slot's 16 tokens, then per column
 #pragma unroll
@@ -699,7 +967,7 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                         for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                         if ((tt & 15) == 0) red[k * RMAX + n] = mx;
                     }
-                    if (bar_red_or(bwg, kSoftThreads, !okw || *abort_flag)) {
+                    if (bar_red_or(kBarSoft, kSoftThreads, !okw || *abort_flag)) {
                         aborted = true;
                         break;
                     }
@@ -716,9 +984,9 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                         m_ref[n] = mn;
                         l_part[n] *= alpha[n];
                     }
-                    if (jt >= NWG && any_scale) {
-                        // O^T (TMEM) *= alpha once this warpgroup's previous P.V has landed
-                        wait_bar(bar(B::PEMPTY + (t - NWG) % NSB), ((t - NWG) / NSB) & 1, ctl);
+                    if (jt > 0 && any_scale) {
+                        // O^T (TMEM) *= alpha once the previous tile's P.V has landed
+                        wait_bar(bar(B::PEMPTY + (t - 1) % NSB), ((t - 1) / NSB) & 1, ctl);
                         tc_fence_after();
 #pragma unroll
                         for (int c = 0; c < NPAD; c += 16) {
@@ -730,7 +998,7 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                         }
                     }
                     // keep red[] stable until every thread has read it
-                    named_bar_sync(bwg, kSoftThreads);
+                    named_bar_sync(kBarSoft, kSoftThreads);
                 }
                 float pr[RMAX];
 #pragma unroll
@@ -771,188 +1039,31 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bar(B::PFULL + t % NSB));
-            }
-            if (in_piece) ++t;
 
-            if (pend && (!in_piece || jt == 0)) {
-                // ---- epilogue of the previous piece, in the warpgroup of the tile just taken
-                // (or, after the last piece, of the tile that would come next)
-                pend = false;
-                const bool complete = (e_S0 >= u0) && (e_S1 <= u1);
-                if ((in_piece ? t - 1 : t) % NWG == wg) {
-                    const int R = G * e_Q, ncol = HG * R, par = e_pc & 1;
-                    // a split piece reads its segment's ticket first: the load's latency
-                    // overlaps the wait for the piece's last P.V
-                    int* ticket = p.tickets + e_b * Hkv + e_hg;
-                    int tk = -1;
-                    if (!complete && tt == 0) tk = ld_acquire_gpu(ticket);
-                    named_bar_sync(bwg, kSoftThreads);     // (one warpgroup: its piece-end sums)
-                    // this piece's O^T accumulators are final once its last P.V is done
-                    wait_bar(bar(B::ODONE + par), (e_pc >> 1) & 1, ctl);
-                    tc_fence_after();
-                    float acc[RMAX], Lsum[RMAX], Mx[RMAX];
-#pragma unroll
-                    for (int n = 0; n < RMAX; ++n) {
-                        acc[n] = 0.f;
-                        Lsum[n] = 0.f;
-                        Mx[n] = -INFINITY;
-                    }
-                    // common reference: the max over the warpgroups that had tiles in the piece
-#pragma unroll
-                    for (int w2 = 0; w2 < NWG; ++w2) {
-                        if (e_ntile >= NWG || e_tfirst % NWG == w2) {
-#pragma unroll
-                            for (int n = 0; n < RMAX; ++n) Mx[n] = fmaxf(Mx[n], emref[(par * NWG + w2) * RMAX + n]);
-                        }
-                    }
-#pragma unroll
-                    for (int w2 = 0; w2 < NWG; ++w2) {
-                        if (e_ntile >= NWG || e_tfirst % NWG == w2) {
-                            float o[NPAD];
-#pragma unroll
-                            for (int c = 0; c < NPAD; c += 16) {
-                                float tmp[16];
-                                tmem_ld16(tmem + lane_base + K::COL_O + (par * NWG + w2) * NPAD + c, tmp);
-#pragma unroll
-                                for (int x = 0; x < 16; ++x) o[c + x] = tmp[x];
-                            }
-                            const float* lw = lred + (par * NWG + w2) * 4 * RMAX;
-#pragma unroll
-                            for (int n = 0; n < RMAX; ++n) {
-                                const float mw = emref[(par * NWG + w2) * RMAX + n];
-                                // this warpgroup's part, brought to the common reference
-                                const float a = NWG == 1 ? 1.f : (mw == -INFINITY ? 0.f : fast_exp2(mw - Mx[n]));
-                                const float lsum = lw[n] + lw[RMAX + n] + lw[2 * RMAX + n] + lw[3 * RMAX + n];
-                                const float ow = SPLIT ? (o[2 * n] + o[2 * n + 1]) : o[n];
-                                Lsum[n] = __fmaf_rn(lsum, a, Lsum[n]);
-                                acc[n] = __fmaf_rn(ow, a, acc[n]);
-                            }
-                        }
-                    }
-                    tc_fence_before();
-                    // column n's output row offset, computed by lane n and broadcast
-                    const size_t my_off = lane < ncol ? col_row_offset(p, e_qoff, R, e_hg, lane, D) : 0;
-                    if (complete) {
-#pragma unroll
-                        for (int n = 0; n < RMAX; ++n) {
-                            const size_t off = __shfl_sync(0xffffffffu, my_off, n);
-                            if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(acc[n], Lsum[n]));
-                        }
-                    } else {
-                        const int c_first = owner_cta(e_S0, W, P), c_last = owner_cta(e_S1 - 1, W, P);
-                        // Every other piece published already (early ticket read): merge here.
-                        // Otherwise store the partial; a later piece hands it to the merge warp,
-                        // while the CTA's last piece publishes it and draws its ticket here.
-                        bool direct = bar_red_or(bwg, kSoftThreads, tk == c_last - c_first);
-                        bool handed = false;
-                        if (!direct) {
-                            float* slot = slot_ptr(p, cta, e_S0, u0);
-#pragma unroll
-                            for (int n = 0; n < RMAX; ++n) {
-                                if (n < ncol) {
-                                    if (tt == n) {
-                                        slot[n] = Mx[n];
-                                        slot[p.rows_pad + n] = Lsum[n];
-                                    }
-                                    if (tt < D) slot[2 * p.rows_pad + (size_t)n * D + tt] = acc[n];
-                                }
-                            }
-                            if (in_piece) {
-                                // (a CTA range cuts at most two segments, so the 4-entry task ring
-                                // never wraps onto a pending task)
-                                if (tt == 0) {
-                                    int* task = reinterpret_cast<int*>(smem + K::OFF_MQ) + (n_tasks & 3) * 8;
-                                    task[0] = e_b;
-                                    task[1] = e_hg;
-                                    task[2] = e_qoff;
-                                    task[3] = e_Q;
-                                    task[4] = e_S0;
-                                    task[5] = e_S1;
-                                    task[6] = 0;
-                                }
-                                mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
-                                handed = true;
-                            } else {
-                                named_bar_sync(bwg, kSoftThreads);     // every thread's part is stored
-                                int lst = 0;
-                                if (tt == 0) {
-                                    __threadfence();
-                                    lst = atomicAdd(ticket, 1) == c_last - c_first;
-                                    __threadfence();
-                                }
-                                direct = bar_red_or(bwg, kSoftThreads, lst != 0);
-                            }
-                        }
-                        if (direct) {
-                            // merge in CTA order, this piece from registers (the same steps as
-                            // merge_segment_warp, so either place gives the same bits)
-#pragma unroll
-                            for (int n0 = 0; n0 < RMAX; n0 += 8) {
-                                if (n0 >= ncol) break;
-                                float M[8], den[8], num[8];
-#pragma unroll
-                                for (int x = 0; x < 8; ++x) {
-                                    M[x] = -INFINITY;
-                                    den[x] = 0.f;
-                                    num[x] = 0.f;
-                                }
-                                for (int c = c_first; c <= c_last; ++c) {
-                                    float m[8], l[8], a[8];
-                                    if (c == cta) {
-#pragma unroll
-                                        for (int x = 0; x < 8; ++x) {
-                                            m[x] = Mx[n0 + x];
-                                            l[x] = Lsum[n0 + x];
-                                            a[x] = acc[n0 + x];
-                                        }
-                                    } else {
-                                        const float* sl = slot_ptr(p, c, e_S0, cta_start(c, W, P));
-#pragma unroll
-                                        for (int x = 0; x < 8; ++x) {
-                                            const int n = n0 + x;
-                                            m[x] = n < ncol ? __ldcg(sl + n) : -INFINITY;
-                                            l[x] = n < ncol ? __ldcg(sl + p.rows_pad + n) : 0.f;
-                                            a[x] = (n < ncol && tt < D) ? __ldcg(sl + 2 * p.rows_pad + (size_t)n * D + tt) : 0.f;
-                                        }
-                                    }
-#pragma unroll
-                                    for (int x = 0; x < 8; ++x) {
-                                        float wo, wn;
-                                        merge_weights(M[x], m[x], wo, wn);
-                                        den[x] = merge_acc(den[x], wo, l[x], wn);
-                                        num[x] = merge_acc(num[x], wo, a[x], wn);
-                                    }
-                                }
-#pragma unroll
-                                for (int x = 0; x < 8; ++x) {
-                                    const int n = n0 + x;
-                                    const size_t off = __shfl_sync(0xffffffffu, my_off, n);
-                                    if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(num[x], den[x]));
-                                }
-                            }
-                            if (tt == 0) *ticket = 0;              // ready for the next launch
-                        }
-                        if (!handed) {
-                            // its ring entry: nothing left for the merge warp (which walks the ring in order)
-                            if (tt == 0) {
-                                int* task = reinterpret_cast<int*>(smem + K::OFF_MQ) + (n_tasks & 3) * 8;
-                                task[0] = e_b;                      // (not a sentinel)
-                                task[6] = 1;
-                            }
-                            mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
-                        }
-                    }
+                ++t;
+            }
+            if constexpr (!EWG) {
+                if (pend && (!in_piece || jt == 0)) {
+                    pend = false;
+                    pd.last = !in_piece;
+                    piece_epilogue(pd, tt, kBarSoft);
                 }
-                if (!complete) ++n_tasks;                  // every warpgroup counts the ring entries
             }
             if (!in_piece) break;
 
             if (++jt * kTP >= it.npg) {
-                // piece end, in every warpgroup: its column sums and reference max for
-                // the epilogue (double-buffered by piece parity)
+                // piece end: its column sums and reference max for the epilogue
                 const int par = pc & 1;
+                if (EWG && pc >= 2) {
+                    // lred / emref of this parity are free once piece pc - 2's epilogue has read them
+                    const bool okf = wait_bar(bar(B::OFREE + par), ((pc >> 1) - 1) & 1, ctl);
+                    if (bar_red_or(kBarSoft, kSoftThreads, !okf)) {
+                        aborted = true;
+                        break;
+                    }
+                }
                 const int ncol = HG * G * it.cur.Q;
-                float* lw = lred + ((par * NWG + wg) * 4 + (warp & 3)) * RMAX;
+                float* lw = lred + (par * 4 + warp) * RMAX;
 #pragma unroll
                 for (int n = 0; n < RMAX; ++n) {
                     if (n < ncol) {
@@ -961,27 +1072,15 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                         for (int o2 = 16; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
                         if (lane == 0) lw[n] = v;
                     }
-                    if (tt == 0) emref[(par * NWG + wg) * RMAX + n] = m_ref[n];
+                    if (tt == 0) emref[par * RMAX + n] = m_ref[n];
                 }
-                if constexpr (NWG > 1) {
-                    // every warpgroup's part of this piece is written (bounded wait)
-                    mbar_arrive(bar(B::PEND));
-                    const bool okp = wait_bar(bar(B::PEND), pc & 1, ctl);
-                    if (bar_red_or(bwg, kSoftThreads, !okp)) {   // the warpgroup leaves together
-                        aborted = true;
-                        break;
-                    }
-                }
-                pend = true;
-                e_b = it.cur.b;
-                e_hg = it.hg;
-                e_qoff = it.cur.qoff;
-                e_Q = it.cur.Q;
-                e_S0 = it.S0;
-                e_S1 = it.S1;
-                e_tfirst = t_first;
-                e_ntile = jt;
-                e_pc = pc;
+                pd.b = it.cur.b;
+                pd.hg = it.hg;
+                pd.qoff = it.cur.qoff;
+                pd.Q = it.cur.Q;
+                pd.S0 = it.S0;
+                pd.S1 = it.S1;
+                pd.pc = pc;
 #pragma unroll
                 for (int n = 0; n < RMAX; ++n) {
                     m_ref[n] = -INFINITY;
@@ -989,14 +1088,48 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
                 }
                 ++pc;
                 jt = 0;
-                t_first = t;
                 it.advance(p);
                 in_piece = it.valid();
+                if constexpr (EWG) {
+                    // hand the piece over: descriptor, then every thread's arrive (its sums are stored)
+                    if (tt == 0) {
+                        int* q = pdesc + par * 8;
+                        q[0] = pd.b;
+                        q[1] = pd.hg;
+                        q[2] = pd.qoff;
+                        q[3] = pd.Q;
+                        q[4] = pd.S0;
+                        q[5] = pd.S1;
+                        q[6] = in_piece ? 0 : 1;
+                    }
+                    mbar_arrive(bar(B::PREADY + par));
+                } else {
+                    pend = true;
+                }
             }
         }
-        if (!aborted && t % NWG == wg) {   // sentinel for the merge warp, after the last epilogue
-            if (tt == 0) reinterpret_cast<int*>(smem + K::OFF_MQ)[(n_tasks & 3) * 8] = -1;
-            mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
+        (void)aborted;
+    } else if (warp >= kEpiWarp0) {
+        // ------------------------------------------------------------ epilogue warpgroup
+        if constexpr (EWG) {
+            const int tt = tid - kEpiWarp0 * 32;
+            for (int pc = 0;; ++pc) {
+                const int par = pc & 1;
+                const bool okr = wait_bar(bar(B::PREADY + par), (pc >> 1) & 1, ctl);
+                if (bar_red_or(kBarEpi, kSoftThreads, !okr)) break;
+                const int* q = pdesc + par * 8;
+                PieceDesc d;
+                d.b = q[0];
+                d.hg = q[1];
+                d.qoff = q[2];
+                d.Q = q[3];
+                d.S0 = q[4];
+                d.S1 = q[5];
+                d.last = q[6] != 0;
+                d.pc = pc;
+                piece_epilogue(d, tt, kBarEpi);
+                if (d.last) break;
+            }
         }
     }
 
@@ -1009,13 +1142,13 @@ __global__ void __launch_bounds__(Roles<NWG>::kThreads, 1) attn_tc_kernel(const 
     }
 }
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV, int NWG>
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG>
 static cudaError_t launch_t(const AttnParams& p, int ncta, cudaStream_t st) {
-    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, NWG>;
-    auto kern = attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV, NWG>;
+    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG>;
+    auto kern = attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV, EWG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(ncta), dim3(Roles<NWG>::kThreads), K::SMEM, st, p);
+    return launch_pdl(kern, dim3(ncta), dim3(threads_of<EWG>()), K::SMEM, st, p);
 }
 
 }  // namespace tc
@@ -1035,13 +1168,15 @@ int tc_heads_per_segment(int num_kv_heads, int rows) {
 }
 
 // bf16 cache, head_dim 64/128, R = G * max_q_len <= 32.  Narrow segments (N =
-// 16) run two softmax warpgroups; wide ones (N = 32) one, for its registers.
+// 16) run the epilogue in its own warpgroup; wide ones (N = 32), whose softmax
+// needs more registers than a 384-thread block leaves, in the softmax warps.
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, int ncta, cudaStream_t st) {
     const bool split = tc_col_limit(p.rows) == 8;
     if (head_dim == 128)
-        return split ? tc::launch_t<128, 16, true, 2, 4, 2>(p, ncta, st)
-                     : tc::launch_t<128, 32, false, 2, 3, 1>(p, ncta, st);
-    return split ? tc::launch_t<64, 16, true, 4, 6, 2>(p, ncta, st) : tc::launch_t<64, 32, false, 4, 6, 1>(p, ncta, st);
+        return split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
+                     : tc::launch_t<128, 32, false, 2, 3, false>(p, ncta, st);
+    return split ? tc::launch_t<64, 16, true, 4, 6, true>(p, ncta, st)
+                 : tc::launch_t<64, 32, false, 4, 6, false>(p, ncta, st);
 }
 
 }  // namespace pkv

@@ -105,6 +105,23 @@ def test_deterministic_run_to_run():
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("n", [2, 3, 4])
+def test_repeated_calls_reuse_the_workspace(n):
+    """Calls that share a workspace give the same bits, and each call leaves
+    every merge ticket at zero (the workspace is ready for the next call)."""
+    w = config_workload(n)
+    dw = DeviceWorkload(w)
+    dw.prefill()
+    dw.append_step()
+    first = out_bits(dw.attend())
+    for _ in range(3):
+        again = out_bits(dw.attend())
+        assert np.array_equal(again, first)
+    tickets = dw.workspace[256:256 + 4 * w.num_seqs * w.num_kv_heads].view(torch.int32)
+    assert int(tickets.abs().sum().item()) == 0
+    assert dw.errors() == (0, 0)
+
+
 def test_block_permutation_invariance_bitwise():
     w = wl.make_workload("perm", context_lens=[70, 333, 128, 1000], q_lens=[1, 3, 2, 1], num_q_heads=16,
                          num_kv_heads=4, head_dim=128, seed=71, pool_factor=2.0)
