@@ -177,6 +177,36 @@ __device__ __forceinline__ bool bar_red_or(int id, int n, bool v) {
     return r != 0;
 }
 
+// Reduction (sum or max) of N per-lane columns over aligned groups of lanes,
+// by exchanges with lane ^ S for S = G/2 .. 1 (G the group size): at each
+// exchange a lane keeps half of its columns and receives the partner's values
+// of that half, so the whole reduction takes N - 1 shuffles (plus one per
+// exchange once a single column is left) instead of N log2(G).  On return
+// a[0] holds the group's result for column col (N <= G; lanes that differ only
+// in the bits below log2(G / N) hold the same column).
+template <int N, int S, bool MAX>
+struct Butterfly {
+    static __device__ __forceinline__ void run(float* a, int lane, int& col) {
+        if constexpr (N > 1) {
+            constexpr int H = N / 2;
+            const bool up = (lane & S) != 0;
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                const float send = up ? a[j] : a[H + j];
+                const float keep = up ? a[H + j] : a[j];
+                const float got = __shfl_xor_sync(0xffffffffu, send, S);
+                a[j] = MAX ? fmaxf(keep, got) : keep + got;
+            }
+            if (up) col += H;
+            if constexpr (S > 1) Butterfly<H, S / 2, MAX>::run(a, lane, col);
+        } else {
+            const float got = __shfl_xor_sync(0xffffffffu, a[0], S);
+            a[0] = MAX ? fmaxf(a[0], got) : a[0] + got;
+            if constexpr (S > 1) Butterfly<1, S / 2, MAX>::run(a, lane, col);
+        }
+    }
+};
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -960,12 +990,21 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 if (bar_red_or(kBarSoft, kSoftThreads, need || !okw)) {
                     // raise the reference to this tile's max (first tile of a piece, or a big jump):
                     // per (unit slot, column) maxima over the slot's 16 tokens, then per column
+                    if constexpr (RMAX <= 16) {
+                        float a[RMAX];
 #pragma unroll
-                    for (int n = 0; n < RMAX; ++n) {
-                        float mx = s[n];
+                        for (int n = 0; n < RMAX; ++n) a[n] = s[n];
+                        int col = 0;
+                        Butterfly<RMAX, 8, true>::run(a, lane, col);
+                        if ((lane & (16 / RMAX - 1)) == 0) red[k * RMAX + col] = a[0];
+                    } else {
 #pragma unroll
-                        for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                        if ((tt & 15) == 0) red[k * RMAX + n] = mx;
+                        for (int n = 0; n < RMAX; ++n) {
+                            float mx = s[n];
+#pragma unroll
+                            for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                            if ((tt & 15) == 0) red[k * RMAX + n] = mx;
+                        }
                     }
                     if (bar_red_or(kBarSoft, kSoftThreads, !okw || *abort_flag)) {
                         aborted = true;
@@ -1062,18 +1101,15 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         break;
                     }
                 }
-                const int ncol = HG * G * it.cur.Q;
                 float* lw = lred + (par * 4 + warp) * RMAX;
-#pragma unroll
-                for (int n = 0; n < RMAX; ++n) {
-                    if (n < ncol) {
-                        float v = l_part[n];
-#pragma unroll
-                        for (int o2 = 16; o2 >= 1; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
-                        if (lane == 0) lw[n] = v;
-                    }
-                    if (tt == 0) emref[par * RMAX + n] = m_ref[n];
+                {
+                    int col = 0;
+                    Butterfly<RMAX, 16, false>::run(l_part, lane, col);   // (l_part is reset below)
+                    if ((lane & (32 / RMAX - 1)) == 0) lw[col] = l_part[0];
                 }
+#pragma unroll
+                for (int n = 0; n < RMAX; ++n)
+                    if (tt == 0) emref[par * RMAX + n] = m_ref[n];
                 pd.b = it.cur.b;
                 pd.hg = it.hg;
                 pd.qoff = it.cur.qoff;
