@@ -9,8 +9,11 @@ merged in-kernel) on the continuous-batch decode workload: 32 sequences,
 
 Prints ONE JSON line (rank 0).  `value` is KV GB/s of the whole step
 (algorithmic KV bytes / device time of append + attention), inputs resident in
-HBM, L2 flushed between timed steps.  `--impl reference` times the CPU oracle
-on the host cores instead (a deliberately slow reference).
+HBM; by default the timed steps rotate over enough copies of the workload
+that no step finds its K/V in L2 (`--l2 flush` writes a buffer of twice the L2
+size before every step instead, which also evicts the kernels' code).
+`--impl reference` times the CPU oracle on the host cores instead (a
+deliberately slow reference).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch with torchrun (one rank per GPU); every rank runs its own
@@ -46,7 +49,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--l2", choices=["flush", "rotate"], default="flush",
+    ap.add_argument("--l2", choices=["flush", "rotate"], default="rotate",
                     help="keep timed inputs out of L2: flush it before every step (a write of 2x its size), "
                          "or rotate over enough copies of the workload that the data read by a step is not in L2")
     ap.add_argument("--soak-seconds", type=float, default=1.5,
