@@ -468,8 +468,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 }
                 __threadfence_block();
             }
-            // the segment's ticket: its latency overlaps the wait for the piece's last P.V
-            if (gs != 2) tk = ld_acquire_gpu(ticket);
+            // the segment's ticket, read without blocking: its latency overlaps the wait
+            // for the piece's last P.V and the O^T read (an acquire fence follows only
+            // if it shows every other piece published)
+            if (gs != 2) tk = ld_relaxed_gpu(ticket);
         }
         named_bar_sync(bid, kSoftThreads);          // (the piece-end sums of all four warps)
         wait_bar(bar(B::ODONE + par), (d.pc >> 1) & 1, ctl);
@@ -524,6 +526,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         const int c_first = d.last ? owner_cta(d.S0, W, P) : 0;
         const int c_last = d.last ? owner_cta(d.S1 - 1, W, P) : 0;
         // the last piece merges here when every other piece is published already
+        if (tt == 0 && tk == c_last - c_first) fence_acquire_gpu();
         bool direct = d.last && bar_red_or(bid, kSoftThreads, tk == c_last - c_first);
         if (!direct) {
             float* slot = slot_ptr(p, cta, d.S0, u0);
@@ -556,11 +559,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             // the last piece: publish here and draw the ticket
             named_bar_sync(bid, kSoftThreads);     // every thread's part is stored
             int lst = 0;
-            if (tt == 0) {
-                __threadfence();
-                lst = atomicAdd(ticket, 1) == c_last - c_first;
-                __threadfence();
-            }
+            if (tt == 0) lst = atom_add_acq_rel_gpu(ticket, 1) == c_last - c_first;
             direct = bar_red_or(bid, kSoftThreads, lst != 0);
         }
         if (direct) {
@@ -857,9 +856,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     // every other piece is published (and visible): merge without publishing this one
                     last = 1;
                 } else {
-                    __threadfence();                    // the partial (stored before the arrive) first
-                    last = atomicAdd(ticket, 1) == need - 1;
-                    __threadfence();
+                    // publish the partial (stored before the arrive) and draw the ticket
+                    last = atom_add_acq_rel_gpu(ticket, 1) == need - 1;
                 }
                 if (last) *ticket = 0;                  // ready for the next launch
             }
@@ -873,9 +871,14 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 int* ticket = p.tickets + w.cur.b * Hkv + w.hg;
                 const int ncol = HG * G * w.cur.Q;
                 const uint64_t t0 = globaltimer_ns();
+                // (relaxed polls, one acquire fence once the count is reached: an acquire
+                // per poll would slow the rest of the SM)
                 while (*gstate == 0 && !*abort_flag && globaltimer_ns() - t0 < kWaitLimitNs) {
                     int v = 0;
-                    if (lane == 0) v = ld_acquire_gpu(ticket);
+                    if (lane == 0) {
+                        v = ld_relaxed_gpu(ticket);
+                        if (v == cta - c_first) fence_acquire_gpu();
+                    }
                     v = __shfl_sync(0xffffffffu, v, 0);
                     if (v == cta - c_first) {
                         int claimed = 0;
@@ -928,7 +931,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         }
                         break;
                     }
-                    __nanosleep(256);
+                    __nanosleep(1000);
                 }
             }
         }
