@@ -147,6 +147,14 @@ __device__ __forceinline__ int div_small(int n, int d) {
     return (int)__fdividef((float)n + 0.5f, (float)d);
 }
 
+// CTAs that take part: every one gets at least kMinUnitsPerCta units (two
+// 128-token tiles), so a small batch is not spread so thin that a segment
+// crosses dozens of CTAs and its merge walks dozens of partials.
+constexpr int kMinUnitsPerCta = 16;
+__device__ __forceinline__ int participating_ctas(int ncta, int W) {
+    return W <= 0 ? 0 : max(1, min(ncta, W / kMinUnitsPerCta));
+}
+
 // CTA owning unit u under the partition above (P = participating CTAs <= W,
 // so every CTA in [owner(S0), owner(S1 - 1)] holds a piece of [S0, S1)).
 __device__ __forceinline__ int owner_cta(int u, int W, int ncta) {
@@ -204,7 +212,7 @@ __device__ __forceinline__ int block_scan_incl(int v, int* scratch /* NT/32 + 1 
     return v + add;
 }
 
-// Computes W (total units) and the number P = min(grid, W) of CTAs that take
+// Computes W (total units) and the number P = participating_ctas(grid, W) of CTAs that take
 // part, and positions a cursor at the sequence holding unit u0 of this CTA
 // (and, if tail != nullptr, one at the sequence holding its last unit u1 - 1).
 // All NT threads must call it.  CTA 0 reports invalid lengths.  Returns false
@@ -262,7 +270,7 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         const int2 inc = block_scan2_incl<NT>(make_int2(u, q), s2);
         if (seqtab && b < p.num_seqs) seqtab[b] = make_int4(L, Q, inc.x - u, inc.y - q);
         const int W = s2[NT / 32].x;
-        const int P = min(ncta, W);
+        const int P = participating_ctas(ncta, W);
         *W_out = W;
         *P_out = P;
         if (cta >= P) return false;
@@ -306,9 +314,9 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         __syncthreads();
     }
     const int W = total;
-    // With more CTAs than units, only the first W CTAs take part, so that every
-    // participating CTA owns at least one unit.
-    const int P = min(ncta, W);
+    // With few units, only the first P CTAs take part (at least
+    // kMinUnitsPerCta units each, or all W units in one CTA).
+    const int P = participating_ctas(ncta, W);
     *W_out = W;
     *P_out = P;
     if (cta >= P) return false;
