@@ -8,19 +8,20 @@ namespace pkv {
 cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_new, const int64_t* slots,
                           int64_t num_tokens, int* err, cudaStream_t st, int num_sms);
 cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
-cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, int ncta, cudaStream_t st);
+cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st);
 int simt_rows_pad(int rows);
 int tc_heads_per_segment(int num_kv_heads, int rows);
 
 // Kernel choice and grid for one attention call: the tensor-core kernel for
-// bf16 caches (R = G * max_q_len <= 32; one persistent CTA per SM, all of its
-// ~227 KiB of shared memory), the CUDA-core kernel for FP8 caches (4 CTAs per
-// SM).  rows_pad: partial-slot rows (the tensor-core kernel keeps up to 32
-// columns of several kv-heads per segment).
+// bf16 caches with R = G * max_q_len <= 32 and for FP8 caches with head_dim
+// 128 and R <= 8 (one persistent CTA per SM, all of its ~227 KiB of shared
+// memory), else the CUDA-core kernel (4 CTAs per SM).  rows_pad: partial-slot
+// rows (the tensor-core kernel keeps up to 32 columns of several kv-heads per
+// segment).
 AttnLaunch plan_attention(const pkv_cache* c, int group, int max_q_len, int num_ctas, int num_sms) {
     AttnLaunch L;
     const int rows = group * max_q_len;
-    L.tc = c->kv_dtype == PKV_KV_BF16 && rows <= 32;
+    L.tc = c->kv_dtype == PKV_KV_BF16 ? rows <= 32 : (c->head_dim == 128 && rows <= 8);
     L.ncta = num_ctas > 0 ? num_ctas : (L.tc ? num_sms : 4 * num_sms);
     L.rows_pad = L.tc ? 32 : simt_rows_pad(rows);
     L.hg = L.tc ? tc_heads_per_segment(c->num_kv_heads, rows) : 1;
@@ -28,7 +29,7 @@ AttnLaunch plan_attention(const pkv_cache* c, int group, int max_q_len, int num_
 }
 
 cudaError_t launch_attention(const AttnLaunch& L, const AttnParams& p, int head_dim, int elem_bytes, cudaStream_t st) {
-    return L.tc ? launch_attention_tc(p, head_dim, L.ncta, st) : launch_attention_simt(p, head_dim, elem_bytes, L.ncta, st);
+    return L.tc ? launch_attention_tc(p, head_dim, elem_bytes == 1, L.ncta, st) : launch_attention_simt(p, head_dim, elem_bytes, L.ncta, st);
 }
 
 namespace {

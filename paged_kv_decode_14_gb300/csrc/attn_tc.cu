@@ -79,16 +79,23 @@ constexpr int kSeqTab = 256;                  // sequences the shared-memory tab
 // Online-softmax reference slack (powers of two), see the header comment.
 constexpr float kRescaleSlack = 8.f;
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG>
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8>
 struct Cfg {
     static constexpr int RMAX = SPLIT ? NPAD / 2 : NPAD;  // logical columns
-    static constexpr int PAGE = kBlock * D * 2;
+    static constexpr int PAGE = kBlock * D * 2;         // a page as bf16 MMA operand
+    static constexpr int PAGE8 = kBlock * D;            // an FP8 cache page
+    static constexpr int TILE8 = kTP * PAGE8;
+    static constexpr int NS8 = 2;                       // FP8 staging ring depth (K and V each)
+    static constexpr int NSC = 16;                      // scale ring: tiles the producer may lead by, bounded
     static constexpr int NCH = D / 8;                   // 16-byte chunks per token row
     static constexpr int TILE = kTP * PAGE;
     static constexpr int VSLACK = D == 64 ? 1024 : 0;   // M=128 PV on D=64 reads 1 KiB past a page
     static constexpr int OFF_K = 0;                     // + st * TILE
     static constexpr int OFF_V = NSK * TILE;            // + st * (TILE + VSLACK)
-    static constexpr int OFF_Q = OFF_V + NSV * (TILE + VSLACK);
+    static constexpr int OFF_K8 = OFF_V + NSV * (TILE + VSLACK);   // FP8 staging: + st * TILE8
+    static constexpr int OFF_V8 = OFF_K8 + (FP8 ? NS8 * TILE8 : 0);
+    static constexpr int OFF_SC = OFF_V8 + (FP8 ? NS8 * TILE8 : 0);  // float [NSC][k scales 8, v scales 8]
+    static constexpr int OFF_Q = OFF_SC + (FP8 ? NSC * 16 * 4 : 0);
     static constexpr int QBUF = NPAD * D * 2;
     static constexpr int OFF_P = OFF_Q + 2 * QBUF;
     static constexpr int PBUF = NPAD * kTileTok * 2;
@@ -97,12 +104,13 @@ struct Cfg {
     static constexpr int OFF_EM = OFF_LRED + 2 * 4 * RMAX * 4;         // float [2][RMAX]
     static constexpr int OFF_PD = OFF_EM + 2 * RMAX * 4;               // int [2][8]: piece descriptors
     static constexpr int OFF_BAR = OFF_PD + 2 * 8 * 4;
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 16;   // the barriers of Bars
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 16 + (FP8 ? 4 * NS8 + NSC : 0);   // the barriers of Bars
     static constexpr int OFF_MISC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // tmem addr, abort, zero, gather state
     static constexpr int OFF_MQ = OFF_MISC + 16;         // merge tasks: int [4][8]
-    static constexpr int OFF_SEQ = OFF_MQ + 128;         // int4 [kSeqTab]: per-sequence (L, Q, Ub, qoff)
+    static constexpr int OFF_SEQ = OFF_MQ + 128;         // int4 [SEQTAB]: per-sequence (L, Q, Ub, qoff)
     // pre-merged earlier pieces of the CTA's last segment: M[RMAX], den[RMAX], num[RMAX][D]
-    static constexpr int OFF_GATHER = OFF_SEQ + kSeqTab * 16;
+    static constexpr int SEQTAB = FP8 ? kSeqTab / 2 : kSeqTab;   // sequences the table holds
+    static constexpr int OFF_GATHER = OFF_SEQ + SEQTAB * 16;
     static constexpr int GATHER = SPLIT ? RMAX * (D + 2) * 4 : 0;
     static constexpr int SMEM_USED = OFF_GATHER + GATHER + 128;  // + base alignment slack
     // One CTA per SM either way: take the whole per-block budget, so every
@@ -117,14 +125,17 @@ struct Cfg {
     static_assert(SMEM_USED <= SMEM, "shared memory budget");
 };
 
-template <int NSK, int NSV>
+template <int NSK, int NSV, bool FP8>
 struct Bars {
     static constexpr int KFULL = 0, KEMPTY = NSK, VFULL = 2 * NSK, VEMPTY = 2 * NSK + NSV,
                          SFULL = 2 * NSK + 2 * NSV, PFULL = SFULL + NSB, PEMPTY = PFULL + NSB,
                          QFULL = PEMPTY + NSB, QEMPTY = QFULL + 2, DONE = QEMPTY + 2, MQFULL = DONE + 2,
                          ODONE = MQFULL + 4,      // [2]: last P.V of a piece of that parity done
                          PREADY = ODONE + 2,      // [2]: a piece of that parity handed to the epilogue
-                         OFREE = PREADY + 2;      // [2]: its epilogue has read O^T, lred and emref
+                         OFREE = PREADY + 2,      // [2]: its epilogue has read O^T, lred and emref
+                         // FP8 only: staging rings (bulk copy -> conversion) and the scale ring
+                         K8FULL = OFREE + 2, K8EMPTY = K8FULL + 2, V8FULL = K8EMPTY + 2, V8EMPTY = V8FULL + 2,
+                         SCALE = V8EMPTY + 2, END = FP8 ? SCALE + 16 : OFREE + 2;
 };
 
 // A finished piece, as its epilogue needs it.
@@ -340,11 +351,12 @@ __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q,
     }
 }
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG>
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8>
 __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const AttnParams p) {
-    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG>;
-    using B = Bars<NSK, NSV>;
-    static_assert(B::OFREE + 2 == K::NBAR, "barrier count");
+    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>;
+    using B = Bars<NSK, NSV, FP8>;
+    static_assert(B::END == K::NBAR, "barrier count");
+    static_assert(!FP8 || EWG, "FP8 pages are converted by the epilogue warpgroup");
     constexpr int RMAX = K::RMAX;
     constexpr int kThreads = threads_of<EWG>();
     extern __shared__ uint8_t smem_raw[];
@@ -375,13 +387,24 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         reinterpret_cast<uint4*>(smem + K::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
+        // K/V operand slots are filled by bulk copies (bf16) or by the converting
+        // warpgroup (FP8: all 128 threads arrive)
         for (int s = 0; s < NSK; ++s) {
-            mbar_init(bar(B::KFULL + s), 1);
+            mbar_init(bar(B::KFULL + s), FP8 ? kSoftThreads : 1);
             mbar_init(bar(B::KEMPTY + s), 1);
         }
         for (int s = 0; s < NSV; ++s) {
-            mbar_init(bar(B::VFULL + s), 1);
+            mbar_init(bar(B::VFULL + s), FP8 ? kSoftThreads : 1);
             mbar_init(bar(B::VEMPTY + s), 1);
+        }
+        if constexpr (FP8) {
+            for (int s = 0; s < K::NS8; ++s) {
+                mbar_init(bar(B::K8FULL + s), 1);
+                mbar_init(bar(B::K8EMPTY + s), kSoftThreads);
+                mbar_init(bar(B::V8FULL + s), 1);
+                mbar_init(bar(B::V8EMPTY + s), kSoftThreads);
+            }
+            for (int s = 0; s < K::NSC; ++s) mbar_init(bar(B::SCALE + s), 1);
         }
         for (int i = 0; i < NSB; ++i) {
             mbar_init(bar(B::SFULL + i), 1);
@@ -414,7 +437,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     griddep_wait();
     Cursor cur0, curt;
     int u0, u1, W, P;
-    int4* seqtab = p.num_seqs <= kSeqTab ? reinterpret_cast<int4*>(smem + K::OFF_SEQ) : nullptr;
+    int4* seqtab = p.num_seqs <= K::SEQTAB ? reinterpret_cast<int4*>(smem + K::OFF_SEQ) : nullptr;
     const bool has_work =
         plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt, seqtab);
     if (!has_work) {             // uniform across the CTA
@@ -625,6 +648,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         constexpr bool kQAhead = QV <= 4;         // wide pieces load their q at the piece start
         int t = 0, j = 0, kcount = 0, vcount = 0;
         bool ok = true;
+        int pend_t = -1;                  // (FP8) tile whose scales are loaded but not yet written
+        float pend_k = 0.f, pend_v = 0.f;
         // q rows of piece `pi` in column order, 16 bytes per lane and step
         auto load_q = [&](const PieceIter& pi, uint4 (&v)[QV]) {
             const int R = G * pi.cur.Q, ncol = HG * R;
@@ -678,17 +703,40 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     if (lane < np) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
                     blk = 0;
                 }
-                const size_t off = ((size_t)blk * Hkv + it.hg * HG + (qu - qpg * HG)) * K::PAGE;
-                if (t >= NSK) {
-                    bool w = lane == 0 ? wait_bar(bar(B::KEMPTY + ks), ((t / NSK) - 1) & 1, ctl) : true;
-                    ok = __shfl_sync(0xffffffffu, w, 0);
-                    if (!ok) break;
+                const size_t unit = (size_t)blk * Hkv + it.hg * HG + (qu - qpg * HG);
+                const size_t off = unit * (FP8 ? K::PAGE8 : K::PAGE);
+                float ksc = 0.f, vsc = 0.f;
+                if constexpr (FP8) {
+                    // this tile's (block, kv-head) scales; written to the scale ring one tile later
+                    if (lane < np) {
+                        ksc = __ldg(p.k_scales + unit);
+                        vsc = __ldg(p.v_scales + unit);
+                    }
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bar(B::KFULL + ks), np * K::PAGE);
-                __syncwarp();
-                if (lane < np)
-                    bulk_g2s_hint(sb + K::OFF_K + ks * K::TILE + lane * K::PAGE, p.k_cache + off, K::PAGE,
-                                  bar(B::KFULL + ks), pol);
+                if constexpr (FP8) {
+                    const int s8 = t % K::NS8;
+                    if (t >= K::NS8) {
+                        bool w = lane == 0 ? wait_bar(bar(B::K8EMPTY + s8), ((t / K::NS8) - 1) & 1, ctl) : true;
+                        ok = __shfl_sync(0xffffffffu, w, 0);
+                        if (!ok) break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B::K8FULL + s8), np * K::PAGE8);
+                    __syncwarp();
+                    if (lane < np)
+                        bulk_g2s_hint(sb + K::OFF_K8 + s8 * K::TILE8 + lane * K::PAGE8, p.k_cache + off, K::PAGE8,
+                                      bar(B::K8FULL + s8), pol);
+                } else {
+                    if (t >= NSK) {
+                        bool w = lane == 0 ? wait_bar(bar(B::KEMPTY + ks), ((t / NSK) - 1) & 1, ctl) : true;
+                        ok = __shfl_sync(0xffffffffu, w, 0);
+                        if (!ok) break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B::KFULL + ks), np * K::PAGE);
+                    __syncwarp();
+                    if (lane < np)
+                        bulk_g2s_hint(sb + K::OFF_K + ks * K::TILE + lane * K::PAGE, p.k_cache + off, K::PAGE,
+                                      bar(B::KFULL + ks), pol);
+                }
                 ++kcount;
                 if (t0 == 0) {
                     // the piece's q rows -> Q buffer (K-major core matrices)
@@ -705,16 +753,43 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B::QFULL + qb));
                 }
-                if (t >= NSV) {
-                    bool w = lane == 0 ? wait_bar(bar(B::VEMPTY + vs), ((t / NSV) - 1) & 1, ctl) : true;
-                    ok = __shfl_sync(0xffffffffu, w, 0);
-                    if (!ok) break;
+                if constexpr (FP8) {
+                    const int s8 = t % K::NS8;
+                    if (t >= K::NS8) {
+                        bool w = lane == 0 ? wait_bar(bar(B::V8EMPTY + s8), ((t / K::NS8) - 1) & 1, ctl) : true;
+                        ok = __shfl_sync(0xffffffffu, w, 0);
+                        if (!ok) break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B::V8FULL + s8), np * K::PAGE8);
+                    __syncwarp();
+                    if (lane < np)
+                        bulk_g2s_hint(sb + K::OFF_V8 + s8 * K::TILE8 + lane * K::PAGE8, p.v_cache + off, K::PAGE8,
+                                      bar(B::V8FULL + s8), pol);
+                    // the previous tile's scales (their loads have landed by now)
+                    if (pend_t >= 0) {
+                        float* sc = reinterpret_cast<float*>(smem + K::OFF_SC) + (pend_t % K::NSC) * 16;
+                        if (lane < 8) {
+                            sc[lane] = pend_k;
+                            sc[8 + lane] = pend_v;
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B::SCALE + pend_t % K::NSC));
+                    }
+                    pend_t = t;
+                    pend_k = ksc;
+                    pend_v = vsc;
+                } else {
+                    if (t >= NSV) {
+                        bool w = lane == 0 ? wait_bar(bar(B::VEMPTY + vs), ((t / NSV) - 1) & 1, ctl) : true;
+                        ok = __shfl_sync(0xffffffffu, w, 0);
+                        if (!ok) break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + vs), np * K::PAGE);
+                    __syncwarp();
+                    if (lane < np)
+                        bulk_g2s_hint(sb + K::OFF_V + vs * (K::TILE + K::VSLACK) + lane * K::PAGE, p.v_cache + off,
+                                      K::PAGE, bar(B::VFULL + vs), pol);
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + vs), np * K::PAGE);
-                __syncwarp();
-                if (lane < np)
-                    bulk_g2s_hint(sb + K::OFF_V + vs * (K::TILE + K::VSLACK) + lane * K::PAGE, p.v_cache + off,
-                                  K::PAGE, bar(B::VFULL + vs), pol);
                 ++vcount;
                 __syncwarp();
                 if (t0 == 0) {
@@ -741,12 +816,24 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             }
             win = winn;
         }
+        if constexpr (FP8) {
+            if (ok && pend_t >= 0) {          // the last tile's scales
+                float* sc = reinterpret_cast<float*>(smem + K::OFF_SC) + (pend_t % K::NSC) * 16;
+                if (lane < 8) {
+                    sc[lane] = pend_k;
+                    sc[8 + lane] = pend_v;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B::SCALE + pend_t % K::NSC));
+            }
+        }
         // drain: every copy issued has landed before the CTA exits
         if (lane == 0) {
-            for (int tt = max(0, kcount - NSK); tt < kcount; ++tt)
-                wait_bar(bar(B::KFULL + tt % NSK), (tt / NSK) & 1, drain);
-            for (int tt = max(0, vcount - NSV); tt < vcount; ++tt)
-                wait_bar(bar(B::VFULL + tt % NSV), (tt / NSV) & 1, drain);
+            constexpr int RK = FP8 ? K::NS8 : NSK, RV = FP8 ? K::NS8 : NSV;
+            for (int tt = max(0, kcount - RK); tt < kcount; ++tt)
+                wait_bar(bar((FP8 ? B::K8FULL : B::KFULL) + tt % RK), (tt / RK) & 1, drain);
+            for (int tt = max(0, vcount - RV); tt < vcount; ++tt)
+                wait_bar(bar((FP8 ? B::V8FULL : B::VFULL) + tt % RV), (tt / RV) & 1, drain);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -973,7 +1060,15 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 // visible columns: [lo, hi) of this head's R rows (causal within the window)
                 const int lo = hh * R + max(0, pos - lim0) * G, hi = hh * R + R;
 
-                const bool okw = wait_bar(bar(B::SFULL + t % NSB), (t / NSB) & 1, ctl);
+                bool okw = wait_bar(bar(B::SFULL + t % NSB), (t / NSB) & 1, ctl);
+                // (FP8) this token's page scales: S^T holds q . code, and V enters as codes
+                float kscale = 1.f, vscale = 1.f;
+                if constexpr (FP8) {
+                    okw = wait_bar(bar(B::SCALE + t % K::NSC), (t / K::NSC) & 1, ctl) && okw;
+                    const float* sc = reinterpret_cast<const float*>(smem + K::OFF_SC) + (t % K::NSC) * 16;
+                    kscale = sc[k];
+                    vscale = sc[8 + k];
+                }
                 tc_fence_after();
                 float s[RMAX];
 #pragma unroll
@@ -987,7 +1082,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
 #pragma unroll
                 for (int n = 0; n < RMAX; ++n) {
                     const bool vis = tok_ok && n >= lo && n < hi;
-                    s[n] = vis ? s[n] * p.scale_log2 : -INFINITY;
+                    s[n] = vis ? s[n] * (FP8 ? p.scale_log2 * kscale : p.scale_log2) : -INFINITY;
                     need |= s[n] > m_ref[n] + kRescaleSlack;
                 }
                 if (bar_red_or(kBarSoft, kSoftThreads, need || !okw)) {
@@ -1059,12 +1154,13 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         float a, b;
                         if constexpr (SPLIT) {
                             const int n = cc * 4 + h;          // physical columns 2n (high) and 2n+1 (low)
-                            const float hi = __bfloat162float(__float2bfloat16_rn(pr[n]));
+                            const float pv = FP8 ? pr[n] * vscale : pr[n];
+                            const float hi = __bfloat162float(__float2bfloat16_rn(pv));
                             a = hi;
-                            b = pr[n] - hi;
+                            b = pv - hi;
                         } else {
-                            a = pr[cc * 8 + 2 * h];
-                            b = pr[cc * 8 + 2 * h + 1];
+                            a = FP8 ? pr[cc * 8 + 2 * h] * vscale : pr[cc * 8 + 2 * h];
+                            b = FP8 ? pr[cc * 8 + 2 * h + 1] * vscale : pr[cc * 8 + 2 * h + 1];
                         }
                         w4[h] = pack_bf16x2(a, b);
                     }
@@ -1152,11 +1248,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         // ------------------------------------------------------------ epilogue warpgroup
         if constexpr (EWG) {
             const int tt = tid - kEpiWarp0 * 32;
-            for (int pc = 0;; ++pc) {
-                const int par = pc & 1;
-                const bool okr = wait_bar(bar(B::PREADY + par), (pc >> 1) & 1, ctl);
-                if (bar_red_or(kBarEpi, kSoftThreads, !okr)) break;
-                const int* q = pdesc + par * 8;
+            auto take_piece = [&](int pc) -> PieceDesc {
+                const int* q = pdesc + (pc & 1) * 8;
                 PieceDesc d;
                 d.b = q[0];
                 d.hg = q[1];
@@ -1166,8 +1259,115 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 d.S1 = q[5];
                 d.last = q[6] != 0;
                 d.pc = pc;
-                piece_epilogue(d, tt, kBarEpi);
-                if (d.last) break;
+                return d;
+            };
+            if constexpr (!FP8) {
+                for (int pc = 0;; ++pc) {
+                    const bool okr = wait_bar(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1, ctl);
+                    if (bar_red_or(kBarEpi, kSoftThreads, !okr)) break;
+                    const PieceDesc d = take_piece(pc);
+                    piece_epilogue(d, tt, kBarEpi);
+                    if (d.last) break;
+                }
+            } else {
+                // FP8: also turn every staged tile of e4m3 pages into bf16 MMA operands
+                // (codes exact in bf16; the page scales are applied in the softmax).  Each
+                // round takes whatever is ready: a finished piece's epilogue, the next K
+                // tile, the next V tile (agreed across the warpgroup by bar.red).
+                int T = 0;
+                {
+                    PieceIter w = it;
+                    while (w.valid()) {
+                        T += (w.npg + kTP - 1) / kTP;
+                        w.advance(p);
+                    }
+                }
+                // one tile of 8 staged pages (layout [2][D/16][8][16] bytes) -> 8 bf16 pages
+                // ([2][D/8][8][8] elements): each 16-byte chunk of 16 codes becomes two
+                constexpr int CH8 = K::PAGE8 / 16, NC16 = D / 16;
+                auto convert = [&](const uint8_t* src, uint8_t* dst) {
+#pragma unroll 2
+                    for (int i = tt; i < kTP * CH8; i += kSoftThreads) {
+                        const int pg = i / CH8, cp = i % CH8;
+                        const int r = cp & 7, c = (cp >> 3) % NC16, oh = cp / (8 * NC16);
+                        const uint4 v = *reinterpret_cast<const uint4*>(src + pg * K::PAGE8 + cp * 16);
+                        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 a = e4m3x2_to_float2(wv[j]), b = e4m3x2_to_float2(wv[j] >> 16);
+                            o[2 * j] = pack_bf16x2(a.x, a.y);
+                            o[2 * j + 1] = pack_bf16x2(b.x, b.y);
+                        }
+                        uint8_t* d0 = dst + pg * K::PAGE + ((oh * (D / 8) + 2 * c) * 8 + r) * 16;
+                        *reinterpret_cast<uint4*>(d0) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(d0 + 128) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                    fence_proxy_async_smem();             // the MMA reads them through the async proxy
+                };
+                int kt = 0, vt = 0, pc = 0;
+                bool epi_done = false;
+                uint64_t t_prog = globaltimer_ns();
+                while (kt < T || vt < T || !epi_done) {
+                    bool did = false;
+                    // (a piece is taken once its O^T is complete too: its last V tile may
+                    // still be waiting here for conversion)
+                    if (!epi_done &&
+                        bar_red_or(kBarEpi, kSoftThreads,
+                                   mbar_test_wait(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1) &&
+                                       mbar_test_wait(bar(B::ODONE + (pc & 1)), (pc >> 1) & 1))) {
+                        wait_bar(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1, ctl);   // (acquire in every thread)
+                        const PieceDesc d = take_piece(pc);
+                        piece_epilogue(d, tt, kBarEpi);
+                        epi_done = d.last;
+                        ++pc;
+                        did = true;
+                    }
+                    if (kt < T) {
+                        const int s8 = kt % K::NS8, ks = kt % NSK;
+                        const bool rdy = mbar_test_wait(bar(B::K8FULL + s8), (kt / K::NS8) & 1) &&
+                                         (kt < NSK || mbar_test_wait(bar(B::KEMPTY + ks), ((kt / NSK) - 1) & 1));
+                        if (bar_red_or(kBarEpi, kSoftThreads, rdy)) {
+                            wait_bar(bar(B::K8FULL + s8), (kt / K::NS8) & 1, ctl);
+                            if (kt >= NSK) wait_bar(bar(B::KEMPTY + ks), ((kt / NSK) - 1) & 1, ctl);
+                            convert(smem + K::OFF_K8 + s8 * K::TILE8, smem + K::OFF_K + ks * K::TILE);
+                            mbar_arrive(bar(B::KFULL + ks));
+                            mbar_arrive(bar(B::K8EMPTY + s8));
+                            ++kt;
+                            did = true;
+                        }
+                    }
+                    if (vt < kt) {
+                        const int s8 = vt % K::NS8, vs = vt % NSV;
+                        const bool rdy = mbar_test_wait(bar(B::V8FULL + s8), (vt / K::NS8) & 1) &&
+                                         (vt < NSV || mbar_test_wait(bar(B::VEMPTY + vs), ((vt / NSV) - 1) & 1));
+                        if (bar_red_or(kBarEpi, kSoftThreads, rdy)) {
+                            wait_bar(bar(B::V8FULL + s8), (vt / K::NS8) & 1, ctl);
+                            if (vt >= NSV) wait_bar(bar(B::VEMPTY + vs), ((vt / NSV) - 1) & 1, ctl);
+                            convert(smem + K::OFF_V8 + s8 * K::TILE8, smem + K::OFF_V + vs * (K::TILE + K::VSLACK));
+                            mbar_arrive(bar(B::VFULL + vs));
+                            mbar_arrive(bar(B::V8EMPTY + s8));
+                            ++vt;
+                            did = true;
+                        }
+                    }
+                    if (did) {
+                        t_prog = globaltimer_ns();
+                    } else {
+                        // nothing ready: give up on an abort, or after kWaitLimitNs without progress
+                        bool stuck = false;
+                        if (tt == 0) {
+                            stuck = *abort_flag != 0;
+                            if (!stuck && globaltimer_ns() - t_prog > kWaitLimitNs) {
+                                raise_error(p.err, PKV_DEVERR_TIMEOUT);
+                                *abort_flag = 1;
+                                stuck = true;
+                            }
+                        }
+                        if (bar_red_or(kBarEpi, kSoftThreads, stuck)) break;
+                        __nanosleep(32);
+                    }
+                }
             }
         }
     }
@@ -1181,10 +1381,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     }
 }
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG>
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8 = false>
 static cudaError_t launch_t(const AttnParams& p, int ncta, cudaStream_t st) {
-    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG>;
-    auto kern = attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV, EWG>;
+    using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>;
+    auto kern = attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(ncta), dim3(threads_of<EWG>()), K::SMEM, st, p);
@@ -1209,11 +1409,12 @@ int tc_heads_per_segment(int num_kv_heads, int rows) {
 // bf16 cache, head_dim 64/128, R = G * max_q_len <= 32.  Narrow segments (N =
 // 16) run the epilogue in its own warpgroup; wide ones (N = 32), whose softmax
 // needs more registers than a 384-thread block leaves, in the softmax warps.
-cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, int ncta, cudaStream_t st) {
+cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st) {
     const bool split = tc_col_limit(p.rows) == 8;
     if (head_dim == 128)
-        return split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
-                     : tc::launch_t<128, 32, false, 2, 3, false>(p, ncta, st);
+        return fp8     ? tc::launch_t<128, 16, true, 2, 2, true, true>(p, ncta, st)
+               : split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
+                       : tc::launch_t<128, 32, false, 2, 3, false>(p, ncta, st);
     return split ? tc::launch_t<64, 16, true, 4, 6, true>(p, ncta, st)
                  : tc::launch_t<64, 32, false, 4, 6, false>(p, ncta, st);
 }

@@ -67,6 +67,9 @@ SWEEP = [
     (128, 16, 1, [40, 250], [2, 2], "bf16"),          # G = 16, R = 32
     (128, 8, 2, [0, 20, 0, 45], [0, 1, 0, 2], "bf16"),  # empty sequences
     (64, 16, 2, [20, 50], [0, 3], "bf16"),             # a sequence with no query rows
+    (128, 16, 2, [1, 15, 16, 17, 130, 700], [1] * 6, "fp8"),   # FP8, G = 8: one kv-head per segment
+    (128, 8, 2, [5, 40, 77, 300], [2, 1, 2, 1], "fp8"),        # FP8, R = 8 with a causal window
+    (128, 8, 4, [0, 33, 0, 517], [0, 1, 0, 1], "fp8"),         # FP8, empty sequences, four kv-heads per segment
 ]
 
 
@@ -105,7 +108,7 @@ def test_deterministic_run_to_run():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("n", [2, 3, 4])
+@pytest.mark.parametrize("n", [2, 3, 4, 5])
 def test_repeated_calls_reuse_the_workspace(n):
     """Calls that share a workspace give the same bits, and each call leaves
     every merge ticket at zero (the workspace is ready for the next call)."""
