@@ -84,18 +84,19 @@ struct Cfg {
     static constexpr int RMAX = SPLIT ? NPAD / 2 : NPAD;  // logical columns
     static constexpr int PAGE = kBlock * D * 2;         // a page as bf16 MMA operand
     static constexpr int PAGE8 = kBlock * D;            // an FP8 cache page
-    static constexpr int TILE8 = kTP * PAGE8;
-    static constexpr int NS8 = 2;                       // FP8 staging ring depth (K and V each)
     static constexpr int NSC = 16;                      // scale ring: tiles the producer may lead by, bounded
     static constexpr int NCH = D / 8;                   // 16-byte chunks per token row
     static constexpr int TILE = kTP * PAGE;
     static constexpr int VSLACK = D == 64 ? 1024 : 0;   // M=128 PV on D=64 reads 1 KiB past a page
-    static constexpr int OFF_K = 0;                     // + st * TILE
-    static constexpr int OFF_V = NSK * TILE;            // + st * (TILE + VSLACK)
-    static constexpr int OFF_K8 = OFF_V + NSV * (TILE + VSLACK);   // FP8 staging: + st * TILE8
-    static constexpr int OFF_V8 = OFF_K8 + (FP8 ? NS8 * TILE8 : 0);
-    static constexpr int OFF_SC = OFF_V8 + (FP8 ? NS8 * TILE8 : 0);  // float [NSC][k scales 8, v scales 8]
-    static constexpr int OFF_Q = OFF_SC + (FP8 ? NSC * 16 * 4 : 0);
+    // FP8: K tiles stay e4m3 (the S MMA takes them as they are); a V slot's
+    // e4m3 pages land in its upper half and are widened to bf16 in place
+    static constexpr int KSLOT = FP8 ? kTP * PAGE8 : TILE;
+    static constexpr int OFF_K = 0;                     // + st * KSLOT
+    static constexpr int OFF_V = NSK * KSLOT;           // + st * (TILE + VSLACK)
+    static constexpr int OFF_LAND = TILE - kTP * PAGE8;
+    // FP8 scale ring: float [NSC][32]: k scales [8], v scales [8], column factors [8]
+    static constexpr int OFF_SC = OFF_V + NSV * (TILE + VSLACK);
+    static constexpr int OFF_Q = OFF_SC + (FP8 ? NSC * 32 * 4 : 0);
     static constexpr int QBUF = NPAD * D * 2;
     static constexpr int OFF_P = OFF_Q + 2 * QBUF;
     static constexpr int PBUF = NPAD * kTileTok * 2;
@@ -104,7 +105,7 @@ struct Cfg {
     static constexpr int OFF_EM = OFF_LRED + 2 * 4 * RMAX * 4;         // float [2][RMAX]
     static constexpr int OFF_PD = OFF_EM + 2 * RMAX * 4;               // int [2][8]: piece descriptors
     static constexpr int OFF_BAR = OFF_PD + 2 * 8 * 4;
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 16 + (FP8 ? 4 * NS8 + NSC : 0);   // the barriers of Bars
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 16 + (FP8 ? NSV + NSC : 0);   // the barriers of Bars
     static constexpr int OFF_MISC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // tmem addr, abort, zero, gather state
     static constexpr int OFF_MQ = OFF_MISC + 16;         // merge tasks: int [4][8]
     static constexpr int OFF_SEQ = OFF_MQ + 128;         // int4 [SEQTAB]: per-sequence (L, Q, Ub, qoff)
@@ -133,9 +134,9 @@ struct Bars {
                          ODONE = MQFULL + 4,      // [2]: last P.V of a piece of that parity done
                          PREADY = ODONE + 2,      // [2]: a piece of that parity handed to the epilogue
                          OFREE = PREADY + 2,      // [2]: its epilogue has read O^T, lred and emref
-                         // FP8 only: staging rings (bulk copy -> conversion) and the scale ring
-                         K8FULL = OFREE + 2, K8EMPTY = K8FULL + 2, V8FULL = K8EMPTY + 2, V8EMPTY = V8FULL + 2,
-                         SCALE = V8EMPTY + 2, END = FP8 ? SCALE + 16 : OFREE + 2;
+                         // FP8 only: a V slot's e4m3 pages have landed (before their widening), scale ring
+                         VLAND = OFREE + 2, SCALE = VLAND + NSV,
+                         END = FP8 ? SCALE + 16 : OFREE + 2;
 };
 
 // A finished piece, as its epilogue needs it.
@@ -221,6 +222,24 @@ struct Butterfly {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Four e4m3 codes (bytes of w, lowest first) -> four bf16 (lo: codes 0, 1;
+// hi: codes 2, 3), exact, on the integer and bf16x2 pipes instead of the
+// conversion unit.  A code's 4 exponent and 3 mantissa bits are placed in the
+// low exponent bits and the top mantissa bits of a bf16, which then reads as
+// the code's value times 2^-120 (its bf16 subnormals are the e4m3 subnormals);
+// a bf16x2 multiply by 2^120 restores the value.  The NaN codes (0x7f, 0xff)
+// come out as +-480: the cache encoder never writes them.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t hb = ((w >> 4) & 0x07070707u) | (w & 0x80808080u);   // per byte: sign, 3 high exponent bits
+    const uint32_t lb = (w << 4) & 0xF0F0F0F0u;                          // per byte: low exponent bit, mantissa
+    const uint32_t a = __byte_perm(lb, hb, 0x5140), b = __byte_perm(lb, hb, 0x7362);
+    const __nv_bfloat162 k2 = __halves2bfloat162(__ushort_as_bfloat16(0x7B80), __ushort_as_bfloat16(0x7B80));
+    const __nv_bfloat162 ra = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), k2);
+    const __nv_bfloat162 rb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), k2);
+    lo = *reinterpret_cast<const uint32_t*>(&ra);
+    hi = *reinterpret_cast<const uint32_t*>(&rb);
 }
 
 // Pieces of a CTA's unit range [u0, u1), in processing order: the piece
@@ -385,12 +404,15 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     // and only feed S^T columns the softmax ignores.
     for (int i = tid; i < 2 * K::QBUF / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + K::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
+    if constexpr (FP8)   // (scale slots of units past a tile's pages are read, never used)
+        for (int i = tid; i < K::NSC * 128 / 16; i += kThreads)
+            reinterpret_cast<uint4*>(smem + K::OFF_SC)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
         // K/V operand slots are filled by bulk copies (bf16) or by the converting
         // warpgroup (FP8: all 128 threads arrive)
         for (int s = 0; s < NSK; ++s) {
-            mbar_init(bar(B::KFULL + s), FP8 ? kSoftThreads : 1);
+            mbar_init(bar(B::KFULL + s), 1);
             mbar_init(bar(B::KEMPTY + s), 1);
         }
         for (int s = 0; s < NSV; ++s) {
@@ -398,13 +420,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             mbar_init(bar(B::VEMPTY + s), 1);
         }
         if constexpr (FP8) {
-            for (int s = 0; s < K::NS8; ++s) {
-                mbar_init(bar(B::K8FULL + s), 1);
-                mbar_init(bar(B::K8EMPTY + s), kSoftThreads);
-                mbar_init(bar(B::V8FULL + s), 1);
-                mbar_init(bar(B::V8EMPTY + s), kSoftThreads);
-            }
-            for (int s = 0; s < K::NSC; ++s) mbar_init(bar(B::SCALE + s), 1);
+            for (int s = 0; s < NSV; ++s) mbar_init(bar(B::VLAND + s), 1);
+            for (int s = 0; s < K::NSC; ++s) mbar_init(bar(B::SCALE + s), 33);   // 32 cp.async lanes + 1
         }
         for (int i = 0; i < NSB; ++i) {
             mbar_init(bar(B::SFULL + i), 1);
@@ -456,6 +473,45 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     PieceIter it;
     it.tab = seqtab;
     it.init(p, cur0, curt, u0, u1);
+
+    // ---------------------------------------------------------------- FP8 widening
+    // Tiles of the CTA (every role walks the same pieces).
+    auto tile_count = [&]() {
+        int n = 0;
+        PieceIter w = it;
+        while (w.valid()) {
+            n += (w.npg + kTP - 1) / kTP;
+            w.advance(p);
+        }
+        return n;
+    };
+    // Widen one operand slot in place: the bulk copy left the tile's e4m3 pages
+    // (layout [2][D/16][8][16] bytes) in the slot's upper half.  Each thread of
+    // a 128-thread warpgroup (named barrier bid) reads its 16-byte chunk of
+    // every page, the warpgroup syncs, then writes the bf16 operand
+    // ([2][D/8][8][8] elements per page) over the whole slot.  Codes are exact
+    // in bf16; the page scales are applied in the softmax.
+    auto widen = [&](uint8_t* slot, int tt, int bid) {
+        static_assert(!FP8 || K::PAGE8 / 16 == kSoftThreads, "one chunk of every page per thread");
+        constexpr int NC16 = D / 16;
+        uint4 v[kTP];
+#pragma unroll
+        for (int k = 0; k < kTP; ++k)
+            v[k] = *reinterpret_cast<const uint4*>(slot + K::OFF_LAND + k * K::PAGE8 + tt * 16);
+        named_bar_sync(bid, kSoftThreads);
+        const int r = tt & 7, c = (tt >> 3) % NC16, oh = tt / (8 * NC16);
+        uint8_t* d0 = slot + ((oh * (D / 8) + 2 * c) * 8 + r) * 16;
+#pragma unroll
+        for (int k = 0; k < kTP; ++k) {
+            const uint32_t wv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) e4m3x4_to_bf16x4(wv[j], o[2 * j], o[2 * j + 1]);
+            *reinterpret_cast<uint4*>(d0 + k * K::PAGE) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(d0 + k * K::PAGE + 128) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();             // the MMA reads the slot through the async proxy
+    };
 
     // ---------------------------------------------------------------- piece epilogue
     // Run by one warpgroup (thread tt = TMEM lane = d row, named barrier bid)
@@ -648,8 +704,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         constexpr bool kQAhead = QV <= 4;         // wide pieces load their q at the piece start
         int t = 0, j = 0, kcount = 0, vcount = 0;
         bool ok = true;
-        int pend_t = -1;                  // (FP8) tile whose scales are loaded but not yet written
-        float pend_k = 0.f, pend_v = 0.f;
+        float cur_c = 1.f;                // (FP8) lane n < 8: column n's factor 2^-E_n in the current piece
         // q rows of piece `pi` in column order, 16 bytes per lane and step
         auto load_q = [&](const PieceIter& pi, uint4 (&v)[QV]) {
             const int R = G * pi.cur.Q, ncol = HG * R;
@@ -696,99 +751,135 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 const int qu = qfirst + (lane & 7);
                 const int qpg = div_small(qu, HG);                    // page of the lane's unit
                 const int pg = qpg - ws;                          // in [0, 40) for the tile's units
-                const int e1 = __shfl_sync(0xffffffffu, win, pg & 31);
-                const int e2 = __shfl_sync(0xffffffffu, win2, pg & 31);
-                int blk = pg < 32 ? e1 : e2;
+                int blk = __shfl_sync(0xffffffffu, win, pg & 31);
+                // the next window's entries only once the tile reaches them (its load may be in flight)
+                if (div_small(qfirst + np - 1, HG) - ws >= 32) {
+                    const int e2 = __shfl_sync(0xffffffffu, win2, pg & 31);
+                    if (pg >= 32) blk = e2;
+                }
                 if (blk < 0 || blk >= p.num_blocks) {
                     if (lane < np) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
                     blk = 0;
                 }
-                const size_t unit = (size_t)blk * Hkv + it.hg * HG + (qu - qpg * HG);
+                const int qh = qu - qpg * HG;                         // the unit's head within the group
+                const size_t unit = (size_t)blk * Hkv + it.hg * HG + qh;
                 const size_t off = unit * (FP8 ? K::PAGE8 : K::PAGE);
-                float ksc = 0.f, vsc = 0.f;
-                if constexpr (FP8) {
-                    // this tile's (block, kv-head) scales; written to the scale ring one tile later
-                    if (lane < np) {
-                        ksc = __ldg(p.k_scales + unit);
-                        vsc = __ldg(p.v_scales + unit);
-                    }
+                // one bulk copy per page: the group's heads of a block are adjacent in the
+                // cache and the tile, so the lane of a page's first unit copies its run
+                const bool lead = lane < np && (lane == 0 || qh == 0);
+                const int run = min(HG - qh, np - lane);
+                if (t >= NSK) {
+                    bool w = lane == 0 ? wait_bar(bar(B::KEMPTY + ks), ((t / NSK) - 1) & 1, ctl) : true;
+                    ok = __shfl_sync(0xffffffffu, w, 0);
+                    if (!ok) break;
                 }
-                if constexpr (FP8) {
-                    const int s8 = t % K::NS8;
-                    if (t >= K::NS8) {
-                        bool w = lane == 0 ? wait_bar(bar(B::K8EMPTY + s8), ((t / K::NS8) - 1) & 1, ctl) : true;
-                        ok = __shfl_sync(0xffffffffu, w, 0);
-                        if (!ok) break;
-                    }
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B::K8FULL + s8), np * K::PAGE8);
+                {
+                    constexpr int KP = FP8 ? K::PAGE8 : K::PAGE;      // (FP8: the S MMA reads e4m3 pages)
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B::KFULL + ks), np * KP);
                     __syncwarp();
-                    if (lane < np)
-                        bulk_g2s_hint(sb + K::OFF_K8 + s8 * K::TILE8 + lane * K::PAGE8, p.k_cache + off, K::PAGE8,
-                                      bar(B::K8FULL + s8), pol);
-                } else {
-                    if (t >= NSK) {
-                        bool w = lane == 0 ? wait_bar(bar(B::KEMPTY + ks), ((t / NSK) - 1) & 1, ctl) : true;
-                        ok = __shfl_sync(0xffffffffu, w, 0);
-                        if (!ok) break;
-                    }
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B::KFULL + ks), np * K::PAGE);
-                    __syncwarp();
-                    if (lane < np)
-                        bulk_g2s_hint(sb + K::OFF_K + ks * K::TILE + lane * K::PAGE, p.k_cache + off, K::PAGE,
+                    if (lead)
+                        bulk_g2s_hint(sb + K::OFF_K + ks * K::KSLOT + lane * KP, p.k_cache + off, run * KP,
                                       bar(B::KFULL + ks), pol);
                 }
                 ++kcount;
                 if (t0 == 0) {
                     // the piece's q rows -> Q buffer (K-major core matrices)
                     uint8_t* qdst = smem + K::OFF_Q + qb * K::QBUF;
+                    if constexpr (FP8) {
+                        // e4m3 operand of the S MMA: row n times 2^E_n (its largest magnitude
+                        // brought to [128, 256)), split exactly into hi + lo e4m3 terms (a
+                        // bf16 value's 8 significant bits), stored as rows n and 8 + n; the
+                        // softmax adds the two columns and multiplies by 2^-E_n
+                        static_assert(!FP8 || (K::NCH == 16 && QV == 4 && RMAX == 8), "FP8 q staging: D = 128, R <= 8");
+                        int ek[QV];
 #pragma unroll
-                    for (int k = 0; k < QV; ++k) {
-                        const int idx = lane + 32 * k;
-                        if (idx < ncol * K::NCH) {
-                            const int n = idx / K::NCH, c = idx % K::NCH;
-                            *reinterpret_cast<uint4*>(qdst + (n >> 3) * (K::NCH * 128) + c * 128 + (n & 7) * 16) = qv[k];
+                        for (int k = 0; k < QV; ++k) {
+                            const uint32_t wq[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+                            float mx = 0.f;
+#pragma unroll
+                            for (int h = 0; h < 4; ++h)
+                                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(wq[h] << 16)),
+                                                     fabsf(__uint_as_float(wq[h] & 0xFFFF0000u))));
+#pragma unroll
+                            for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                            const int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+                            const int E = mx > 0.f ? min(126, max(-126, 7 - e)) : 0;
+                            ek[k] = E;
+                            const float sf = __uint_as_float((uint32_t)(E + 127) << 23);
+                            const int idx = lane + 32 * k;
+                            if (idx < ncol * K::NCH) {
+                                uint32_t hi[2] = {0u, 0u}, lo[2] = {0u, 0u};
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const float x0 = __uint_as_float(wq[h] << 16) * sf;
+                                    const float x1 = __uint_as_float(wq[h] & 0xFFFF0000u) * sf;
+                                    const uint32_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+                                    const float2 b1 = e4m3x2_to_float2(c1);
+                                    const uint32_t c2 =
+                                        __nv_cvt_float2_to_fp8x2(make_float2(x0 - b1.x, x1 - b1.y), __NV_SATFINITE, __NV_E4M3);
+                                    hi[h >> 1] |= (c1 & 0xFFFFu) << ((h & 1) * 16);
+                                    lo[h >> 1] |= (c2 & 0xFFFFu) << ((h & 1) * 16);
+                                }
+                                const int n = idx / K::NCH, c = idx % K::NCH;    // row, 8-element chunk
+                                uint8_t* rh = qdst + (c >> 1) * 128 + n * 16 + (c & 1) * 8;
+                                *reinterpret_cast<uint2*>(rh) = make_uint2(hi[0], hi[1]);
+                                *reinterpret_cast<uint2*>(rh + (D / 16) * 128) = make_uint2(lo[0], lo[1]);
+                            }
+                        }
+                        // column n's factor -> lane n: row n sits in lanes (n & 1) * 16 + [0, 16), step n >> 1
+                        int en = 0;
+#pragma unroll
+                        for (int k = 0; k < QV; ++k) {
+                            const int v = __shfl_sync(0xffffffffu, ek[k], (lane & 1) * 16);
+                            if ((lane >> 1) == k) en = v;
+                        }
+                        cur_c = __uint_as_float((uint32_t)(127 - en) << 23);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < QV; ++k) {
+                            const int idx = lane + 32 * k;
+                            if (idx < ncol * K::NCH) {
+                                const int n = idx / K::NCH, c = idx % K::NCH;
+                                *reinterpret_cast<uint4*>(qdst + (n >> 3) * (K::NCH * 128) + c * 128 + (n & 7) * 16) =
+                                    qv[k];
+                            }
                         }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B::QFULL + qb));
                 }
+                if (t >= NSV) {
+                    bool w = lane == 0 ? wait_bar(bar(B::VEMPTY + vs), ((t / NSV) - 1) & 1, ctl) : true;
+                    ok = __shfl_sync(0xffffffffu, w, 0);
+                    if (!ok) break;
+                }
                 if constexpr (FP8) {
-                    const int s8 = t % K::NS8;
-                    if (t >= K::NS8) {
-                        bool w = lane == 0 ? wait_bar(bar(B::V8EMPTY + s8), ((t / K::NS8) - 1) & 1, ctl) : true;
-                        ok = __shfl_sync(0xffffffffu, w, 0);
-                        if (!ok) break;
-                    }
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B::V8FULL + s8), np * K::PAGE8);
+                    // e4m3 pages -> the slot's upper half; the epilogue warpgroup widens them
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B::VLAND + vs), np * K::PAGE8);
                     __syncwarp();
-                    if (lane < np)
-                        bulk_g2s_hint(sb + K::OFF_V8 + s8 * K::TILE8 + lane * K::PAGE8, p.v_cache + off, K::PAGE8,
-                                      bar(B::V8FULL + s8), pol);
-                    // the previous tile's scales (their loads have landed by now)
-                    if (pend_t >= 0) {
-                        float* sc = reinterpret_cast<float*>(smem + K::OFF_SC) + (pend_t % K::NSC) * 16;
-                        if (lane < 8) {
-                            sc[lane] = pend_k;
-                            sc[8 + lane] = pend_v;
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar(B::SCALE + pend_t % K::NSC));
+                    if (lead)
+                        bulk_g2s_hint(sb + K::OFF_V + vs * (K::TILE + K::VSLACK) + K::OFF_LAND + lane * K::PAGE8,
+                                      p.v_cache + off, run * K::PAGE8, bar(B::VLAND + vs), pol);
+                    // this tile's (block, kv-head) scales straight into the scale ring (cp.async,
+                    // each lane's arrival once its copies land) and the columns' factors (lane 0's
+                    // arrival after the warp's stores): 33 arrivals complete the slot
+                    const int sl = t % K::NSC;
+                    const uint32_t scs = sb + K::OFF_SC + sl * 128;
+                    if (lane < np) {
+                        cp_async_4(scs + lane * 4, p.k_scales + unit);
+                        cp_async_4(scs + 32 + lane * 4, p.v_scales + unit);
                     }
-                    pend_t = t;
-                    pend_k = ksc;
-                    pend_v = vsc;
+                    cp_async_mbar_arrive_noinc(bar(B::SCALE + sl));
+                    if (lane < 8) reinterpret_cast<float*>(smem + K::OFF_SC)[sl * 32 + 16 + lane] = cur_c;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B::SCALE + sl));
                 } else {
-                    if (t >= NSV) {
-                        bool w = lane == 0 ? wait_bar(bar(B::VEMPTY + vs), ((t / NSV) - 1) & 1, ctl) : true;
-                        ok = __shfl_sync(0xffffffffu, w, 0);
-                        if (!ok) break;
-                    }
                     if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + vs), np * K::PAGE);
                     __syncwarp();
-                    if (lane < np)
+                    if (lead)
                         bulk_g2s_hint(sb + K::OFF_V + vs * (K::TILE + K::VSLACK) + lane * K::PAGE, p.v_cache + off,
-                                      K::PAGE, bar(B::VFULL + vs), pol);
+                                      run * K::PAGE, bar(B::VFULL + vs), pol);
                 }
                 ++vcount;
                 __syncwarp();
@@ -816,24 +907,13 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             }
             win = winn;
         }
-        if constexpr (FP8) {
-            if (ok && pend_t >= 0) {          // the last tile's scales
-                float* sc = reinterpret_cast<float*>(smem + K::OFF_SC) + (pend_t % K::NSC) * 16;
-                if (lane < 8) {
-                    sc[lane] = pend_k;
-                    sc[8 + lane] = pend_v;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B::SCALE + pend_t % K::NSC));
-            }
-        }
         // drain: every copy issued has landed before the CTA exits
+        if constexpr (FP8) cp_async_wait_all();
         if (lane == 0) {
-            constexpr int RK = FP8 ? K::NS8 : NSK, RV = FP8 ? K::NS8 : NSV;
-            for (int tt = max(0, kcount - RK); tt < kcount; ++tt)
-                wait_bar(bar((FP8 ? B::K8FULL : B::KFULL) + tt % RK), (tt / RK) & 1, drain);
-            for (int tt = max(0, vcount - RV); tt < vcount; ++tt)
-                wait_bar(bar((FP8 ? B::V8FULL : B::VFULL) + tt % RV), (tt / RV) & 1, drain);
+            for (int tt = max(0, kcount - NSK); tt < kcount; ++tt)
+                wait_bar(bar(B::KFULL + tt % NSK), (tt / NSK) & 1, drain);
+            for (int tt = max(0, vcount - NSV); tt < vcount; ++tt)
+                wait_bar(bar((FP8 ? B::VLAND : B::VFULL) + tt % NSV), (tt / NSV) & 1, drain);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -841,7 +921,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         // S^T of tile t once its K and its piece's q have landed and the
         // softmax has released S^T buffer t % NSB (P of tile t - NSB written).
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(128, NPAD, false, false);
+            constexpr uint32_t idS = FP8 ? idesc_e4m3_f32(128, NPAD) : idesc_bf16_f32(128, NPAD, false, false);
+            constexpr int SBO = FP8 ? (D / 16) * 128 : K::NCH * 128;   // between 8-row core-matrix groups
             int t = 0, j = 0;
             bool ok = true;
             while (ok && it.valid()) {
@@ -853,12 +934,16 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     if (t >= NSB && !(ok = wait_bar(bar(B::PFULL + t % NSB), ((t / NSB) - 1) & 1, ctl))) break;
                     if (!(ok = wait_bar(bar(B::KFULL + ks), (t / NSK) & 1, ctl))) break;
                     tc_fence_after();
-                    const uint32_t kbase = sb + K::OFF_K + ks * K::TILE;
+                    const uint32_t kbase = sb + K::OFF_K + ks * K::KSLOT;
+                    // K steps of 32 bytes (16 bf16 or 32 e4m3 elements), two core matrices each
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint64_t a = smem_desc(kbase + k * 256, 128, K::NCH * 128);
-                        const uint64_t b = smem_desc(qbase + k * 256, 128, K::NCH * 128);
-                        mma_bf16(tmem + K::COL_S + (t % NSB) * NPAD, a, b, idS, k > 0);
+                    for (int k = 0; k < (FP8 ? D / 32 : D / 16); ++k) {
+                        const uint64_t a = smem_desc(kbase + k * 256, 128, SBO);
+                        const uint64_t b = smem_desc(qbase + k * 256, 128, SBO);
+                        if constexpr (FP8)
+                            mma_f8(tmem + K::COL_S + (t % NSB) * NPAD, a, b, idS, k > 0);
+                        else
+                            mma_bf16(tmem + K::COL_S + (t % NSB) * NPAD, a, b, idS, k > 0);
                     }
                     mma_commit(bar(B::SFULL + t % NSB));
                     mma_commit(bar(B::KEMPTY + ks));
@@ -1061,13 +1146,16 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 const int lo = hh * R + max(0, pos - lim0) * G, hi = hh * R + R;
 
                 bool okw = wait_bar(bar(B::SFULL + t % NSB), (t / NSB) & 1, ctl);
-                // (FP8) this token's page scales: S^T holds q . code, and V enters as codes
-                float kscale = 1.f, vscale = 1.f;
+                // (FP8) this token's page scales and the columns' factors: S^T holds
+                // (2^E_n q_n) . code split over columns n and 8 + n, and V enters as codes
+                float kscale = 1.f, vscale = 1.f, cf[FP8 ? RMAX : 1];
                 if constexpr (FP8) {
                     okw = wait_bar(bar(B::SCALE + t % K::NSC), (t / K::NSC) & 1, ctl) && okw;
-                    const float* sc = reinterpret_cast<const float*>(smem + K::OFF_SC) + (t % K::NSC) * 16;
+                    const float* sc = reinterpret_cast<const float*>(smem + K::OFF_SC) + (t % K::NSC) * 32;
                     kscale = sc[k];
                     vscale = sc[8 + k];
+#pragma unroll
+                    for (int n = 0; n < RMAX; ++n) cf[n] = sc[16 + n] * (p.scale_log2 * kscale);
                 }
                 tc_fence_after();
                 float s[RMAX];
@@ -1076,13 +1164,21 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     float tmp[16];
                     tmem_ld16(tmem + lane_base + K::COL_S + (t % NSB) * NPAD + c, tmp);
 #pragma unroll
-                    for (int x = 0; x < 16 && c + x < RMAX; ++x) s[c + x] = tmp[x];
+                    for (int x = 0; x < 16 && c + x < RMAX; ++x) {
+                        if constexpr (FP8)
+                            s[c + x] = tmp[x] + tmp[x + RMAX];   // hi + lo q terms (RMAX = 8)
+                        else
+                            s[c + x] = tmp[x];
+                    }
                 }
                 bool need = false;
 #pragma unroll
                 for (int n = 0; n < RMAX; ++n) {
                     const bool vis = tok_ok && n >= lo && n < hi;
-                    s[n] = vis ? s[n] * (FP8 ? p.scale_log2 * kscale : p.scale_log2) : -INFINITY;
+                    if constexpr (FP8)
+                        s[n] = vis ? s[n] * cf[n] : -INFINITY;
+                    else
+                        s[n] = vis ? s[n] * p.scale_log2 : -INFINITY;
                     need |= s[n] > m_ref[n] + kRescaleSlack;
                 }
                 if (bar_red_or(kBarSoft, kSoftThreads, need || !okw)) {
@@ -1270,51 +1366,20 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     if (d.last) break;
                 }
             } else {
-                // FP8: also turn every staged tile of e4m3 pages into bf16 MMA operands
-                // (codes exact in bf16; the page scales are applied in the softmax).  Each
-                // round takes whatever is ready: a finished piece's epilogue, the next K
-                // tile, the next V tile (agreed across the warpgroup by bar.red).
-                int T = 0;
-                {
-                    PieceIter w = it;
-                    while (w.valid()) {
-                        T += (w.npg + kTP - 1) / kTP;
-                        w.advance(p);
-                    }
-                }
-                // one tile of 8 staged pages (layout [2][D/16][8][16] bytes) -> 8 bf16 pages
-                // ([2][D/8][8][8] elements): each 16-byte chunk of 16 codes becomes two
-                constexpr int CH8 = K::PAGE8 / 16, NC16 = D / 16;
-                auto convert = [&](const uint8_t* src, uint8_t* dst) {
-#pragma unroll 2
-                    for (int i = tt; i < kTP * CH8; i += kSoftThreads) {
-                        const int pg = i / CH8, cp = i % CH8;
-                        const int r = cp & 7, c = (cp >> 3) % NC16, oh = cp / (8 * NC16);
-                        const uint4 v = *reinterpret_cast<const uint4*>(src + pg * K::PAGE8 + cp * 16);
-                        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-                        uint32_t o[8];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float2 a = e4m3x2_to_float2(wv[j]), b = e4m3x2_to_float2(wv[j] >> 16);
-                            o[2 * j] = pack_bf16x2(a.x, a.y);
-                            o[2 * j + 1] = pack_bf16x2(b.x, b.y);
-                        }
-                        uint8_t* d0 = dst + pg * K::PAGE + ((oh * (D / 8) + 2 * c) * 8 + r) * 16;
-                        *reinterpret_cast<uint4*>(d0) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4*>(d0 + 128) = make_uint4(o[4], o[5], o[6], o[7]);
-                    }
-                    fence_proxy_async_smem();             // the MMA reads them through the async proxy
-                };
-                int kt = 0, vt = 0, pc = 0;
+                // FP8: this warpgroup also widens every V tile in place (the softmax
+                // warpgroup widens K).  Each round takes whatever is ready: a finished
+                // piece's epilogue, the next V tile (agreed across the warpgroup by bar.red).
+                const int T = tile_count();
+                int vt = 0, pc = 0;
                 bool epi_done = false;
                 uint64_t t_prog = globaltimer_ns();
-                while (kt < T || vt < T || !epi_done) {
+                while (vt < T || !epi_done) {
                     bool did = false;
-                    // (a piece is taken once its O^T is complete too: its last V tile may
-                    // still be waiting here for conversion)
+                    // (one thread probes, the warpgroup agrees; a piece is taken once its O^T
+                    // is complete too: its last V tile may still be waiting here for widening)
                     if (!epi_done &&
                         bar_red_or(kBarEpi, kSoftThreads,
-                                   mbar_test_wait(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1) &&
+                                   tt == 0 && mbar_test_wait(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1) &&
                                        mbar_test_wait(bar(B::ODONE + (pc & 1)), (pc >> 1) & 1))) {
                         wait_bar(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1, ctl);   // (acquire in every thread)
                         const PieceDesc d = take_piece(pc);
@@ -1323,30 +1388,12 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         ++pc;
                         did = true;
                     }
-                    if (kt < T) {
-                        const int s8 = kt % K::NS8, ks = kt % NSK;
-                        const bool rdy = mbar_test_wait(bar(B::K8FULL + s8), (kt / K::NS8) & 1) &&
-                                         (kt < NSK || mbar_test_wait(bar(B::KEMPTY + ks), ((kt / NSK) - 1) & 1));
-                        if (bar_red_or(kBarEpi, kSoftThreads, rdy)) {
-                            wait_bar(bar(B::K8FULL + s8), (kt / K::NS8) & 1, ctl);
-                            if (kt >= NSK) wait_bar(bar(B::KEMPTY + ks), ((kt / NSK) - 1) & 1, ctl);
-                            convert(smem + K::OFF_K8 + s8 * K::TILE8, smem + K::OFF_K + ks * K::TILE);
-                            mbar_arrive(bar(B::KFULL + ks));
-                            mbar_arrive(bar(B::K8EMPTY + s8));
-                            ++kt;
-                            did = true;
-                        }
-                    }
-                    if (vt < kt) {
-                        const int s8 = vt % K::NS8, vs = vt % NSV;
-                        const bool rdy = mbar_test_wait(bar(B::V8FULL + s8), (vt / K::NS8) & 1) &&
-                                         (vt < NSV || mbar_test_wait(bar(B::VEMPTY + vs), ((vt / NSV) - 1) & 1));
-                        if (bar_red_or(kBarEpi, kSoftThreads, rdy)) {
-                            wait_bar(bar(B::V8FULL + s8), (vt / K::NS8) & 1, ctl);
-                            if (vt >= NSV) wait_bar(bar(B::VEMPTY + vs), ((vt / NSV) - 1) & 1, ctl);
-                            convert(smem + K::OFF_V8 + s8 * K::TILE8, smem + K::OFF_V + vs * (K::TILE + K::VSLACK));
+                    if (vt < T) {
+                        const int vs = vt % NSV;
+                        if (bar_red_or(kBarEpi, kSoftThreads, tt == 0 && mbar_test_wait(bar(B::VLAND + vs), (vt / NSV) & 1))) {
+                            wait_bar(bar(B::VLAND + vs), (vt / NSV) & 1, ctl);   // (acquire in every thread)
+                            widen(smem + K::OFF_V + vs * (K::TILE + K::VSLACK), tt, kBarEpi);
                             mbar_arrive(bar(B::VFULL + vs));
-                            mbar_arrive(bar(B::V8EMPTY + s8));
                             ++vt;
                             did = true;
                         }
@@ -1365,7 +1412,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                             }
                         }
                         if (bar_red_or(kBarEpi, kSoftThreads, stuck)) break;
-                        __nanosleep(32);
+                        __nanosleep(96);
                     }
                 }
             }
@@ -1412,7 +1459,7 @@ int tc_heads_per_segment(int num_kv_heads, int rows) {
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st) {
     const bool split = tc_col_limit(p.rows) == 8;
     if (head_dim == 128)
-        return fp8     ? tc::launch_t<128, 16, true, 2, 2, true, true>(p, ncta, st)
+        return fp8     ? tc::launch_t<128, 16, true, 4, 4, true, true>(p, ncta, st)
                : split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
                        : tc::launch_t<128, 32, false, 2, 3, false>(p, ncta, st);
     return split ? tc::launch_t<64, 16, true, 4, 6, true>(p, ncta, st)

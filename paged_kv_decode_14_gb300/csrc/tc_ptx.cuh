@@ -81,6 +81,18 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// 4-byte global -> shared copy (LDGSTS); completion is tracked by
+// cp_async_mbar_arrive_noinc on an mbarrier.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+// Arrive on `bar` once every cp.async this thread issued so far has landed;
+// the arrival counts against the barrier's expected count (.noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
 // ------------------------------------------------------------------ fences
 
 // Load with acquire semantics at GPU scope: accesses after it are ordered
@@ -185,6 +197,25 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16)
            | ((uint32_t)(N >> 3) << 17)           // N / 8
            | ((uint32_t)(M >> 4) << 24);          // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with e4m3 A/B (both K-major) and
+// fp32 accumulation (A/B format code 0 = e4m3).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                              // D format: f32
+           | ((uint32_t)(N >> 3) << 17)           // N / 8
+           | ((uint32_t)(M >> 4) << 24);          // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem] with 8-bit A/B (K = 32 per instruction),
+// issued by one thread.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem], issued by one thread.

@@ -87,6 +87,24 @@ def test_sweep(case):
         assert_attention_close(got, ref, f"sweep {case} ncta {ncta}")
 
 
+def test_fp8_subnormal_codes():
+    """Page scales 2^14 times absmax / 448 leave most stored codes e4m3
+    subnormals (exponent field 0): the attention must decode them exactly."""
+    w = wl.make_workload("fp8sub", context_lens=[300, 77, 1000, 16], q_lens=[1] * 4, num_q_heads=32,
+                         num_kv_heads=8, head_dim=128, kv_dtype="fp8", seed=91)
+    w.k_scales = (w.k_scales * np.float32(16384.0)).astype(np.float32)
+    w.v_scales = (w.v_scales * np.float32(16384.0)).astype(np.float32)
+    kc, vc = oracle.build_cache(w)
+    ref, _ = oracle.attend(w, kc, vc)
+    dw, got = run_gpu(w)
+    gk, gv = dw.cache_bytes()
+    assert caches_equal(gk, kc, True) and caches_equal(gv, vc, True)
+    written = np.concatenate([c[(c & 0x7F) != 0x7F] for c in (gk, gv)])   # (unwritten slots hold NaN)
+    sub = (((written >> 3) & 15) == 0) & ((written & 7) != 0)
+    assert np.mean(sub) > 0.3, "the case should hold mostly subnormal codes"
+    assert_attention_close(got, ref, "fp8 subnormal codes")
+
+
 @pytest.mark.parametrize("ncta", [1, 2, 3, 7, 152, 608, 5000])
 def test_grid_sizes_agree(ncta):
     """Different grids cut the KV differently; the LSE merge makes them agree."""
