@@ -381,10 +381,11 @@ def run_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3", "data": "synthetic",
             "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
                        "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": 16,
-                       "context_lens": "uniform [256, 2048]", "pool_blocks": w.num_blocks,
+                       "kv_dtype": w.kv_dtype, "context_lens": lens_summary(w), "q_len_max": int(w.q_lens.max()),
+                       "pool_blocks": w.num_blocks,
                        "kv_bytes_per_step": kvb, "l2": l2_note,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_hbm_peak": 100.0 * value / peak,
@@ -414,6 +415,11 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def lens_summary(w):
+    L = np.asarray(w.context_lens)
+    return f"min {int(L.min())}, median {int(np.median(L))}, max {int(L.max())}, mean {float(L.mean()):.0f}"
 
 
 def main():
