@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay CUDA graphs of the steps instead of launching them through the binding")
     ap.add_argument("--l2", choices=["flush", "rotate"], default="rotate",
                     help="keep timed inputs out of L2: flush it before every step (a write of 2x its size), "
                          "or rotate over enough copies of the workload that the data read by a step is not in L2")
@@ -291,6 +293,32 @@ def run_ours(args):
                f"inputs rotated over {n_copies} copies ({n_copies * w.kv_bytes() / 1e6:.0f} MB of KV > "
                f"{l2 / 1e6:.0f} MB L2), no flush")
 
+    # --graph: each copy's step (append + attention, with the attention's
+    # programmatic launch edge) and, for the per-kernel split, its append and
+    # its attention alone are captured as CUDA graphs and replayed.  By default
+    # steps launch through the binding: the host stays ahead of the GPU at
+    # these step times, and the eager launches measured no slower.
+    use_graph = args.graph
+    g_step, g_app, g_att = [], [], []
+    if use_graph:
+        for d in dws:
+            d.step()                      # first launches (attributes, lazy loads) outside capture
+        torch.cuda.synchronize(dev)
+        cs = torch.cuda.Stream(dev)
+        for d in dws:
+            for lst, fn in ((g_step, d.step), (g_app, d.append_step), (g_att, d.attend)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cs):
+                    fn()
+                lst.append(g)
+        torch.cuda.synchronize(dev)
+
+    def run_step(i):
+        if use_graph:
+            g_step[i % n_copies].replay()
+        else:
+            dws[i % n_copies].step()
+
     def pick(i):
         if flush is not None:
             flush.zero_()
@@ -303,7 +331,8 @@ def run_ours(args):
 
     # ---------------- device-resident timing
     for i in range(args.warmup):
-        pick(i).step()
+        pick(i)
+        run_step(i)
     barrier()
     # a step is timed as one interval (no event between append and attention,
     # so the attention's programmatic launch can overlap the append's tail)
@@ -316,14 +345,15 @@ def run_ours(args):
         t_end = time.perf_counter() + args.soak_seconds
         while time.perf_counter() < t_end:
             for i in range(20):
-                pick(i).step()
+                pick(i)
+                run_step(i)
             torch.cuda.synchronize(dev)
     barrier()
     wall0 = time.perf_counter()
     for i, (e0, e2) in enumerate(ev):
-        d = pick(i)                       # L2 flush (outside the timed events) or the next copy
+        pick(i)                           # L2 flush (outside the timed events), if flushing
         e0.record(stream)
-        d.step()
+        run_step(i)
         e2.record(stream)
     barrier()
     wall = time.perf_counter() - wall0
@@ -336,9 +366,15 @@ def run_ours(args):
     for i, (e0, e1, e2) in enumerate(kev):
         d = pick(i)
         e0.record(stream)
-        d.append_step()
+        if use_graph:
+            g_app[i % n_copies].replay()
+        else:
+            d.append_step()
         e1.record(stream)
-        d.attend()
+        if use_graph:
+            g_att[i % n_copies].replay()
+        else:
+            d.attend()
         e2.record(stream)
     barrier()
     attn_ms = [b.elapsed_time(c) for _, b, c in kev]
@@ -387,6 +423,7 @@ def run_ours(args):
                        "kv_dtype": w.kv_dtype, "context_lens": lens_summary(w), "q_len_max": int(w.q_lens.max()),
                        "pool_blocks": w.num_blocks,
                        "kv_bytes_per_step": kvb, "l2": l2_note,
+                       "launch": "CUDA graph replay per step" if use_graph else "eager, through the binding",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_hbm_peak": 100.0 * value / peak,
             "seq_steps_per_s": world * w.num_seqs * args.steps / (tot / 1e3),

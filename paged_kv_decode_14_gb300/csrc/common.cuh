@@ -147,12 +147,15 @@ __device__ __forceinline__ int div_small(int n, int d) {
     return (int)__fdividef((float)n + 0.5f, (float)d);
 }
 
-// CTAs that take part: every one gets at least kMinUnitsPerCta units (two
-// 128-token tiles), so a small batch is not spread so thin that a segment
-// crosses dozens of CTAs and its merge walks dozens of partials.
+// CTAs that take part: enough that every one gets at least kMinUnitsPerCta
+// units (two 128-token tiles), so a small batch is not spread so thin that a
+// segment crosses dozens of CTAs and its merge walks dozens of partials; but
+// at least one per non-empty segment (S of them), so short segments are not
+// packed several to a CTA, whose piece epilogues would then run one after
+// another.
 constexpr int kMinUnitsPerCta = 16;
-__device__ __forceinline__ int participating_ctas(int ncta, int W) {
-    return W <= 0 ? 0 : max(1, min(ncta, W / kMinUnitsPerCta));
+__device__ __forceinline__ int participating_ctas(int ncta, int W, int S) {
+    return W <= 0 ? 0 : max(1, min(ncta, max(W / kMinUnitsPerCta, S)));
 }
 
 // CTA owning unit u under the partition above (P = participating CTAs <= W,
@@ -212,7 +215,7 @@ __device__ __forceinline__ int block_scan_incl(int v, int* scratch /* NT/32 + 1 
     return v + add;
 }
 
-// Computes W (total units) and the number P = participating_ctas(grid, W) of CTAs that take
+// Computes W (total units) and the number P = participating_ctas(grid, W, S) of CTAs that take
 // part, and positions a cursor at the sequence holding unit u0 of this CTA
 // (and, if tail != nullptr, one at the sequence holding its last unit u1 - 1).
 // All NT threads must call it.  CTA 0 reports invalid lengths.  Returns false
@@ -270,7 +273,8 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         const int2 inc = block_scan2_incl<NT>(make_int2(u, q), s2);
         if (seqtab && b < p.num_seqs) seqtab[b] = make_int4(L, Q, inc.x - u, inc.y - q);
         const int W = s2[NT / 32].x;
-        const int P = participating_ctas(ncta, W);
+        const int S = __syncthreads_count(u > 0) * (p.num_kv_heads / p.hg);   // non-empty segments
+        const int P = participating_ctas(ncta, W, S);
         *W_out = W;
         *P_out = P;
         if (cta >= P) return false;
@@ -298,7 +302,7 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
     const bool one_chunk = p.num_seqs <= NT;      // lengths stay in registers between the passes
     int Lc = 0, Qc = 0;
     // pass 1: total units
-    int total = 0;
+    int total = 0, nonempty = 0;
     for (int base = 0; base < p.num_seqs; base += NT) {
         int b = base + tid;
         int u = 0;
@@ -311,12 +315,11 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         }
         block_scan_incl<NT>(u, scratch);
         total += scratch[NT / 32];
-        __syncthreads();
+        nonempty += __syncthreads_count(u > 0);
     }
     const int W = total;
-    // With few units, only the first P CTAs take part (at least
-    // kMinUnitsPerCta units each, or all W units in one CTA).
-    const int P = participating_ctas(ncta, W);
+    // With few units, only the first P CTAs take part
+    const int P = participating_ctas(ncta, W, nonempty * (p.num_kv_heads / p.hg));
     *W_out = W;
     *P_out = P;
     if (cta >= P) return false;
