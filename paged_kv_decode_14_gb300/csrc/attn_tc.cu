@@ -758,28 +758,35 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     if (pg >= 32) blk = e2;
                 }
                 if (blk < 0 || blk >= p.num_blocks) {
-                    if (lane < np) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+                    if (lane < np) raise_error(p.err, PKV_DEVERR_BLOCK_ID);      // (lane < 8 here)
                     blk = 0;
                 }
                 const int qh = qu - qpg * HG;                         // the unit's head within the group
                 const size_t unit = (size_t)blk * Hkv + it.hg * HG + qh;
                 const size_t off = unit * (FP8 ? K::PAGE8 : K::PAGE);
-                // one bulk copy per page: the group's heads of a block are adjacent in the
-                // cache and the tile, so the lane of a page's first unit copies its run
-                const bool lead = lane < np && (lane == 0 || qh == 0);
-                const int run = min(HG - qh, np - lane);
-                if (t >= NSK) {
-                    bool w = lane == 0 ? wait_bar(bar(B::KEMPTY + ks), ((t / NSK) - 1) & 1, ctl) : true;
-                    ok = __shfl_sync(0xffffffffu, w, 0);
+                // K and V of the tile in one pass: lanes 0-7 copy K, lanes 8-15 V (unit slot
+                // lane & 7).  One bulk copy per page: the group's heads of a block are adjacent
+                // in the cache and the tile, so the lane of a page's first unit copies its run.
+                const int sl = lane & 7, kv = lane >> 3;
+                const bool lead = kv < 2 && sl < np && (sl == 0 || qh == 0);
+                const int run = min(HG - qh, np - sl);
+                {
+                    bool w = true;
+                    if (lane == 0 && t >= NSK) w = wait_bar(bar(B::KEMPTY + ks), ((t / NSK) - 1) & 1, ctl);
+                    if (lane == 8 && t >= NSV) w = wait_bar(bar(B::VEMPTY + vs), ((t / NSV) - 1) & 1, ctl);
+                    ok = __all_sync(0xffffffffu, w);
                     if (!ok) break;
                 }
                 {
-                    constexpr int KP = FP8 ? K::PAGE8 : K::PAGE;      // (FP8: the S MMA reads e4m3 pages)
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B::KFULL + ks), np * KP);
+                    // (FP8: the S MMA reads the e4m3 K pages; V lands in its slot's upper half)
+                    constexpr int KP = FP8 ? K::PAGE8 : K::PAGE;
+                    const uint32_t vslot = sb + K::OFF_V + vs * (K::TILE + K::VSLACK) + (FP8 ? K::OFF_LAND : 0);
+                    const uint32_t fb = kv == 0 ? bar(B::KFULL + ks) : bar((FP8 ? B::VLAND : B::VFULL) + vs);
+                    if (sl == 0 && kv < 2) mbar_arrive_expect_tx(fb, np * KP);
                     __syncwarp();
                     if (lead)
-                        bulk_g2s_hint(sb + K::OFF_K + ks * K::KSLOT + lane * KP, p.k_cache + off, run * KP,
-                                      bar(B::KFULL + ks), pol);
+                        bulk_g2s_hint(kv == 0 ? sb + K::OFF_K + ks * K::KSLOT + sl * KP : vslot + sl * KP,
+                                      (kv == 0 ? p.k_cache : p.v_cache) + off, run * KP, fb, pol);
                 }
                 ++kcount;
                 if (t0 == 0) {
@@ -849,37 +856,20 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B::QFULL + qb));
                 }
-                if (t >= NSV) {
-                    bool w = lane == 0 ? wait_bar(bar(B::VEMPTY + vs), ((t / NSV) - 1) & 1, ctl) : true;
-                    ok = __shfl_sync(0xffffffffu, w, 0);
-                    if (!ok) break;
-                }
                 if constexpr (FP8) {
-                    // e4m3 pages -> the slot's upper half; the epilogue warpgroup widens them
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B::VLAND + vs), np * K::PAGE8);
-                    __syncwarp();
-                    if (lead)
-                        bulk_g2s_hint(sb + K::OFF_V + vs * (K::TILE + K::VSLACK) + K::OFF_LAND + lane * K::PAGE8,
-                                      p.v_cache + off, run * K::PAGE8, bar(B::VLAND + vs), pol);
                     // this tile's (block, kv-head) scales straight into the scale ring (cp.async,
                     // each lane's arrival once its copies land) and the columns' factors (lane 0's
                     // arrival after the warp's stores): 33 arrivals complete the slot
-                    const int sl = t % K::NSC;
-                    const uint32_t scs = sb + K::OFF_SC + sl * 128;
+                    const int ssl = t % K::NSC;
+                    const uint32_t scs = sb + K::OFF_SC + ssl * 128;
                     if (lane < np) {
                         cp_async_4(scs + lane * 4, p.k_scales + unit);
                         cp_async_4(scs + 32 + lane * 4, p.v_scales + unit);
                     }
-                    cp_async_mbar_arrive_noinc(bar(B::SCALE + sl));
-                    if (lane < 8) reinterpret_cast<float*>(smem + K::OFF_SC)[sl * 32 + 16 + lane] = cur_c;
+                    cp_async_mbar_arrive_noinc(bar(B::SCALE + ssl));
+                    if (lane < 8) reinterpret_cast<float*>(smem + K::OFF_SC)[ssl * 32 + 16 + lane] = cur_c;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B::SCALE + sl));
-                } else {
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B::VFULL + vs), np * K::PAGE);
-                    __syncwarp();
-                    if (lead)
-                        bulk_g2s_hint(sb + K::OFF_V + vs * (K::TILE + K::VSLACK) + lane * K::PAGE, p.v_cache + off,
-                                      run * K::PAGE, bar(B::VFULL + vs), pol);
+                    if (lane == 0) mbar_arrive(bar(B::SCALE + ssl));
                 }
                 ++vcount;
                 __syncwarp();
