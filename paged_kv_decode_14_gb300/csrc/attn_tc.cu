@@ -113,7 +113,11 @@ struct Cfg {
     static constexpr int SEQTAB = FP8 ? kSeqTab / 2 : kSeqTab;   // sequences the table holds
     static constexpr int OFF_GATHER = OFF_SEQ + SEQTAB * 16;
     static constexpr int GATHER = SPLIT ? RMAX * (D + 2) * 4 : 0;
-    static constexpr int SMEM_USED = OFF_GATHER + GATHER + 128;  // + base alignment slack
+    // the weighted CTA boundaries (int [TABMAX + 1]), for wide segments
+    static constexpr int TABMAX = 160;
+    static constexpr int OFF_BND = (OFF_GATHER + GATHER + 15) / 16 * 16;
+    static constexpr bool PTAB = !EWG && OFF_BND + (TABMAX + 1) * 4 + 128 <= kMaxSmem - 1024;
+    static constexpr int SMEM_USED = (PTAB ? OFF_BND + (TABMAX + 1) * 4 : OFF_GATHER + GATHER) + 128;  // + slack
     // One CTA per SM either way: take the whole per-block budget, so every
     // operand read the descriptors can form stays inside the allocation.
     static constexpr int SMEM = kMaxSmem - 1024;
@@ -321,10 +325,10 @@ __device__ __forceinline__ float merge_acc(float x, float wo, float y, float wn)
 // Merge the partials of segment [S0, S1) (NCOL columns) into out; one warp,
 // one round trip of loads per piece, pieces in CTA order.
 template <int D>
-__device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q, int S0, int S1, int W, int P,
+__device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q, int S0, int S1, const Part& part,
                                    int lane) {
     constexpr int DPL = D / 32;
-    const int c_first = owner_cta(S0, W, P), c_last = owner_cta(S1 - 1, W, P);
+    const int c_first = part.owner(S0), c_last = part.owner(S1 - 1);
     const int R = p.group * Q, ncol = p.hg * R;
     for (int n0 = 0; n0 < ncol; n0 += 8) {
         float M[8], den[8], num[8][DPL];
@@ -336,7 +340,7 @@ __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q,
             for (int x = 0; x < DPL; ++x) num[k][x] = 0.f;
         }
         for (int c = c_first; c <= c_last; ++c) {
-            const float* s = slot_ptr(p, c, S0, cta_start(c, W, P));
+            const float* s = slot_ptr(p, c, S0, part.start(c));
             float m[8], l[8], a[8][DPL];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -455,8 +459,15 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     Cursor cur0, curt;
     int u0, u1, W, P;
     int4* seqtab = p.num_seqs <= K::SEQTAB ? reinterpret_cast<int4*>(smem + K::OFF_SEQ) : nullptr;
-    const bool has_work =
-        plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt, seqtab);
+    // Wide segments (epilogue in the softmax warps, about three tiles of time
+    // per piece) cut the CTA ranges by weight, charging every segment piece 24
+    // units; narrow ones (epilogue off the softmax path) keep the equal split,
+    // which needs no table at the start.
+    int* bndtab = (K::PTAB && !EWG) ? reinterpret_cast<int*>(smem + K::OFF_BND) : nullptr;
+    bool tab_used = false;
+    const bool has_work = plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt,
+                                                seqtab, bndtab, K::TABMAX, 24, &tab_used);
+    const Part part{W, P, tab_used ? bndtab : nullptr};
     if (!has_work) {             // uniform across the CTA
         tc_fence_before();
         __syncthreads();
@@ -602,8 +613,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 return;
             }
         }
-        const int c_first = d.last ? owner_cta(d.S0, W, P) : 0;
-        const int c_last = d.last ? owner_cta(d.S1 - 1, W, P) : 0;
+        const int c_first = d.last ? part.owner(d.S0) : 0;
+        const int c_last = d.last ? part.owner(d.S1 - 1) : 0;
         // the last piece merges here when every other piece is published already
         if (tt == 0 && tk == c_last - c_first) fence_acquire_gpu();
         bool direct = d.last && bar_red_or(bid, kSoftThreads, tk == c_last - c_first);
@@ -664,7 +675,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                             a[x] = acc[n0 + x];
                         }
                     } else {
-                        const float* sl = slot_ptr(p, c, d.S0, cta_start(c, W, P));
+                        const float* sl = slot_ptr(p, c, d.S0, part.start(c));
 #pragma unroll
                         for (int x = 0; x < 8; ++x) {
                             const int n = n0 + x;
@@ -1012,7 +1023,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             const int seg_b = task[0], hg = task[1], S0 = task[4], S1 = task[5];
             int last = 0;
             if (lane == 0) {
-                const int need = owner_cta(S1 - 1, W, P) - owner_cta(S0, W, P) + 1;
+                const int need = part.owner(S1 - 1) - part.owner(S0) + 1;
                 int* ticket = p.tickets + seg_b * p.num_kv_heads + hg;
                 if (ld_acquire_gpu(ticket) == need - 1) {
                     // every other piece is published (and visible): merge without publishing this one
@@ -1025,11 +1036,11 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             __syncwarp();
-            if (last) merge_segment_warp<D>(p, hg, task[2], task[3], S0, S1, W, P, lane);
+            if (last) merge_segment_warp<D>(p, hg, task[2], task[3], S0, S1, part, lane);
         }
         if constexpr (SPLIT) {
             if (ok && w.S0 < u0 && w.S1 <= u1) {
-                const int c_first = owner_cta(w.S0, W, P);          // this CTA is the segment's last
+                const int c_first = part.owner(w.S0);          // this CTA is the segment's last
                 int* ticket = p.tickets + w.cur.b * Hkv + w.hg;
                 const int ncol = HG * G * w.cur.Q;
                 const uint64_t t0 = globaltimer_ns();
@@ -1059,7 +1070,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                                 for (int x = 0; x < DPL; ++x) num[k][x] = 0.f;
                             }
                             for (int c = c_first; c < cta; ++c) {
-                                const float* sl = slot_ptr(p, c, w.S0, cta_start(c, W, P));
+                                const float* sl = slot_ptr(p, c, w.S0, part.start(c));
 #pragma unroll
                                 for (int k = 0; k < RMAX; ++k) {
                                     const bool ld = k < ncol;

@@ -168,6 +168,28 @@ __device__ __forceinline__ int cta_start(int c, int W, int ncta) {
     return floor_div_small((long long)c * W, ncta);
 }
 
+// The partition a launch uses: CTA c streams units [start(c), start(c + 1)).
+// Either the equal split of the W units over P CTAs (the formulas above), or
+// a table of P + 1 boundaries in shared memory (bnd != nullptr) cut so that
+// every CTA gets an equal share of units plus a fixed cost per segment piece.
+// Every CTA holds the same table, so owner() and start() agree across CTAs.
+struct Part {
+    int W, P;
+    const int* bnd;
+    __device__ __forceinline__ int start(int c) const { return bnd ? bnd[c] : cta_start(c, W, P); }
+    // the CTA whose range holds unit u (u < W): the last c with start(c) <= u
+    __device__ __forceinline__ int owner(int u) const {
+        if (!bnd) return owner_cta(u, W, P);
+        int lo = 0, hi = P - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (bnd[mid] <= u) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    }
+};
+
 // Units (pages x kv-heads) of sequence b; sequences with no query rows or
 // invalid lengths (Q > L, Q above the launch's max_q_len, more pages than a
 // block-table row holds) contribute none.
@@ -252,10 +274,16 @@ __device__ __forceinline__ int2 block_scan2_incl(int2 v, int2* scratch /* NT/32 
 // With seqtab != nullptr and num_seqs <= NT, seqtab[b] receives (L, Q, units
 // before b, first q row of b) for every sequence, so that cursors can move on
 // without reading global memory (cursor_next with the table).
+// With bnd != nullptr, num_seqs <= NT and P <= bnd_max, the CTA ranges are cut
+// by weight instead (every non-empty segment weighs its units plus ce) into
+// the table bnd[0..P] (*bnd_used is set to whether it was).  A range may come
+// out empty only at a segment boundary, and such a CTA has no work.
 template <int NT>
 __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch, Cursor* cur,
                             int* u0_out, int* u1_out, int* W_out, int* P_out, Cursor* tail = nullptr,
-                            int4* seqtab = nullptr) {
+                            int4* seqtab = nullptr, int* bnd = nullptr, int bnd_max = 0, int ce = 0,
+                            bool* bnd_used = nullptr) {
+    if (bnd_used) *bnd_used = false;
     const int tid = threadIdx.x;
     if (p.num_seqs <= NT) {
         // one chunk: a single load of the lengths and a single two-value scan
@@ -273,16 +301,43 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         const int2 inc = block_scan2_incl<NT>(make_int2(u, q), s2);
         if (seqtab && b < p.num_seqs) seqtab[b] = make_int4(L, Q, inc.x - u, inc.y - q);
         const int W = s2[NT / 32].x;
-        const int S = __syncthreads_count(u > 0) * (p.num_kv_heads / p.hg);   // non-empty segments
+        const int nseg = p.num_kv_heads / p.hg;                             // segments of a sequence
+        const int S = __syncthreads_count(u > 0) * nseg;                   // non-empty segments
         const int P = participating_ctas(ncta, W, S);
         *W_out = W;
         *P_out = P;
         if (cta >= P) return false;
-        const int u0 = cta_start(cta, W, P);
-        const int u1 = cta_start(cta + 1, W, P);
+        const int Ub = inc.x - u;
+        int u0, u1;
+        if (bnd != nullptr && P <= bnd_max) {
+            // weighted cut: boundary i sits at weight floor(i Wt / P); the thread of
+            // the sequence whose weight range holds it maps it to a unit (a weight
+            // inside a segment's extra ce maps to the segment's end)
+            const int w = u + (u > 0 ? ce * nseg : 0);
+            const int wincl = block_scan_incl<NT>(w, scratch);
+            const int Wt = scratch[NT / 32];
+            if (b < p.num_seqs && u > 0) {
+                const int Wb = wincl - w, seglen = u / nseg, segw = seglen + ce;
+                int i = floor_div_small((long long)Wb * P + Wt - 1, Wt);
+                const int i_end = min(P, floor_div_small((long long)(Wb + w) * P + Wt - 1, Wt));
+                for (; i < i_end; ++i) {
+                    const int off = floor_div_small((long long)i * Wt, P) - Wb;
+                    const int j = floor_div_small(off, segw), o = off - j * segw;
+                    bnd[i] = Ub + j * seglen + min(o, seglen);
+                }
+            }
+            if (tid == 0) bnd[P] = W;
+            __syncthreads();
+            u0 = bnd[cta];
+            u1 = bnd[cta + 1];
+            if (bnd_used) *bnd_used = true;
+        } else {
+            u0 = cta_start(cta, W, P);
+            u1 = cta_start(cta + 1, W, P);
+        }
         *u0_out = u0;
         *u1_out = u1;
-        const int Ub = inc.x - u;
+        if (u0 >= u1) return false;
         if (b < p.num_seqs && u > 0) {
             Cursor c;
             c.b = b;
