@@ -34,10 +34,19 @@
 // the CUDA cores (except zeroing the unwritten tail rows of a sequence's last
 // page, which may hold NaN).
 //
+// FP8 (e4m3) caches, head_dim 128, NCOL <= 8: the K pages stay e4m3 and S^T
+// runs on kind::f8f6f4 MMAs against the q rows, each scaled by a power of two
+// and split exactly into two e4m3 terms (columns n and 8 + n, added in the
+// softmax with the page's k scale); the V pages land in the upper half of a
+// bf16 operand slot and the epilogue warpgroup widens them in place; P
+// carries the page's v scale.  Page scales reach a ring in shared memory by
+// cp.async.
+//
 // Work partition: the balanced unit partition of common.cuh, one persistent
-// CTA per SM.  A CTA takes its last piece first and then walks its range from
-// the start, so both pieces of every segment cut between two CTAs finish
-// early and their merge overlaps the rest of the work.
+// CTA per SM (for wide segments, cut by weight with a per-piece charge).  A
+// CTA takes its last piece first and then walks its range from the start, so
+// both pieces of every segment cut between two CTAs finish early and their
+// merge overlaps the rest of the work.
 //
 // Split segments: a split piece's epilogue stores its partial (m, l, acc) and
 // hands it to the merge warp, which reads the segment's ticket: when every
