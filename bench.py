@@ -227,9 +227,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": 16,
-                       "kv_bytes_per_step": w.kv_bytes()},
+            "config": workload_config(w),
             "seq_steps_per_s": w.num_seqs / (ms / 1e3),
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": st.threads, "kind": "oracle",
                              "sample": f"each step: oracle append + attention for {spp} of the {w.num_seqs} "
@@ -418,11 +416,7 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3", "data": "synthetic",
-            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": 16,
-                       "kv_dtype": w.kv_dtype, "context_lens": lens_summary(w), "q_len_max": int(w.q_lens.max()),
-                       "pool_blocks": w.num_blocks,
-                       "kv_bytes_per_step": kvb, "l2": l2_note,
+            "config": {**workload_config(w), "l2": l2_note,
                        "launch": "CUDA graph replay per step" if use_graph else "eager, through the binding",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_hbm_peak": 100.0 * value / peak,
@@ -457,6 +451,14 @@ def run_ours(args):
 def lens_summary(w):
     L = np.asarray(w.context_lens)
     return f"min {int(L.min())}, median {int(np.median(L))}, max {int(L.max())}, mean {float(L.mean()):.0f}"
+
+
+def workload_config(w) -> dict:
+    """The workload keys of the JSON line's config (the same in both arms)."""
+    return {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": 16,
+            "kv_dtype": w.kv_dtype, "context_lens": lens_summary(w), "q_len_max": int(w.q_lens.max()),
+            "pool_blocks": w.num_blocks, "kv_bytes_per_step": w.kv_bytes()}
 
 
 def main():
