@@ -110,6 +110,7 @@ struct Cfg {
     static constexpr int OFF_P = OFF_Q + 2 * QBUF;
     static constexpr int PBUF = NPAD * kTileTok * 2;
     static constexpr int OFF_RED = OFF_P + NSB * PBUF;                 // float [8 slots][RMAX]
+    static_assert(NSB * PBUF >= 384 * 16, "the P ring holds the planning scratch (int4 per sequence)");
     static constexpr int OFF_LRED = OFF_RED + 8 * RMAX * 4;            // float [2][4 warps][RMAX]
     static constexpr int OFF_EM = OFF_LRED + 2 * 4 * RMAX * 4;         // float [2][RMAX]
     static constexpr int OFF_PD = OFF_EM + 2 * RMAX * 4;               // int [2][8]: piece descriptors
@@ -475,7 +476,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     int* bndtab = (K::PTAB && !EWG) ? reinterpret_cast<int*>(smem + K::OFF_BND) : nullptr;
     bool tab_used = false;
     const bool has_work = plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt,
-                                                seqtab, bndtab, K::TABMAX, 24, &tab_used);
+                                                seqtab, bndtab, K::TABMAX, 24, &tab_used,
+                                                reinterpret_cast<int4*>(smem + K::OFF_P));   // (P ring unused yet)
     const Part part{W, P, tab_used ? bndtab : nullptr};
     if (!has_work) {             // uniform across the CTA
         tc_fence_before();

@@ -276,13 +276,15 @@ __device__ __forceinline__ int2 block_scan2_incl(int2 v, int2* scratch /* NT/32 
 // without reading global memory (cursor_next with the table).
 // With bnd != nullptr, num_seqs <= NT and P <= bnd_max, the CTA ranges are cut
 // by weight instead (every non-empty segment weighs its units plus ce) into
-// the table bnd[0..P] (*bnd_used is set to whether it was).  A range may come
-// out empty only at a segment boundary, and such a CTA has no work.
+// the table bnd[0..P] (*bnd_used is set to whether it was), using tmp (int4
+// per sequence, scratch for the call) for the sequences' weight prefixes.  A
+// range may come out empty only at a segment boundary, and such a CTA has no
+// work.
 template <int NT>
 __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch, Cursor* cur,
                             int* u0_out, int* u1_out, int* W_out, int* P_out, Cursor* tail = nullptr,
                             int4* seqtab = nullptr, int* bnd = nullptr, int bnd_max = 0, int ce = 0,
-                            bool* bnd_used = nullptr) {
+                            bool* bnd_used = nullptr, int4* tmp = nullptr) {
     if (bnd_used) *bnd_used = false;
     const int tid = threadIdx.x;
     if (p.num_seqs <= NT) {
@@ -310,23 +312,32 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         const int Ub = inc.x - u;
         int u0, u1;
         if (bnd != nullptr && P <= bnd_max) {
-            // weighted cut: boundary i sits at weight floor(i Wt / P); the thread of
-            // the sequence whose weight range holds it maps it to a unit (a weight
-            // inside a segment's extra ce maps to the segment's end)
+            // weighted cut: boundary i sits at weight x = floor(i Wt / P), in the
+            // sequence whose weight range holds it; a weight inside a segment's
+            // extra ce maps to the segment's end.  One thread per boundary.
             const int w = u + (u > 0 ? ce * nseg : 0);
             const int wincl = block_scan_incl<NT>(w, scratch);
             const int Wt = scratch[NT / 32];
-            if (b < p.num_seqs && u > 0) {
-                const int Wb = wincl - w, seglen = u / nseg, segw = seglen + ce;
-                int i = floor_div_small((long long)Wb * P + Wt - 1, Wt);
-                const int i_end = min(P, floor_div_small((long long)(Wb + w) * P + Wt - 1, Wt));
-                for (; i < i_end; ++i) {
-                    const int off = floor_div_small((long long)i * Wt, P) - Wb;
-                    const int j = floor_div_small(off, segw), o = off - j * segw;
-                    bnd[i] = Ub + j * seglen + min(o, seglen);
+            if (b < p.num_seqs) tmp[b] = make_int4(wincl, Ub, u, 0);
+            __syncthreads();
+            for (int i = tid; i <= P; i += NT) {
+                int v = W;
+                if (i < P) {
+                    const int x = floor_div_small((long long)i * Wt, P);
+                    int lo = 0, hi = p.num_seqs - 1;          // the first sequence with wincl > x
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        if (tmp[mid].x > x) hi = mid;
+                        else lo = mid + 1;
+                    }
+                    const int4 e = tmp[lo];                    // (wincl, Ub, units): non-empty
+                    const int seglen = e.z / nseg, segw = seglen + ce;
+                    const int off = x - (e.x - e.z - ce * nseg);
+                    const int j = off / segw, o = off - j * segw;
+                    v = e.y + j * seglen + min(o, seglen);
                 }
+                bnd[i] = v;
             }
-            if (tid == 0) bnd[P] = W;
             __syncthreads();
             u0 = bnd[cta];
             u1 = bnd[cta + 1];
