@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>;
     using B = Bars<NSK, NSV, FP8>;
     static_assert(B::END == K::NBAR, "barrier count");
-    static_assert(!FP8 || EWG, "FP8 pages are converted by the epilogue warpgroup");
+    static_assert(!FP8 || EWG, "FP8 V pages are widened by the epilogue warpgroup");
     constexpr int RMAX = K::RMAX;
     constexpr int kThreads = threads_of<EWG>();
     extern __shared__ uint8_t smem_raw[];
@@ -423,8 +423,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             reinterpret_cast<uint4*>(smem + K::OFF_SC)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
-        // K/V operand slots are filled by bulk copies (bf16) or by the converting
-        // warpgroup (FP8: all 128 threads arrive)
+        // K slots are filled by bulk copies (bf16 or e4m3 pages); V slots too, or
+        // (FP8) by the epilogue warpgroup's widening (all 128 threads arrive)
         for (int s = 0; s < NSK; ++s) {
             mbar_init(bar(B::KFULL + s), 1);
             mbar_init(bar(B::KEMPTY + s), 1);
@@ -1378,8 +1378,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     if (d.last) break;
                 }
             } else {
-                // FP8: this warpgroup also widens every V tile in place (the softmax
-                // warpgroup widens K).  Each round takes whatever is ready: a finished
+                // FP8: this warpgroup also widens every V tile in place (K stays e4m3
+                // for the S MMA).  Each round takes whatever is ready: a finished
                 // piece's epilogue, the next V tile (agreed across the warpgroup by bar.red).
                 const int T = tile_count();
                 int vt = 0, pc = 0;
