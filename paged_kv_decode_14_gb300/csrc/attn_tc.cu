@@ -109,7 +109,9 @@ struct Cfg {
     static constexpr int QBUF = NPAD * D * 2;
     static constexpr int OFF_P = OFF_Q + 2 * QBUF;
     static constexpr int PBUF = NPAD * kTileTok * 2;
-    static constexpr int OFF_RED = OFF_P + NSB * PBUF;                 // float [8 slots][RMAX]
+    // wide segments (no high/low columns) keep P's low parts in a second ring
+    static constexpr int OFF_PLO = OFF_P + NSB * PBUF;
+    static constexpr int OFF_RED = OFF_PLO + (SPLIT ? 0 : NSB * PBUF);  // float [8 slots][RMAX]
     static_assert(NSB * PBUF >= 384 * 16, "the P ring holds the planning scratch (int4 per sequence)");
     static constexpr int OFF_LRED = OFF_RED + 8 * RMAX * 4;            // float [2][4 warps][RMAX]
     static constexpr int OFF_EM = OFF_LRED + 2 * 4 * RMAX * 4;         // float [2][RMAX]
@@ -993,6 +995,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         const uint64_t a = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
                         const uint64_t b = smem_desc(pbase + pg * 256, 128, 16 * 128);
                         mma_bf16(ocol, a, b, idPV, (pg > 0 || t0 > 0) ? 1u : 0u);
+                        if constexpr (!SPLIT) {      // (wide: P's low parts, same accumulator)
+                            const uint64_t bl = smem_desc(pbase + (K::OFF_PLO - K::OFF_P) + pg * 256, 128, 16 * 128);
+                            mma_bf16(ocol, a, bl, idPV, 1u);
+                        }
                     }
                     mma_commit(bar(B::PEMPTY + t % NSB));
                     mma_commit(bar(B::VEMPTY + vs));
@@ -1256,7 +1262,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 uint8_t* pdst = smem + K::OFF_P + (t % NSB) * K::PBUF + tt * 16;
 #pragma unroll
                 for (int cc = 0; cc < NPAD / 8; ++cc) {
-                    uint32_t w4[4];
+                    uint32_t w4[4], l4[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         float a, b;
@@ -1267,12 +1273,21 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                             a = hi;
                             b = pv - hi;
                         } else {
+                            // wide: column n's high part here, its low part in the second ring
                             a = FP8 ? pr[cc * 8 + 2 * h] * vscale : pr[cc * 8 + 2 * h];
                             b = FP8 ? pr[cc * 8 + 2 * h + 1] * vscale : pr[cc * 8 + 2 * h + 1];
+                            const float ah = __bfloat162float(__float2bfloat16_rn(a));
+                            const float bh = __bfloat162float(__float2bfloat16_rn(b));
+                            l4[h] = pack_bf16x2(a - ah, b - bh);
+                            a = ah;
+                            b = bh;
                         }
                         w4[h] = pack_bf16x2(a, b);
                     }
                     *reinterpret_cast<uint4*>(pdst + cc * (16 * 128)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    if constexpr (!SPLIT)
+                        *reinterpret_cast<uint4*>(pdst + (K::OFF_PLO - K::OFF_P) + cc * (16 * 128)) =
+                            make_uint4(l4[0], l4[1], l4[2], l4[3]);
                 }
                 // unwritten tail slots of the sequence's last page: zero their V rows (they may hold NaN)
                 if (k < np && pos >= L) {
@@ -1473,9 +1488,9 @@ cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int
     if (head_dim == 128)
         return fp8     ? tc::launch_t<128, 16, true, 4, 4, true, true>(p, ncta, st)
                : split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
-                       : tc::launch_t<128, 32, false, 2, 3, false>(p, ncta, st);
+                       : tc::launch_t<128, 32, false, 2, 2, false>(p, ncta, st);
     return split ? tc::launch_t<64, 16, true, 4, 6, true>(p, ncta, st)
-                 : tc::launch_t<64, 32, false, 4, 6, false>(p, ncta, st);
+                 : tc::launch_t<64, 32, false, 4, 4, false>(p, ncta, st);
 }
 
 }  // namespace pkv

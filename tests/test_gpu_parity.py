@@ -72,6 +72,11 @@ SWEEP = [
     (128, 8, 4, [0, 33, 0, 517], [0, 1, 0, 1], "fp8"),         # FP8, empty sequences, four kv-heads per segment
     # verify windows (R = 20, wide segments: the weighted cut) over short and long sequences
     (128, 32, 8, [20, 700, 33, 17, 400, 90, 16, 1000], [5] * 8, "bf16"),
+    # large batches: past the shared-memory sequence table (256 bf16 / 128 FP8
+    # sequences) and past one planning chunk (384 sequences)
+    (128, 32, 8, np.random.default_rng(901).integers(1, 81, 600).tolist(), [1] * 600, "bf16"),
+    (128, 32, 8, np.random.default_rng(902).integers(1, 121, 200).tolist(), [1] * 200, "fp8"),
+    (128, 32, 8, np.random.default_rng(903).integers(5, 61, 450).tolist(), [5] * 450, "bf16"),
 ]
 
 
