@@ -28,6 +28,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -110,7 +111,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -211,7 +212,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from paged_kv_decode_14_gb300 import workloads as wl
-    w = wl.CONFIGS[args.config]()
+    w = wl.WORKLOADS[args.config]()
     spp = 2
     st = OracleStepper(w, spp)
     for _ in range(args.warmup):
@@ -271,7 +272,7 @@ def run_ours(args):
     from paged_kv_decode_14_gb300.runner import DeviceWorkload
 
     nat.lib()
-    w = wl.CONFIGS[args.config]()
+    w = wl.WORKLOADS[args.config]()
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     if args.l2 == "rotate":

@@ -46,8 +46,8 @@ def lib():
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
-                raise RuntimeError(f"libpagedkv.so not found at {LIB_PATH}: run "
-                                   "`python -c 'import __graft_entry__ as g; g.build()'` first")
+                raise RuntimeError(f"libpagedkv.so not found at {LIB_PATH}: build it first "
+                                   "(`python -m paged_kv_decode_14_gb300.build`)")
             L = ctypes.CDLL(LIB_PATH)
             c = ctypes
             vp, i32, i64 = c.c_void_p, c.c_int32, c.c_int64

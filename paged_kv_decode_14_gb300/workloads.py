@@ -310,7 +310,8 @@ def long_fp8_b128_d128(seed: int = 5, num_seqs: int = 128, n_long: int = 4,
                          pool_factor=1.1, outlier_p=0.01)
 
 
-CONFIGS = {
+# The five named workloads, by number.
+WORKLOADS = {
     1: tiny_decode,
     2: decode_b32_d128,
     3: prefix_reuse_b32_d64,

@@ -46,7 +46,7 @@ def caches_equal(a: np.ndarray, b: np.ndarray, fp8: bool) -> bool:
 
 @functools.lru_cache(maxsize=None)
 def config_workload(n: int):
-    return wl.CONFIGS[n]()
+    return wl.WORKLOADS[n]()
 
 
 @functools.lru_cache(maxsize=None)
