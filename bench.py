@@ -9,11 +9,15 @@ merged in-kernel) on the continuous-batch decode workload: 32 sequences,
 
 Prints ONE JSON line (rank 0).  `value` is KV GB/s of the whole step
 (algorithmic KV bytes / device time of append + attention), inputs resident in
-HBM; by default the timed steps rotate over enough copies of the workload
-that no step finds its K/V in L2 (`--l2 flush` writes a buffer of twice the L2
-size before every step instead, which also evicts the kernels' code).
-`--impl reference` times the CPU oracle on the host cores instead (a
-deliberately slow reference).
+HBM.  By default the timed steps rotate over enough copies of the workload
+that no step finds its K/V in L2, and K steps are timed back to back as one
+CUDA-event interval behind a queued spin kernel, so the interval holds the
+GPU's time and not the host's launch overhead; `--l2 flush` writes a buffer of
+twice the L2 size before every step instead (timed per step, the flush
+excluded), which also evicts the kernels' code.  The attention kernel's
+roofline uses its own device time per launch, taken the same way over K
+launches.  `--impl reference` times the CPU oracle on the host cores instead
+(a deliberately slow reference).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch with torchrun (one rank per GPU); every rank runs its own
@@ -71,10 +75,12 @@ def hbm_peak():
 
 
 def attn_algorithmic_bytes(w) -> int:
-    """Bytes the attention must move once: KV (+ FP8 scales), q, out, the block
-    table entries it reads and the two length arrays."""
+    """Bytes the attention must move once: KV (+ FP8 scales) counting each
+    distinct physical block once (blocks shared by several sequences' tables
+    are one read), q, out, the block-table entries it reads and the two length
+    arrays."""
     nblk = int(((w.context_lens.astype(np.int64) + 15) // 16).sum())
-    return w.kv_bytes() + 2 * w.q.nbytes + 4 * nblk + 8 * w.num_seqs
+    return w.unique_kv_bytes() + 2 * w.q.nbytes + 4 * nblk + 8 * w.num_seqs
 
 
 def kernel_source_hash() -> str:
@@ -196,7 +202,8 @@ class OracleStepper:
 
 
 def cpu_baseline(w, seconds: float, seqs_per_step: int = 8):
-    """Oracle throughput over ~`seconds` of sample steps: (GB/s, threads, steps, s)."""
+    """Oracle throughput over ~`seconds` of sample steps:
+    (GB/s, threads, steps, s, sequences per step)."""
     st = OracleStepper(w, seqs_per_step)
     tot_b, tot_t, n = 0, 0.0, 0
     while tot_t < seconds:
@@ -204,7 +211,7 @@ def cpu_baseline(w, seconds: float, seqs_per_step: int = 8):
         tot_b += b
         tot_t += t
         n += 1
-    return tot_b / tot_t / 1e9, st.threads, n, tot_t
+    return tot_b / tot_t / 1e9, st.threads, n, tot_t, st.spp
 
 
 def run_reference(args):
@@ -255,6 +262,14 @@ def job_throughput_gbs(bytes_per_step: int, steps: int, max_ms: float, world: in
     return world * bytes_per_step * steps / (max_ms / 1e3) / 1e9
 
 
+def queue_ahead(torch, ms: float = 25.0):
+    """Queue a spin kernel of ~`ms` on the current stream before a timed
+    region: the host enqueues the timed launches while it runs, so the events
+    measure the GPU's time, not the Python launch overhead of the binding (a
+    serving loop launches from native code or a CUDA graph)."""
+    torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -275,9 +290,11 @@ def run_ours(args):
     w = wl.WORKLOADS[args.config]()
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    kvb = w.unique_kv_bytes()            # algorithmic KV bytes of a step (shared blocks once)
     if args.l2 == "rotate":
-        # independent copies (own cache, q, tables) until 3x the L2 size is covered
-        n_copies = max(2, -(-3 * l2 // max(1, w.kv_bytes())))
+        # independent copies (own cache, q, tables) until 3x the L2 size is
+        # covered, at most 16 (a small workload stays L2-resident: said below)
+        n_copies = min(16, max(2, -(-3 * l2 // max(1, kvb))))
         flush = None
     else:
         n_copies = 1
@@ -288,15 +305,18 @@ def run_ours(args):
         d.prefill()
         dws.append(d)
     dw = dws[0]
-    l2_note = (f"flushed before every timed step ({flush.numel() >> 20} MiB write)" if flush is not None else
-               f"inputs rotated over {n_copies} copies ({n_copies * w.kv_bytes() / 1e6:.0f} MB of KV > "
-               f"{l2 / 1e6:.0f} MB L2), no flush")
+    if flush is not None:
+        l2_note = f"flushed before every timed step ({flush.numel() >> 20} MiB write)"
+    elif n_copies * kvb > l2:
+        l2_note = (f"inputs rotated over {n_copies} copies ({n_copies * kvb / 1e6:.0f} MB of KV > "
+                   f"{l2 / 1e6:.0f} MB L2), no flush")
+    else:
+        l2_note = (f"inputs rotated over {n_copies} copies ({n_copies * kvb / 1e6:.1f} MB of KV, L2-resident: "
+                   f"{l2 / 1e6:.0f} MB L2)")
 
-    # --graph: each copy's step (append + attention, with the attention's
-    # programmatic launch edge) and, for the per-kernel split, its append and
-    # its attention alone are captured as CUDA graphs and replayed.  By default
-    # steps launch through the binding: the host stays ahead of the GPU at
-    # these step times, and the eager launches measured no slower.
+    # --graph: each copy's step (append + attention) and, for the per-kernel
+    # split, its append and its attention alone are captured as CUDA graphs
+    # and replayed.  By default steps launch through the binding.
     use_graph = args.graph
     g_step, g_app, g_att = [], [], []
     if use_graph:
@@ -318,101 +338,103 @@ def run_ours(args):
         else:
             dws[i % n_copies].step()
 
-    def pick(i):
-        if flush is not None:
-            flush.zero_()
-        return dws[i % n_copies]
+    def run_attn(i):
+        if use_graph:
+            g_att[i % n_copies].replay()
+        else:
+            dws[i % n_copies].attend()
+
+    def run_app(i):
+        if use_graph:
+            g_app[i % n_copies].replay()
+        else:
+            dws[i % n_copies].append_step()
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # ---------------- device-resident timing
+    def timed(fn, n):
+        """Device time of n calls fn(0..n-1), us per call: back to back in one
+        event interval (rotate mode), or each after an L2 flush that the events
+        exclude (flush mode)."""
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            queue_ahead(torch)
+            e0.record(stream)
+            for i in range(n):
+                fn(i)
+            e1.record(stream)
+            barrier()
+            return e0.elapsed_time(e1) * 1e3 / n
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i, (a, b) in enumerate(evs):
+            flush.zero_()
+            a.record(stream)
+            fn(i)
+            b.record(stream)
+        barrier()
+        return 1e3 * float(np.sum([a.elapsed_time(b) for a, b in evs])) / n
+
+    # ---------------- device-resident timing of the whole step
     for i in range(args.warmup):
-        pick(i)
         run_step(i)
     barrier()
-    # a step is timed as one interval (no event between append and attention,
-    # so the attention's programmatic launch can overlap the append's tail)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local) if not args.no_clocks else None
     if clocks:
         clocks.__enter__()
         # keep the GPU under the same load while the sampler starts up, right
-        # before the timed region (the timed region alone is tens of ms)
+        # before the timed region (the timed region alone is a few ms)
         t_end = time.perf_counter() + args.soak_seconds
         while time.perf_counter() < t_end:
             for i in range(20):
-                pick(i)
                 run_step(i)
             torch.cuda.synchronize(dev)
     barrier()
     wall0 = time.perf_counter()
-    for i, (e0, e2) in enumerate(ev):
-        pick(i)                           # L2 flush (outside the timed events), if flushing
-        e0.record(stream)
-        run_step(i)
-        e2.record(stream)
-    barrier()
+    step_us = timed(run_step, args.steps)
     wall = time.perf_counter() - wall0
     if clocks:
         clocks.__exit__()
-    step_ms = [a.elapsed_time(c) for a, c in ev]
-    # per-kernel split (separate pass, for the roofline of the attention kernel)
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i, (e0, e1, e2) in enumerate(kev):
-        d = pick(i)
-        e0.record(stream)
-        if use_graph:
-            g_app[i % n_copies].replay()
-        else:
-            d.append_step()
-        e1.record(stream)
-        if use_graph:
-            g_att[i % n_copies].replay()
-        else:
-            d.attend()
-        e2.record(stream)
-    barrier()
-    attn_ms = [b.elapsed_time(c) for _, b, c in kev]
-    app_ms = [a.elapsed_time(b) for a, b, _ in kev]
-    tot = max_over_ranks(float(np.sum(step_ms)), world, dev)
-    kvb = w.kv_bytes()
-    ms = tot / args.steps
-    value = job_throughput_gbs(kvb, args.steps, tot, world)
+    tot_ms = max_over_ranks(step_us * args.steps / 1e3, world, dev)
+    ms = tot_ms / args.steps
+    value = job_throughput_gbs(kvb, args.steps, tot_ms, world)
+
+    # ---------------- per-kernel split (the roofline of the attention kernel)
+    attn_us = timed(run_attn, args.steps)
+    app_us = timed(run_app, args.steps)
 
     # ---------------- end to end through the public API, host buffers
-    hin, hout = w.step_io_bytes()
-    pin = {n: getattr(dw, n).cpu().pin_memory() for n in ("q", "k_new", "v_new", "slots", "block_tables",
-                                                           "context_lens", "q_lens")}
+    # every step uploads its inputs (one pinned buffer, one copy), runs the
+    # step and reads its output back to pinned host memory
+    pins = [d.pinned_io() for d in dws]
     host_out = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    for i in range(args.warmup + args.steps):
-        d = pick(i)
-        if i >= args.warmup:
-            e2e_ev[i - args.warmup][0].record(stream)
-        for n, t in pin.items():
-            getattr(d, n).copy_(t, non_blocking=True)
+
+    def e2e_step(i):
+        d = dws[i % n_copies]
+        d.io.copy_(pins[i % n_copies], non_blocking=True)
         d.step()
         host_out.copy_(d.out, non_blocking=True)
-        if i >= args.warmup:
-            e2e_ev[i - args.warmup][1].record(stream)
+
+    for i in range(args.warmup):
+        e2e_step(i)
     barrier()
-    e2e_tot = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in e2e_ev)), world, dev)
+    e2e_us = timed(e2e_step, args.steps)
+    e2e_tot = max_over_ranks(e2e_us * args.steps / 1e3, world, dev)
     e2e_val = job_throughput_gbs(kvb, args.steps, e2e_tot, world)
+    hin, hout = int(dw.io.numel()), int(dw.out.numel() * dw.out.element_size())
 
     # ---------------- roofline of the dominant kernel (attention)
     peak, peak_kind = hbm_peak()
-    attn_avg_ms = float(np.mean(attn_ms))
-    achieved = attn_algorithmic_bytes(w) / (attn_avg_ms * 1e-3) / 1e9
+    abytes = attn_algorithmic_bytes(w)
+    achieved = abytes / (attn_us * 1e-6) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": load_traffic(w.name), "peak_kind": f"{peak_kind} (copy bandwidth)",
             "kernel": "paged attention (persistent split-KV, in-kernel merge)",
-            "algorithmic_bytes_per_launch": attn_algorithmic_bytes(w),
-            "avg_launch_us": attn_avg_ms * 1e3}
+            "algorithmic_bytes_per_launch": abytes, "avg_launch_us": attn_us,
+            "timing": ("back-to-back launches over rotating copies, one event interval, host ahead"
+                       if flush is None else "per launch, L2 flushed before each (flush excluded)")}
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -421,24 +443,27 @@ def run_ours(args):
                        "launch": "CUDA graph replay per step" if use_graph else "eager, through the binding",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_hbm_peak": 100.0 * value / peak,
-            "seq_steps_per_s": world * w.num_seqs * args.steps / (tot / 1e3),
-            "attention_us": attn_avg_ms * 1e3, "append_us": float(np.mean(app_ms)) * 1e3,
-            "step_us_p10_p50_p90": [float(np.percentile(step_ms, q)) * 1e3 for q in (10, 50, 90)],
+            "seq_steps_per_s": world * w.num_seqs * args.steps / (tot_ms / 1e3),
+            "attention_us": attn_us, "append_us": app_us,
             "roofline": roof,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": hin, "d2h_bytes_per_step": hout,
                     "ms_per_step": e2e_tot / args.steps},
             "gpu_launches": 2 * args.steps,
             "wall_s_timed_region": wall}
+    if kvb != w.kv_bytes():
+        line["kv_bytes_logical_per_step"] = w.kv_bytes()
+        line["value_logical_kv"] = job_throughput_gbs(w.kv_bytes(), args.steps, tot_ms, world)
     if clocks:
         line["clocks"] = clocks.summary()
         if line["clocks"] is not None:
             line["clocks"]["window"] = f"{args.soak_seconds:.1f} s of identical untimed steps + the timed region"
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, threads, n, el = cpu_baseline(w, args.cpu_seconds)
+        gbs, threads, n, el, spp = cpu_baseline(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{n} full decode steps (append + attention of all {w.num_seqs} "
-                                          f"sequences) in {el:.1f} s"}
+                                "sample": f"{n} oracle steps in {el:.1f} s, each the append of the step's new "
+                                          f"tokens and the attention of {spp} of the {w.num_seqs} sequences "
+                                          f"(rotating); GB/s from the KV bytes of those sequences"}
     errs = [e for d in dws for e in d.errors()]
     if any(errs):
         line["device_errors"] = errs

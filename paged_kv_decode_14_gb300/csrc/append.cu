@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t* __restrict__
                                                      const float* __restrict__ k_scales,
                                                      const float* __restrict__ v_scales, int* err) {
     griddep_launch();                            // the attention that follows may start its set-up
+    griddep_wait();                              // the previous kernel's reads and writes are done
     const int NCH = D * E / 16;                  // 16-byte chunks per token row in the cache
     const int64_t per_tok = (int64_t)Hkv * NCH * 2;
     const int64_t total = num_tokens * per_tok;
@@ -73,15 +74,14 @@ cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_n
     const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (E == 2)
-        append_kernel<2><<<(unsigned)blocks, threads, 0, st>>>(
-            (const uint8_t*)k_new, (const uint8_t*)v_new, slots, num_tokens, c.num_kv_heads, c.head_dim,
-            c.num_blocks, (uint8_t*)c.k_cache, (uint8_t*)c.v_cache, nullptr, nullptr, err);
-    else
-        append_kernel<1><<<(unsigned)blocks, threads, 0, st>>>(
-            (const uint8_t*)k_new, (const uint8_t*)v_new, slots, num_tokens, c.num_kv_heads, c.head_dim,
-            c.num_blocks, (uint8_t*)c.k_cache, (uint8_t*)c.v_cache, c.k_scales, c.v_scales, err);
-    return cudaGetLastError();
+    // A programmatic dependent launch: the kernel may be scheduled while the
+    // previous one (an attention that triggers early) still runs, and waits
+    // for it before touching memory.
+    const float* ks = E == 2 ? nullptr : c.k_scales;
+    const float* vs = E == 2 ? nullptr : c.v_scales;
+    return launch_pdl(E == 2 ? append_kernel<2> : append_kernel<1>, dim3((unsigned)blocks), dim3(threads), 0, st,
+                      (const uint8_t*)k_new, (const uint8_t*)v_new, slots, num_tokens, (int)c.num_kv_heads,
+                      (int)c.head_dim, (int64_t)c.num_blocks, (uint8_t*)c.k_cache, (uint8_t*)c.v_cache, ks, vs, err);
 }
 
 }  // namespace pkv

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x;
+    griddep_launch();     // the next kernel on the stream may launch (it waits for this grid's results)
     griddep_wait();       // inputs of the previous kernel on the stream are visible
     Cursor cur;
     int u0, u1, W, P;
@@ -331,10 +332,9 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
 template <int D, int E, int RT>
 static cudaError_t launch_simt_t(const AttnParams& p, int ncta, cudaStream_t st) {
     using K = simt::Cfg<D, E, RT>;
-    auto kern = simt::attn_simt_kernel<D, E, RT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(ncta), dim3(simt::kThreads), (size_t)K::SMEM, st, p);
+    static std::atomic<uint64_t> attr_set{0};
+    return launch_pdl_bigsmem(attr_set, simt::attn_simt_kernel<D, E, RT>, dim3(ncta), dim3(simt::kThreads),
+                              (size_t)K::SMEM, st, p);
 }
 
 template <int D, int E>

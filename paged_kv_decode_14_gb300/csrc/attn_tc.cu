@@ -134,8 +134,13 @@ struct Cfg {
     // operand read the descriptors can form stays inside the allocation.
     static constexpr int SMEM = kMaxSmem - 1024;
     static constexpr int COL_S = 0;                      // S^T buffers: NSB x NPAD columns
-    static constexpr int COL_O = NSB * NPAD;             // O^T accumulators: [piece parity] x NPAD columns
-    static constexpr int NCOLS = (NSB + 2) * NPAD;
+    // O^T accumulators: [piece parity][kv-head of the segment] x NPAD columns.
+    // Each kv-head of a segment accumulates into its own: a P.V MMA of one
+    // head's page also multiplies the zero P entries of the other heads'
+    // columns, and 0 x NaN (a NaN stored in the page's V) must not reach them.
+    static constexpr int HGMAX = SPLIT ? 4 : 2;          // kv-heads per segment
+    static constexpr int COL_O = NSB * NPAD;
+    static constexpr int NCOLS = NSB * NPAD + 2 * HGMAX * NPAD;
     static constexpr int TMEM_COLS = NCOLS <= 64 ? 64 : NCOLS <= 128 ? 128 : 256;
     static_assert(NCOLS <= 256, "TMEM budget");
     static_assert(OFF_BAR % 8 == 0 && OFF_SEQ % 16 == 0 && OFF_RED % 16 == 0, "shared memory alignment");
@@ -195,10 +200,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// OR of v over the n threads of named barrier `id` (non-.aligned, like
+// named_bar_sync).
 __device__ __forceinline__ bool bar_red_or(int id, int n, bool v) {
     uint32_t r;
     asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbar.red.or.pred p, %2, %3, q;\nselp.u32 %0, 1, 0, p;\n}\n"
+        "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbarrier.red.or.pred p, %2, %3, q;\nselp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(r)
         : "r"((uint32_t)v), "r"(id), "r"(n)
         : "memory");
@@ -245,8 +252,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // conversion unit.  A code's 4 exponent and 3 mantissa bits are placed in the
 // low exponent bits and the top mantissa bits of a bf16, which then reads as
 // the code's value times 2^-120 (its bf16 subnormals are the e4m3 subnormals);
-// a bf16x2 multiply by 2^120 restores the value.  The NaN codes (0x7f, 0xff)
-// come out as +-480: the cache encoder never writes them.
+// a bf16x2 multiply by 2^120 restores the value.  The NaN codes (0x7f, 0xff;
+// the append keeps a NaN source value NaN) would come out as +-480 (0x43f0):
+// OR-ing 0x7fc0 into their lanes turns that into a bf16 NaN of the same sign.
 __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
     const uint32_t hb = ((w >> 4) & 0x07070707u) | (w & 0x80808080u);   // per byte: sign, 3 high exponent bits
     const uint32_t lb = (w << 4) & 0xF0F0F0F0u;                          // per byte: low exponent bit, mantissa
@@ -254,8 +262,9 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
     const __nv_bfloat162 k2 = __halves2bfloat162(__ushort_as_bfloat16(0x7B80), __ushort_as_bfloat16(0x7B80));
     const __nv_bfloat162 ra = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), k2);
     const __nv_bfloat162 rb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), k2);
-    lo = *reinterpret_cast<const uint32_t*>(&ra);
-    hi = *reinterpret_cast<const uint32_t*>(&rb);
+    const uint32_t nan = __vcmpeq4(w & 0x7F7F7F7Fu, 0x7F7F7F7Fu);        // 0xff in the bytes holding a NaN code
+    lo = *reinterpret_cast<const uint32_t*>(&ra) | (__byte_perm(nan, 0u, 0x1100) & 0x7FC07FC0u);
+    hi = *reinterpret_cast<const uint32_t*>(&rb) | (__byte_perm(nan, 0u, 0x3322) & 0x7FC07FC0u);
 }
 
 // Pieces of a CTA's unit range [u0, u1), in processing order: the piece
@@ -401,6 +410,15 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x;
+    // The kernel that follows on the stream may launch now: its CTAs take the
+    // SMs this grid frees as its CTAs finish, and run their own set-up while
+    // the last ones still stream (its dependency wait still holds back what
+    // it reads from this grid's results).
+    griddep_launch();
+    // This CTA's sequence lengths, loaded first: their latency overlaps the
+    // barrier, TMEM and Q-buffer set-up below.
+    int2 lq = make_int2(0, 0);
+    if (p.num_seqs <= kThreads && tid < p.num_seqs) lq = make_int2(__ldg(p.context_lens + tid), __ldg(p.q_lens + tid));
 
     auto bar = [&](int i) -> uint32_t { return sb + K::OFF_BAR + 8 * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K::OFF_MISC);
@@ -464,10 +482,12 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         tmem_alloc(smem_u32(tmem_slot), K::TMEM_COLS);
         tmem_relinquish();
     }
-    // Everything above touches only this CTA's shared memory and TMEM, so
-    // under a programmatic dependent launch it overlaps the previous kernel;
-    // inputs are read only after that kernel's writes are visible.
-    griddep_wait();
+    // Under a programmatic dependent launch this kernel starts while the
+    // previous kernel on the stream (the step's append) still runs.  The
+    // planning reads only caller inputs that kernel does not write (lengths,
+    // block tables, q), so it runs at once; the producer waits for the
+    // previous kernel's writes to be visible before its first K/V copy, and
+    // the merge warp before it touches the workspace.
     Cursor cur0, curt;
     int u0, u1, W, P;
     int4* seqtab = p.num_seqs <= K::SEQTAB ? reinterpret_cast<int4*>(smem + K::OFF_SEQ) : nullptr;
@@ -479,7 +499,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     bool tab_used = false;
     const bool has_work = plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt,
                                                 seqtab, bndtab, K::TABMAX, 24, &tab_used,
-                                                reinterpret_cast<int4*>(smem + K::OFF_P));   // (P ring unused yet)
+                                                reinterpret_cast<int4*>(smem + K::OFF_P),   // (P ring unused yet)
+                                                &lq);
     const Part part{W, P, tab_used ? bndtab : nullptr};
     if (!has_work) {             // uniform across the CTA
         tc_fence_before();
@@ -581,20 +602,30 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         tc_fence_after();
         float acc[RMAX], Lsum[RMAX], Mx[RMAX];
         {
-            float o[NPAD];
+            // column n belongs to kv-head n / R of the segment and sits in that head's accumulator
 #pragma unroll
-            for (int c = 0; c < NPAD; c += 16) {
-                float tmp[16];
-                tmem_ld16(tmem + lbase + K::COL_O + par * NPAD + c, tmp);
+            for (int n = 0; n < RMAX; ++n) acc[n] = 0.f;
+            for (int hh = 0; hh < HG; ++hh) {
+                float o[NPAD];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) o[c + x] = tmp[x];
+                for (int c = 0; c < NPAD; c += 16) {
+                    float tmp[16];
+                    tmem_ld16(tmem + lbase + K::COL_O + (par * K::HGMAX + hh) * NPAD + c, tmp);
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) o[c + x] = tmp[x];
+                }
+#pragma unroll
+                for (int n = 0; n < RMAX; ++n)
+                    if (n >= hh * R && n < hh * R + R) acc[n] = SPLIT ? (o[2 * n] + o[2 * n + 1]) : o[n];
             }
             const float* lw = lred + par * 4 * RMAX;
 #pragma unroll
             for (int n = 0; n < RMAX; ++n) {
                 Mx[n] = emref[par * RMAX + n];
                 Lsum[n] = lw[n] + lw[RMAX + n] + lw[2 * RMAX + n] + lw[3 * RMAX + n];
-                acc[n] = SPLIT ? (o[2 * n] + o[2 * n + 1]) : o[n];
+                // no visible token of the piece reached column n: its head's accumulator may
+                // not even have been started in this piece
+                if (Mx[n] == -INFINITY) acc[n] = 0.f;
             }
         }
         tc_fence_before();
@@ -754,6 +785,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             if constexpr (kQAhead) load_q(it, qv);
             win = load_win(it, div_small(it.pg0, HG));
         }
+        griddep_wait();                   // K/V pages the previous kernel wrote are visible from here
         while (ok && it.valid()) {
             PieceIter nx = it;
             uint4 qn[kQAhead ? QV : 1];
@@ -981,7 +1013,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             int t = 0, pc = 0;
             bool ok = true;
             while (ok && it.valid()) {
-                const uint32_t ocol = tmem + K::COL_O + (pc & 1) * NPAD;
+                const uint32_t obase = tmem + K::COL_O + (pc & 1) * K::HGMAX * NPAD;
+                uint32_t started = 0;             // kv-heads whose accumulator this piece has started
                 if (EWG && pc >= 2 && !(ok = wait_bar(bar(B::OFREE + (pc & 1)), ((pc >> 1) - 1) & 1, ctl))) break;
                 for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
                     const int np = min(kTP, it.npg - t0);
@@ -991,13 +1024,20 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     tc_fence_after();
                     const uint32_t vbase = sb + K::OFF_V + vs * (K::TILE + K::VSLACK);
                     const uint32_t pbase = sb + K::OFF_P + (t % NSB) * K::PBUF;
-                    for (int pg = 0; pg < np; ++pg) {
-                        const uint64_t a = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
-                        const uint64_t b = smem_desc(pbase + pg * 256, 128, 16 * 128);
-                        mma_bf16(ocol, a, b, idPV, (pg > 0 || t0 > 0) ? 1u : 0u);
-                        if constexpr (!SPLIT) {      // (wide: P's low parts, same accumulator)
-                            const uint64_t bl = smem_desc(pbase + (K::OFF_PLO - K::OFF_P) + pg * 256, 128, 16 * 128);
-                            mma_bf16(ocol, a, bl, idPV, 1u);
+                    // unit slot pg holds unit it.pg0 + t0 + pg of the segment: kv-head (hh0 + pg) % HG
+                    const int hh0 = (it.pg0 + t0) - div_small(it.pg0 + t0, HG) * HG;
+                    for (int hh = 0; hh < HG; ++hh) {
+                        const uint32_t ocol = obase + hh * NPAD;
+                        for (int pg = hh >= hh0 ? hh - hh0 : hh - hh0 + HG; pg < np; pg += HG) {
+                            const uint32_t accum = (started >> hh) & 1u;
+                            started |= 1u << hh;
+                            const uint64_t a = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
+                            const uint64_t b = smem_desc(pbase + pg * 256, 128, 16 * 128);
+                            mma_bf16(ocol, a, b, idPV, accum);
+                            if constexpr (!SPLIT) {      // (wide: P's low parts, same accumulator)
+                                const uint64_t bl = smem_desc(pbase + (K::OFF_PLO - K::OFF_P) + pg * 256, 128, 16 * 128);
+                                mma_bf16(ocol, a, bl, idPV, 1u);
+                            }
                         }
                     }
                     mma_commit(bar(B::PEMPTY + t % NSB));
@@ -1021,6 +1061,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         // segment, this warp waits for the segment's earlier pieces to be
         // published and merges them into shared memory, so that the last
         // epilogue only adds its own part.
+        griddep_wait();                   // tickets and partials of the previous launch are settled
         int n_expect = 0;
         PieceIter w = it;                 // -> the last piece
         for (;;) {
@@ -1152,7 +1193,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 const int Q = it.cur.Q, R = G * Q, L = it.cur.L, lim0 = L - Q;
                 const int np = min(kTP, it.npg - jt * kTP);
                 const int vs = t % NSV;
-                const uint32_t ocol = K::COL_O + (pc & 1) * NPAD;
+                const uint32_t obase = K::COL_O + (pc & 1) * K::HGMAX * NPAD;
                 // this thread's token: unit slot k of the tile -> (page, kv-head), position
                 const int k = tt >> 4;
                 const int qu = it.pg0 + jt * kTP + k;
@@ -1236,16 +1277,19 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         l_part[n] *= alpha[n];
                     }
                     if (jt > 0 && any_scale) {
-                        // O^T (TMEM) *= alpha once the previous tile's P.V has landed
+                        // O^T (TMEM) *= alpha once the previous tile's P.V has landed, in the
+                        // accumulator of every kv-head of the segment
                         wait_bar(bar(B::PEMPTY + (t - 1) % NSB), ((t - 1) / NSB) & 1, ctl);
                         tc_fence_after();
+                        for (int h2 = 0; h2 < HG; ++h2) {
 #pragma unroll
-                        for (int c = 0; c < NPAD; c += 16) {
-                            float o[16];
-                            tmem_ld16(tmem + lane_base + ocol + c, o);
+                            for (int c = 0; c < NPAD; c += 16) {
+                                float o[16];
+                                tmem_ld16(tmem + lane_base + obase + h2 * NPAD + c, o);
 #pragma unroll
-                            for (int x = 0; x < 16; ++x) o[x] *= alpha[SPLIT ? (c + x) / 2 : (c + x)];
-                            tmem_st16(tmem + lane_base + ocol + c, o);
+                                for (int x = 0; x < 16; ++x) o[x] *= alpha[SPLIT ? (c + x) / 2 : (c + x)];
+                                tmem_st16(tmem + lane_base + obase + h2 * NPAD + c, o);
+                            }
                         }
                     }
                     // keep red[] stable until every thread has read it
@@ -1447,8 +1491,9 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     }
 
     // ---------------------------------------------------------------- teardown
+    // (every role reaches this barrier from its own code path: the non-.aligned form)
     tc_fence_before();
-    __syncthreads();
+    cta_bar_sync();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, K::TMEM_COLS);
@@ -1458,10 +1503,9 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
 template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8 = false>
 static cudaError_t launch_t(const AttnParams& p, int ncta, cudaStream_t st) {
     using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>;
-    auto kern = attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(ncta), dim3(threads_of<EWG>()), K::SMEM, st, p);
+    static std::atomic<uint64_t> attr_set{0};
+    return launch_pdl_bigsmem(attr_set, attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>, dim3(ncta),
+                              dim3(threads_of<EWG>()), (size_t)K::SMEM, st, p);
 }
 
 }  // namespace tc
@@ -1472,10 +1516,12 @@ static int tc_col_limit(int rows) { return rows <= 8 ? 8 : 32; }
 
 // kv-heads per segment: the largest divisor of Hkv whose columns
 // (heads x G x max_q_len) fit the column limit.
+// At most 4 (narrow) or 2 (wide): each kv-head of a segment has its own O^T
+// accumulator in TMEM.
 int tc_heads_per_segment(int num_kv_heads, int rows) {
-    const int lim = tc_col_limit(rows);
+    const int lim = tc_col_limit(rows), cap = rows <= 8 ? 4 : 2;
     int hg = 1;
-    for (int h = 1; h <= num_kv_heads; ++h)
+    for (int h = 1; h <= min(num_kv_heads, cap); ++h)
         if (num_kv_heads % h == 0 && h * rows <= lim) hg = h;
     return hg;
 }

@@ -18,6 +18,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/pagedkv.h"
 
 namespace pkv {
@@ -63,6 +65,36 @@ __host__ inline cudaError_t launch_pdl(void (*kern)(Args...), dim3 grid, dim3 bl
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// launch_pdl for a kernel with more than 48 KiB of dynamic shared memory.
+// The function attribute that allows it is set once per device (`done` holds
+// one bit per device, static in the caller, one per kernel): setting it on
+// every launch costs a driver call for nothing.  A launch refused after the
+// attribute was lost (a device reset) sets it again and retries once.
+template <typename... Args>
+__host__ inline cudaError_t launch_pdl_bigsmem(std::atomic<uint64_t>& done, void (*kern)(Args...), dim3 grid,
+                                               dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    const bool set = bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0;
+    if (!set) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (bit) done.fetch_or(bit, std::memory_order_release);
+    }
+    e = launch_pdl(kern, grid, block, smem, st, args...);
+    if (e != cudaSuccess && set) {
+        (void)cudaGetLastError();
+        done.fetch_and(~bit, std::memory_order_release);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        done.fetch_or(bit, std::memory_order_release);
+        e = launch_pdl(kern, grid, block, smem, st, args...);
+    }
+    return e;
 }
 
 // ------------------------------------------------------------------ workspace
@@ -274,6 +306,8 @@ __device__ __forceinline__ int2 block_scan2_incl(int2 v, int2* scratch /* NT/32 
 // With seqtab != nullptr and num_seqs <= NT, seqtab[b] receives (L, Q, units
 // before b, first q row of b) for every sequence, so that cursors can move on
 // without reading global memory (cursor_next with the table).
+// With pre_lq != nullptr and num_seqs <= NT, *pre_lq holds this thread's
+// (context_lens[tid], q_lens[tid]), already loaded by the caller.
 // With bnd != nullptr, num_seqs <= NT and P <= bnd_max, the CTA ranges are cut
 // by weight instead (every non-empty segment weighs its units plus ce) into
 // the table bnd[0..P] (*bnd_used is set to whether it was), using tmp (int4
@@ -284,7 +318,7 @@ template <int NT>
 __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch, Cursor* cur,
                             int* u0_out, int* u1_out, int* W_out, int* P_out, Cursor* tail = nullptr,
                             int4* seqtab = nullptr, int* bnd = nullptr, int bnd_max = 0, int ce = 0,
-                            bool* bnd_used = nullptr, int4* tmp = nullptr) {
+                            bool* bnd_used = nullptr, int4* tmp = nullptr, const int2* pre_lq = nullptr) {
     if (bnd_used) *bnd_used = false;
     const int tid = threadIdx.x;
     if (p.num_seqs <= NT) {
@@ -294,8 +328,13 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         const int b = tid;
         int L = 0, Q = 0, u = 0, q = 0;
         if (b < p.num_seqs) {
-            L = p.context_lens[b];
-            Q = p.q_lens[b];
+            if (pre_lq) {
+                L = pre_lq->x;
+                Q = pre_lq->y;
+            } else {
+                L = p.context_lens[b];
+                Q = p.q_lens[b];
+            }
             if (cta == 0 && Q != 0 && !seq_valid(p, L, Q)) raise_error(p.err, PKV_DEVERR_LENGTH);
             u = seq_units(p, L, Q);
             q = seq_qrows(Q);

@@ -128,9 +128,15 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
+// Named barrier over `threads` threads.  The non-.aligned form: the
+// threads of a warp-specialised kernel may reach a barrier through different
+// code paths (the compiler is free to duplicate a role's tail), which the
+// .aligned form (bar.sync, __syncthreads) leaves undefined.
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+    asm volatile("barrier.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
+// The whole CTA, non-.aligned (see named_bar_sync).
+__device__ __forceinline__ void cta_bar_sync() { asm volatile("barrier.sync 0;\n" ::: "memory"); }
 
 // ------------------------------------------------------------------ TMEM
 

@@ -21,9 +21,22 @@ def out_bits(t: torch.Tensor) -> np.ndarray:
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def assert_attention_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str = ""):
+def assert_attention_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str = "", nan_aware: bool = False):
+    """Element-wise tolerance check.  By default any NaN in the GPU output
+    fails.  With nan_aware, an element must be NaN on the GPU exactly where
+    the oracle's is (a NaN stored in the cache propagates), and the others
+    must be within the tolerance."""
     g = to_f64(gpu_bits)
-    assert not np.isnan(g).any(), f"{what}: NaN in GPU output"
+    if nan_aware:
+        gn, rn = np.isnan(g), np.isnan(ref)
+        if not np.array_equal(gn, rn):
+            i = np.argwhere(gn != rn)[0]
+            raise AssertionError(f"{what}: NaN pattern differs ({int(gn.sum())} NaN on the GPU, "
+                                 f"{int(rn.sum())} in the oracle); first at {tuple(i)}")
+        g = np.where(gn, 0.0, g)
+        ref = np.where(rn, 0.0, ref)
+    else:
+        assert not np.isnan(g).any(), f"{what}: NaN in GPU output"
     err = np.abs(g - ref)
     bound = ATOL + RTOL * np.abs(ref)
     bad = err > bound

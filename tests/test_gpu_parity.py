@@ -112,6 +112,41 @@ def test_fp8_subnormal_codes():
     assert_attention_close(got, ref, "fp8 subnormal codes")
 
 
+@pytest.mark.parametrize("head_dim,group,num_kv_heads,dtype", [
+    (128, 4, 2, "fp8"),     # tensor-core FP8 kernel, two kv-heads per segment
+    (64, 4, 2, "fp8"),      # CUDA-core FP8 kernel (head_dim 64)
+    (128, 16, 2, "fp8"),    # CUDA-core FP8 kernel (G * Q > 8)
+    (128, 4, 2, "bf16"),    # tensor-core narrow kernel, two kv-heads per segment
+    (64, 1, 4, "bf16"),     # narrow kernel, four kv-heads per segment
+    (128, 16, 2, "bf16"),   # wide kernel (N = 32), two kv-heads per segment
+])
+def test_nan_in_cache_propagates(head_dim, group, num_kv_heads, dtype):
+    """A NaN source value is stored as NaN (bf16 bits copied; an E4M3 NaN code
+    for FP8: the append keeps NaN).  Attention over it gives NaN exactly where
+    the fp64 oracle does: every element of the rows whose K holds a NaN at a
+    visible position, and the one dimension of the rows whose V does; the
+    other kv-heads that share a segment, a tile and a P.V MMA with the NaN
+    page stay finite."""
+    Hkv = num_kv_heads
+    w = wl.make_workload("nan", context_lens=[300, 77, 1000, 40], q_lens=[1, 1, 1, 1],
+                         num_q_heads=Hkv * group, num_kv_heads=Hkv, head_dim=head_dim, kv_dtype=dtype,
+                         seed=93, outlier_p=0.01 if dtype == "fp8" else 0.0)
+    nan = np.uint16(0x7FC0)
+    firsts = np.concatenate([[0], np.cumsum(w.context_lens - w.q_lens)])
+    w.prefill_k = w.prefill_k.copy()
+    w.prefill_v = w.prefill_v.copy()
+    # K of sequence 0 at position 5 (kv-head 1), V of sequence 2 at position 600 (kv-head 0, dim 3)
+    w.prefill_k[int(firsts[0]) + 5, 1, 7] = nan
+    w.prefill_v[int(firsts[2]) + 600, 0, 3] = nan
+    kc, vc = oracle.build_cache(w)
+    ref, _ = oracle.attend(w, kc, vc)
+    assert np.isnan(ref).any() and not np.isnan(ref).all()
+    dw, got = run_gpu(w)
+    gk, gv = dw.cache_bytes()
+    assert caches_equal(gk, kc, dtype == "fp8") and caches_equal(gv, vc, dtype == "fp8")
+    assert_attention_close(got, ref, f"NaN {dtype} D={head_dim} G={group} Hkv={Hkv}", nan_aware=True)
+
+
 @pytest.mark.parametrize("ncta", [1, 2, 3, 7, 152, 608, 5000])
 def test_grid_sizes_agree(ncta):
     """Different grids cut the KV differently; the LSE merge makes them agree."""
