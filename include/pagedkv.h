@@ -122,7 +122,9 @@ PKV_API pkv_status pkv_paged_kv_append(const pkv_cache* cache, const void* k_new
  * Workspace for pkv_paged_attention, in bytes.  The workspace holds the
  * device error word, one merge ticket per (sequence, kv-head) and the split
  * partial results.  It must be zeroed once before first use
- * (pkv_workspace_init); the kernels leave it ready for the next call.
+ * (pkv_workspace_init); a call that completes leaves it ready for the next
+ * call.  A call that reports PKV_ERR_TIMEOUT (pkv_read_device_error) may have
+ * left merge tickets set: zero the workspace again before reusing it.
  * num_ctas = 0 means the library's default grid for the current device.
  */
 PKV_API size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
@@ -159,11 +161,35 @@ PKV_API pkv_status pkv_workspace_init(void* workspace, size_t workspace_bytes, v
  *   workspace      device, >= pkv_attention_workspace_size(...) bytes, zeroed
  *                  once by pkv_workspace_init; not shared by concurrent calls.
  *
- * Supported: block_size 16, head_dim 64 or 128, Hq % Hkv == 0,
- * (Hq / Hkv) * max_q_len <= 32, max_blocks_per_seq * Hkv < 2^20 (contexts
- * below 2^24 / Hkv tokens); otherwise PKV_ERR_UNSUPPORTED, nothing launched.
+ * Supported: block_size 16, head_dim 64 or 128, Hq % Hkv == 0 (any GQA
+ * group G = Hq / Hkv), max_q_len <= 16, and max_blocks_per_seq * Hkv * S <
+ * 2^20 (contexts below 2^24 / (Hkv * S) tokens) where S is the smallest
+ * divisor of G with (G / S) * max_q_len <= 32; otherwise PKV_ERR_UNSUPPORTED,
+ * nothing launched.  When G * max_q_len > 32 (a wide group verifying a
+ * window), a kv-head's G query heads are processed as S consecutive groups
+ * of G / S heads; each reads the kv-head's pages (the repeat reads mostly
+ * hit L2).
  * Results are deterministic and depend only
  * on logical positions (not on which physical blocks hold them).
+ *
+ * NaN in the cache: a NaN stored in K makes every element of the rows that
+ * see it NaN, and a NaN in V the matching dimension of those rows, as in the
+ * definition.  One departure: inside a causal window (q_len > 1), a NaN in
+ * the V row of a window token also reaches the window's earlier queries that
+ * do not see that token (their zero weights multiply it in the same
+ * tensor-core product), unless none of the tokens of that part of the
+ * sequence is visible to them.
+ *
+ * Launch (programmatic dependent launch).  When the previous kernel on
+ * `stream` lets its dependents start early -- pkv_paged_kv_append does -- this
+ * kernel's set-up, which reads context_lens, q_lens, block_tables and q,
+ * overlaps that kernel; its K/V reads and its workspace accesses wait until
+ * that kernel has completed.  So a kernel that lets its dependents start
+ * early must not write those four inputs.  This kernel lets the next kernel
+ * on the stream launch at once; a kernel launched for programmatic
+ * dependence must wait for its prerequisites (griddepcontrol.wait) before
+ * reading `out` or the workspace.  Kernels launched the ordinary way see
+ * the usual stream order.
  */
 PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, int32_t num_q_heads,
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -187,11 +213,14 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
  * cudaMalloc, cudaFree or allocating library call.
  *
  *   device_error   optional device int32 error word that receives the
- *                  PKV_DEVERR_* bits (NULL: errors are not reported).
+ *                  PKV_DEVERR_* bits.  NULL: device-side errors (a bad block
+ *                  id, a bad length, a wait that ran out) are not reported
+ *                  at all and the output is unspecified.
  *
  * The first call on a device looks up the array's device address with that
  * device current and caches it; make that first call before any stream
- * capture.  Each call clears the array's error word and merge tickets on
+ * capture, and do not reset the device (cudaDeviceReset) between calls: the
+ * cached address would then be stale.  Each call clears the array's error word and merge tickets on
  * `stream` before launching.  All calls share the one array and it keeps the
  * last call's contents, so calls whose kernels overlap on the GPU (other
  * streams or other host threads on the same device) race: serialise them.
@@ -213,6 +242,19 @@ PKV_API pkv_status pkv_paged_attention_noalloc(const pkv_cache* cache, const voi
  * PKV_ERR_DEVICE_INDEX.  For tests and debugging, not the hot path.
  */
 PKV_API pkv_status pkv_read_device_error(void* error_word, int32_t* code, void* stream);
+
+/*
+ * For tests of the device-side timeout path only (the pages have no
+ * counterpart).  Every bounded wait inside the tensor-core attention kernel
+ * (mbarrier phases, merge tickets) gives up after limit_ns nanoseconds
+ * (0 restores the default, 2 s), sets PKV_DEVERR_TIMEOUT and winds the CTA
+ * down.  A non-NULL hold_flag (device int32) makes the kernel wait for
+ * *hold_flag != 0 before its first K/V copy: a flag that nothing sets makes
+ * that wait run out.  The settings are process-wide and apply to every
+ * later pkv_paged_attention(_noalloc) launch (not to the CUDA-core kernel,
+ * which has no waits) until they are set again; not for concurrent use.
+ */
+PKV_API void pkv_debug_set_wait_limit(uint64_t limit_ns, const int32_t* hold_flag);
 
 /* Static description of a status code. */
 PKV_API const char* pkv_status_string(pkv_status status);

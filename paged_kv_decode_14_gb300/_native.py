@@ -63,6 +63,8 @@ def lib():
             L.pkv_paged_attention_noalloc.restype = c.c_int
             L.pkv_paged_attention_noalloc.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, i32, vp, vp, i32, i32,
                                                       c.c_float, vp, i32, vp, vp]
+            L.pkv_debug_set_wait_limit.restype = None
+            L.pkv_debug_set_wait_limit.argtypes = [c.c_uint64, vp]
             L.pkv_read_device_error.restype = c.c_int
             L.pkv_read_device_error.argtypes = [vp, c.POINTER(i32), vp]
             L.pkv_status_string.restype = c.c_char_p
@@ -147,6 +149,11 @@ def make_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_q_len, num
     return ws
 
 
+def workspace_init(workspace, stream=None):
+    """pkv_workspace_init: zero a workspace (needed once, and after a timeout)."""
+    _check(lib().pkv_workspace_init(_ptr(workspace), int(workspace.numel()), _stream(stream)), "pkv_workspace_init")
+
+
 def attention(cache: PagedKVCache, q, block_tables, context_lens, q_lens, max_q_len: int, scale: float,
               workspace, out=None, num_ctas: int = 0, stream=None):
     """pkv_paged_attention: q bf16 [sum q_lens, Hq, D] -> out bf16 of the same shape."""
@@ -194,6 +201,13 @@ def read_device_error(error_word, stream=None) -> int:
     if st not in (0, 5, 6):
         _check(st, "pkv_read_device_error")
     return int(code.value)
+
+
+def debug_set_wait_limit(limit_ns: int = 0, hold_flag=None):
+    """Test hook of the timeout path (pkv_debug_set_wait_limit): the wait
+    limit of later attention launches (0 = the default 2 s) and an optional
+    device int32 flag the kernel waits on before its first K/V copy."""
+    lib().pkv_debug_set_wait_limit(int(limit_ns), _ptr(hold_flag))
 
 
 def version() -> str:

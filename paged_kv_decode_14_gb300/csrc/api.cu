@@ -1,5 +1,6 @@
 // C ABI of libpagedkv: argument checks, grid planning and kernel dispatch.
 // Declarations and contracts: include/pagedkv.h.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -12,24 +13,40 @@ cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int
 int simt_rows_pad(int rows);
 int tc_heads_per_segment(int num_kv_heads, int rows);
 
-// Kernel choice and grid for one attention call: the tensor-core kernel for
-// bf16 caches with R = G * max_q_len <= 32 and for FP8 caches with head_dim
-// 128 and R <= 8 (one persistent CTA per SM, all of its ~227 KiB of shared
-// memory), else the CUDA-core kernel (4 CTAs per SM).  rows_pad: partial-slot
-// rows (the tensor-core kernel keeps up to 32 columns of several kv-heads per
-// segment).
-AttnLaunch plan_attention(const pkv_cache* c, int group, int max_q_len, int num_ctas, int num_sms) {
+// Kernel choice and grid for one attention call, in virtual kv-heads (vheads
+// of group vgroup; kv_split of them per cache kv-head): the tensor-core
+// kernel for bf16 caches (R = vgroup * max_q_len <= 32 always) and for FP8
+// caches with head_dim 128 and R <= 8 (one persistent CTA per SM, all of its
+// ~227 KiB of shared memory), else the CUDA-core kernel (4 CTAs per SM).
+// rows_pad: partial-slot rows (the tensor-core kernel keeps up to 32 columns
+// of several kv-heads per segment).  Virtual kv-heads that share cache pages
+// are never grouped in one segment (its pages are copied as one run).
+AttnLaunch plan_attention(const pkv_cache* c, int vgroup, int vheads, int kv_split, int max_q_len, int num_ctas,
+                          int num_sms) {
     AttnLaunch L;
-    const int rows = group * max_q_len;
+    const int rows = vgroup * max_q_len;
     L.tc = c->kv_dtype == PKV_KV_BF16 ? rows <= 32 : (c->head_dim == 128 && rows <= 8);
     L.ncta = num_ctas > 0 ? num_ctas : (L.tc ? num_sms : 4 * num_sms);
     L.rows_pad = L.tc ? 32 : simt_rows_pad(rows);
-    L.hg = L.tc ? tc_heads_per_segment(c->num_kv_heads, rows) : 1;
+    L.hg = (L.tc && kv_split == 1) ? tc_heads_per_segment(vheads, rows) : 1;
     return L;
 }
 
 cudaError_t launch_attention(const AttnLaunch& L, const AttnParams& p, int head_dim, int elem_bytes, cudaStream_t st) {
     return L.tc ? launch_attention_tc(p, head_dim, elem_bytes == 1, L.ncta, st) : launch_attention_simt(p, head_dim, elem_bytes, L.ncta, st);
+}
+
+// Debug settings of the timeout path (pkv_debug_set_wait_limit).
+namespace {
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // 2 s
+std::atomic<uint64_t> g_wait_limit_ns{0};
+std::atomic<const int*> g_hold{nullptr};
+}  // namespace
+
+void fill_debug(AttnParams& p) {
+    const uint64_t lim = g_wait_limit_ns.load(std::memory_order_relaxed);
+    p.wait_limit_ns = lim ? lim : kDefaultWaitLimitNs;
+    p.hold = g_hold.load(std::memory_order_relaxed);
 }
 
 namespace {
@@ -68,6 +85,67 @@ pkv_status check_cache(const pkv_cache* c) {
 int default_ctas(int num_sms) { return 4 * num_sms; }
 
 }  // namespace
+
+// Argument checks, virtual kv-heads, kernel choice and parameters of one
+// attention call, shared by pkv_paged_attention and
+// pkv_paged_attention_noalloc.  On PKV_OK with *empty false, *p is complete
+// except for its workspace pointers (err, tickets, partials), which follow
+// the layout *wl.  *empty: no sequences, nothing to launch.
+pkv_status attention_setup(const pkv_cache* cache, const void* q, int num_q_heads, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens, const int32_t* q_lens, int num_seqs,
+                           int max_q_len, float scale, void* out, int num_ctas, int num_sms, AttnParams* p,
+                           AttnLaunch* L, WorkspaceLayout* wl, bool* empty) {
+    *empty = false;
+    pkv_status s = check_cache(cache);
+    if (s != PKV_OK) return s;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) {
+        *empty = true;
+        return PKV_OK;
+    }
+    if (!q || !out || !block_tables || !context_lens || !q_lens) return PKV_ERR_INVALID_ARG;
+    if (max_blocks_per_seq <= 0 || max_q_len < 1 || num_ctas < 0) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+    if (max_q_len > 16) return PKV_ERR_UNSUPPORTED;
+    const int group = num_q_heads / cache->num_kv_heads;
+    const int ks = kv_split_for(group, max_q_len);
+    const int vgroup = group / ks, vheads = cache->num_kv_heads * ks;
+    if ((int64_t)max_blocks_per_seq * vheads >= (1 << 20)) return PKV_ERR_UNSUPPORTED;   // unit indices stay below 2^20
+    if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+    if (num_sms <= 0) return PKV_ERR_CUDA;
+    *L = plan_attention(cache, vgroup, vheads, ks, max_q_len, num_ctas, num_sms);
+    *wl = workspace_layout(num_seqs, vheads, cache->head_dim, L->rows_pad, L->ncta);
+
+    p->k_cache = (const uint8_t*)cache->k_cache;
+    p->v_cache = (const uint8_t*)cache->v_cache;
+    p->k_scales = cache->k_scales;
+    p->v_scales = cache->v_scales;
+    p->q = (const __nv_bfloat16*)q;
+    p->out = (__nv_bfloat16*)out;
+    p->block_tables = block_tables;
+    p->context_lens = context_lens;
+    p->q_lens = q_lens;
+    p->err = nullptr;
+    p->tickets = nullptr;
+    p->partials = nullptr;
+    p->num_blocks = cache->num_blocks;
+    p->num_seqs = num_seqs;
+    p->num_q_heads = num_q_heads;
+    p->num_kv_heads = vheads;
+    p->group = vgroup;
+    p->max_blocks_per_seq = max_blocks_per_seq;
+    p->max_q_len = max_q_len;
+    p->rows = vgroup * max_q_len;
+    p->rows_pad = L->rows_pad;
+    p->slot_floats = (int)wl->slot_floats;
+    p->scale_log2 = scale * kLog2e;
+    p->hg = L->hg;
+    p->kv_split = ks;
+    p->cache_kv_heads = cache->num_kv_heads;
+    fill_debug(*p);
+    return PKV_OK;
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -111,8 +189,9 @@ PKV_API size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_q_head
     if (head_dim <= 0 || max_q_len < 1) return 0;
     if (num_ctas <= 0) num_ctas = default_ctas(num_sms_current());
     if (num_ctas <= 0) return 0;
-    const int rows_pad = max(32, simt_rows_pad((num_q_heads / num_kv_heads) * max_q_len));
-    return workspace_layout(num_seqs, num_kv_heads, head_dim, rows_pad, num_ctas).total;
+    const int group = num_q_heads / num_kv_heads, ks = kv_split_for(group, max_q_len);
+    const int rows_pad = max(32, simt_rows_pad((group / ks) * max_q_len));
+    return workspace_layout(num_seqs, num_kv_heads * ks, head_dim, rows_pad, num_ctas).total;
 }
 
 PKV_API pkv_status pkv_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -126,52 +205,28 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
                                        const int32_t* context_lens, const int32_t* q_lens, int32_t num_seqs,
                                        int32_t max_q_len, float scale, void* out, void* workspace,
                                        size_t workspace_bytes, int32_t num_ctas, void* stream) {
-    pkv_status s = check_cache(cache);
-    if (s != PKV_OK) return s;
-    if (num_seqs < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
-    if (num_seqs == 0) return PKV_OK;
-    if (!q || !out || !block_tables || !context_lens || !q_lens || !workspace) return PKV_ERR_INVALID_ARG;
-    if (max_blocks_per_seq <= 0 || max_q_len < 1) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return PKV_ERR_INVALID_ARG;
-    const int group = num_q_heads / cache->num_kv_heads;
-    if (max_q_len > 16 || group * max_q_len > 32) return PKV_ERR_UNSUPPORTED;
-    if ((int64_t)max_blocks_per_seq * cache->num_kv_heads >= (1 << 20)) return PKV_ERR_UNSUPPORTED;   // unit indices stay below 2^20
-    if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
-    const int sms = num_sms_current();
-    if (sms <= 0) return PKV_ERR_CUDA;
-    if (num_ctas < 0) return PKV_ERR_INVALID_ARG;
-    const AttnLaunch L = plan_attention(cache, group, max_q_len, num_ctas, sms);
-    const WorkspaceLayout wl = workspace_layout(num_seqs, cache->num_kv_heads, cache->head_dim, L.rows_pad, L.ncta);
-    if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
-
     AttnParams p;
-    p.k_cache = (const uint8_t*)cache->k_cache;
-    p.v_cache = (const uint8_t*)cache->v_cache;
-    p.k_scales = cache->k_scales;
-    p.v_scales = cache->v_scales;
-    p.q = (const __nv_bfloat16*)q;
-    p.out = (__nv_bfloat16*)out;
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    p.q_lens = q_lens;
+    AttnLaunch L;
+    WorkspaceLayout wl;
+    bool empty = false;
+    const pkv_status s = attention_setup(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, q_lens,
+                                         num_seqs, max_q_len, scale, out, num_ctas, num_sms_current(), &p, &L, &wl,
+                                         &empty);
+    if (s != PKV_OK || empty) return s;
+    if (!workspace) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+    if (workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
     p.err = (int*)workspace;
     p.tickets = (int*)((uint8_t*)workspace + wl.tickets_off);
     p.partials = (float*)((uint8_t*)workspace + wl.partials_off);
-    p.num_blocks = cache->num_blocks;
-    p.num_seqs = num_seqs;
-    p.num_q_heads = num_q_heads;
-    p.num_kv_heads = cache->num_kv_heads;
-    p.group = group;
-    p.max_blocks_per_seq = max_blocks_per_seq;
-    p.max_q_len = max_q_len;
-    p.rows = group * max_q_len;
-    p.rows_pad = L.rows_pad;
-    p.slot_floats = (int)wl.slot_floats;
-    p.scale_log2 = scale * kLog2e;
-    p.hg = L.hg;
     const int E = cache->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
     cudaError_t e = launch_attention(L, p, cache->head_dim, E, (cudaStream_t)stream);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+PKV_API void pkv_debug_set_wait_limit(uint64_t limit_ns, const int32_t* hold_flag) {
+    g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    g_hold.store(hold_flag, std::memory_order_relaxed);
 }
 
 PKV_API pkv_status pkv_read_device_error(void* error_word, int32_t* code, void* stream) {

@@ -20,7 +20,10 @@
 #include "common.cuh"
 
 namespace pkv {
-AttnLaunch plan_attention(const pkv_cache* c, int group, int max_q_len, int num_ctas, int num_sms);
+pkv_status attention_setup(const pkv_cache* cache, const void* q, int num_q_heads, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens, const int32_t* q_lens, int num_seqs,
+                           int max_q_len, float scale, void* out, int num_ctas, int num_sms, AttnParams* p,
+                           AttnLaunch* L, WorkspaceLayout* wl, bool* empty);
 cudaError_t launch_attention(const AttnLaunch& L, const AttnParams& p, int head_dim, int elem_bytes, cudaStream_t st);
 }  // namespace pkv
 
@@ -54,8 +57,6 @@ pkv_status device_setup(void** scratch, int* sms) {
     return PKV_OK;
 }
 
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
 }  // namespace
 
 using namespace pkv;
@@ -64,59 +65,26 @@ extern "C" PKV_API pkv_status pkv_paged_attention_noalloc(
     const pkv_cache* c, const void* q, int32_t num_q_heads, const int32_t* block_tables,
     int32_t max_blocks_per_seq, const int32_t* context_lens, const int32_t* q_lens, int32_t num_seqs,
     int32_t max_q_len, float scale, void* out, int32_t num_ctas, int32_t* device_error, void* stream) {
-    // the same argument checks as pkv_paged_attention
-    if (!c || !c->k_cache || !c->v_cache || c->num_blocks <= 0 || c->num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
-    if (c->block_size != kBlock || (c->head_dim != 64 && c->head_dim != 128)) return PKV_ERR_UNSUPPORTED;
-    if (c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
-    if (c->kv_dtype == PKV_KV_FP8_E4M3 && (!c->k_scales || !c->v_scales)) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(c->k_cache) || !aligned16(c->v_cache)) return PKV_ERR_INVALID_ARG;
-    if (num_seqs < 0 || num_q_heads <= 0 || num_q_heads % c->num_kv_heads) return PKV_ERR_INVALID_ARG;
-    if (num_seqs == 0) return PKV_OK;
-    if (!q || !out || !block_tables || !context_lens || !q_lens) return PKV_ERR_INVALID_ARG;
-    if (max_blocks_per_seq <= 0 || max_q_len < 1 || num_ctas < 0) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
-    const int group = num_q_heads / c->num_kv_heads;
-    if (max_q_len > 16 || group * max_q_len > 32) return PKV_ERR_UNSUPPORTED;
-    if ((int64_t)max_blocks_per_seq * c->num_kv_heads >= (1 << 20)) return PKV_ERR_UNSUPPORTED;   // unit indices stay below 2^20
-    if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
-
+    // the same argument checks and parameters as pkv_paged_attention
     void* scratch = nullptr;
     int sms = 0;
+    AttnParams p;
+    AttnLaunch L;
+    WorkspaceLayout wl;
+    bool empty = false;
     pkv_status s = device_setup(&scratch, &sms);
     if (s != PKV_OK) return s;
-    const AttnLaunch L = plan_attention(c, group, max_q_len, num_ctas, sms);
-    const WorkspaceLayout wl = workspace_layout(num_seqs, c->num_kv_heads, c->head_dim, L.rows_pad, L.ncta);
+    s = pkv::attention_setup(c, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, q_lens, num_seqs,
+                             max_q_len, scale, out, num_ctas, sms, &p, &L, &wl, &empty);
+    if (s != PKV_OK || empty) return s;
     if (wl.total > (size_t)PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;   // beyond the fixed maximum
 
     cudaStream_t st = (cudaStream_t)stream;
     // The error word and the merge tickets must start at zero; the partials need not.
     if (cudaMemsetAsync(scratch, 0, wl.partials_off, st) != cudaSuccess) return PKV_ERR_CUDA;
-
-    AttnParams p;
-    p.k_cache = (const uint8_t*)c->k_cache;
-    p.v_cache = (const uint8_t*)c->v_cache;
-    p.k_scales = c->k_scales;
-    p.v_scales = c->v_scales;
-    p.q = (const __nv_bfloat16*)q;
-    p.out = (__nv_bfloat16*)out;
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    p.q_lens = q_lens;
     p.err = device_error ? (int*)device_error : (int*)scratch;
     p.tickets = (int*)((uint8_t*)scratch + wl.tickets_off);
     p.partials = (float*)((uint8_t*)scratch + wl.partials_off);
-    p.num_blocks = c->num_blocks;
-    p.num_seqs = num_seqs;
-    p.num_q_heads = num_q_heads;
-    p.num_kv_heads = c->num_kv_heads;
-    p.group = group;
-    p.max_blocks_per_seq = max_blocks_per_seq;
-    p.max_q_len = max_q_len;
-    p.rows = group * max_q_len;
-    p.rows_pad = L.rows_pad;
-    p.slot_floats = (int)wl.slot_floats;
-    p.scale_log2 = scale * kLog2e;
-    p.hg = L.hg;
     const int E = c->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
     return launch_attention(L, p, c->head_dim, E, st) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

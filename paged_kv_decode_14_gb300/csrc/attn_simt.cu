@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
                     raise_error(p.err, PKV_DEVERR_BLOCK_ID);
                     blk = 0;
                 }
-                const size_t page_off = ((size_t)blk * Hkv + g) * K::PAGE;
+                const size_t page_off = ((size_t)blk * p.cache_kv_heads + cache_head(p, g)) * K::PAGE;
                 uint8_t* dk = wpages + buf * 2 * K::PAGE;
                 uint8_t* dv = dk + K::PAGE;
 #pragma unroll
@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(const AttnParams p)
                 const int blk = (blk_raw < 0 || blk_raw >= p.num_blocks) ? 0 : blk_raw;
                 float ksc = p.scale_log2, vsc = 1.f;
                 if constexpr (E == 1) {
-                    ksc *= p.k_scales[(size_t)blk * Hkv + g];
-                    vsc = p.v_scales[(size_t)blk * Hkv + g];
+                    ksc *= p.k_scales[(size_t)blk * p.cache_kv_heads + cache_head(p, g)];
+                    vsc = p.v_scales[(size_t)blk * p.cache_kv_heads + cache_head(p, g)];
                 }
                 const int tok0 = (pg0 + lp) * kBlock;
 

@@ -74,7 +74,6 @@ using namespace ptx;
 constexpr int kTP = 8;                        // units (pages of one kv-head) per tile
 constexpr int kTileTok = kTP * kBlock;        // 128 token rows = MMA M
 constexpr int kSoftThreads = 128;             // one warpgroup (the 128 TMEM lanes)
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxSmem = 232448;
 constexpr int NSB = 4;                        // S^T / P ring depth (tiles the MMA may run ahead)
 // warps 0-3 softmax; 4 producer, 5 S^T issuer, 6 merge, 7 P.V issuer; with
@@ -169,18 +168,21 @@ struct PieceDesc {
 struct Ctl {
     volatile int* abort;
     int* err;
+    uint64_t limit_ns;     // the launch's wait limit (AttnParams::wait_limit_ns)
 };
 
-// Bounded wait: spins on try_wait; gives up after kWaitLimitNs or once the
-// CTA's abort flag is set.  A timeout raises PKV_DEVERR_TIMEOUT and the flag.
-// The spin loop is out of line: only the first try sits in the callers' code.
-__device__ __noinline__ bool wait_bar_spin(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
+// Bounded wait: spins on try_wait; gives up after the launch's wait limit or
+// once the CTA's abort flag is set.  A timeout raises PKV_DEVERR_TIMEOUT and
+// the flag.  The spin loop is out of line: only the first try sits in the
+// callers' code.
+__device__ __noinline__ bool wait_bar_spin(uint32_t bar, uint32_t parity, volatile int* abort, int* err,
+                                           uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 raise_error(err, PKV_DEVERR_TIMEOUT);
                 *abort = 1;
                 return false;
@@ -190,7 +192,7 @@ __device__ __noinline__ bool wait_bar_spin(uint32_t bar, uint32_t parity, volati
 }
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_bar_spin(bar, parity, c.abort, c.err);
+    return wait_bar_spin(bar, parity, c.abort, c.err, c.limit_ns);
 }
 
 // 2^x by the SFU (flushes subnormal results to zero, 2^-inf = 0).
@@ -431,8 +433,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     float* lred = reinterpret_cast<float*>(smem + K::OFF_LRED);   // [2][4][RMAX]
     float* emref = reinterpret_cast<float*>(smem + K::OFF_EM);    // [2][RMAX]
     int* pdesc = reinterpret_cast<int*>(smem + K::OFF_PD);        // [2][8]
-    const Ctl ctl{abort_flag, p.err};
-    const Ctl drain{never, p.err};      // bounded waits that ignore the abort flag
+    const Ctl ctl{abort_flag, p.err, p.wait_limit_ns};
+    const Ctl drain{never, p.err, p.wait_limit_ns};      // bounded waits that ignore the abort flag
 
     // Q buffers start zeroed: rows past a piece's columns are never written
     // and only feed S^T columns the softmax ignores.
@@ -584,7 +586,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 if (gs == 1) {
                     const uint64_t g0 = globaltimer_ns();
                     while ((gs = *gstate) == 1 && !*abort_flag) {
-                        if (globaltimer_ns() - g0 > kWaitLimitNs) {
+                        if (globaltimer_ns() - g0 > p.wait_limit_ns) {
                             raise_error(p.err, PKV_DEVERR_TIMEOUT);
                             *abort_flag = 1;
                         }
@@ -786,6 +788,28 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             win = load_win(it, div_small(it.pg0, HG));
         }
         griddep_wait();                   // K/V pages the previous kernel wrote are visible from here
+        if (p.hold != nullptr && it.valid()) {
+            // (tests of the timeout path only) wait, bounded, for a flag; nothing sets the
+            // flag the tests pass, so the wait runs out and every role winds down
+            bool w = true;
+            if (lane == 0) {
+                const uint64_t h0 = globaltimer_ns();
+                while (*reinterpret_cast<const volatile int*>(p.hold) == 0) {
+                    if (*abort_flag) {
+                        w = false;
+                        break;
+                    }
+                    if (globaltimer_ns() - h0 > p.wait_limit_ns) {
+                        raise_error(p.err, PKV_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                        w = false;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, w, 0);
+        }
         while (ok && it.valid()) {
             PieceIter nx = it;
             uint4 qn[kQAhead ? QV : 1];
@@ -818,7 +842,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     blk = 0;
                 }
                 const int qh = qu - qpg * HG;                         // the unit's head within the group
-                const size_t unit = (size_t)blk * Hkv + it.hg * HG + qh;
+                const size_t unit = (size_t)blk * p.cache_kv_heads + cache_head(p, it.hg * HG + qh);
                 const size_t off = unit * (FP8 ? K::PAGE8 : K::PAGE);
                 // K and V of the tile in one pass: lanes 0-7 copy K, lanes 8-15 V (unit slot
                 // lane & 7).  One bulk copy per page: the group's heads of a block are adjacent
@@ -1104,7 +1128,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 const uint64_t t0 = globaltimer_ns();
                 // (relaxed polls, one acquire fence once the count is reached: an acquire
                 // per poll would slow the rest of the SM)
-                while (*gstate == 0 && !*abort_flag && globaltimer_ns() - t0 < kWaitLimitNs) {
+                while (*gstate == 0 && !*abort_flag && globaltimer_ns() - t0 < p.wait_limit_ns) {
                     int v = 0;
                     if (lane == 0) {
                         v = ld_relaxed_gpu(ticket);
@@ -1472,11 +1496,11 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     if (did) {
                         t_prog = globaltimer_ns();
                     } else {
-                        // nothing ready: give up on an abort, or after kWaitLimitNs without progress
+                        // nothing ready: give up on an abort, or after the wait limit without progress
                         bool stuck = false;
                         if (tt == 0) {
                             stuck = *abort_flag != 0;
-                            if (!stuck && globaltimer_ns() - t_prog > kWaitLimitNs) {
+                            if (!stuck && globaltimer_ns() - t_prog > p.wait_limit_ns) {
                                 raise_error(p.err, PKV_DEVERR_TIMEOUT);
                                 *abort_flag = 1;
                                 stuck = true;

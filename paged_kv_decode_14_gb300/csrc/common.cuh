@@ -145,7 +145,31 @@ struct AttnParams {
     int slot_floats;
     float scale_log2;          // scale * log2(e)
     int hg;                    // kv-heads per segment (tensor-core kernel; 1 elsewhere)
+    uint64_t wait_limit_ns;    // every bounded wait of the tensor-core kernel gives up after this
+    const int* hold;           // tests of the timeout path only: wait for *hold != 0 first (nullptr: no wait)
+    // num_kv_heads and group above count virtual kv-heads: when a kv-head's
+    // query rows (G * max_q_len) exceed the 32 columns a segment holds, its G
+    // query heads are split into kv_split consecutive groups, each a virtual
+    // kv-head (so query head h still reads virtual head h / group) that reads
+    // the pages of cache kv-head (virtual head) / kv_split.
+    int kv_split;
+    int cache_kv_heads;        // kv-heads of the cache (num_kv_heads / kv_split)
 };
+
+// Virtual kv-heads per cache kv-head: the smallest divisor of the GQA group
+// that leaves at most 32 query rows per virtual head.
+__host__ inline int kv_split_for(int group, int max_q_len) {
+    for (int ks = 1; ks < group; ++ks)
+        if (group % ks == 0 && (group / ks) * max_q_len <= 32) return ks;
+    return group;
+}
+
+// Cache kv-head of virtual kv-head vh.
+__device__ __forceinline__ int cache_head(const AttnParams& p, int vh);
+
+// The wait limit and hold flag of the next launches (pkv_debug_set_wait_limit),
+// copied into AttnParams by both attention entry points.
+void fill_debug(AttnParams& p);
 
 // Kernel choice and grid of one attention call (see plan_attention in api.cu).
 struct AttnLaunch {
@@ -177,6 +201,10 @@ __device__ __forceinline__ int floor_div_small(long long num, int den) {
 // right side for numerators this small.
 __device__ __forceinline__ int div_small(int n, int d) {
     return (int)__fdividef((float)n + 0.5f, (float)d);
+}
+
+__device__ __forceinline__ int cache_head(const AttnParams& p, int vh) {
+    return p.kv_split == 1 ? vh : div_small(vh, p.kv_split);
 }
 
 // CTAs that take part: enough that every one gets at least kMinUnitsPerCta

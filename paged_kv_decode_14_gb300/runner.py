@@ -107,5 +107,10 @@ class DeviceWorkload:
         return k, v
 
     def errors(self):
-        """(attention workspace error bits, append error bits); clears both."""
-        return nat.read_device_error(self.workspace), nat.read_device_error(self.append_err)
+        """(attention workspace error bits, append error bits); clears both.
+        After a timeout the workspace may hold merge tickets of the aborted
+        call: it is zeroed again, ready for the next call."""
+        a = nat.read_device_error(self.workspace)
+        if a & nat.DEVERR_TIMEOUT:
+            nat.workspace_init(self.workspace)
+        return a, nat.read_device_error(self.append_err)

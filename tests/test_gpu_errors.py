@@ -88,3 +88,32 @@ def test_empty_batch_is_noop():
     assert out.shape == (0, 8, 64)
     nat.append(c, q[:, :2].contiguous(), q[:, :2].contiguous(), torch.zeros(0, dtype=torch.int64, device="cuda"))
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_wait_timeout_reports_and_recovers(dtype):
+    """The device timeout path, made to run out without a fault: a wait
+    limit of 200 us and a hold flag that nothing sets.  The producer's bounded
+    wait on the flag gives up, raises PKV_DEVERR_TIMEOUT and the abort flag,
+    and every role of every CTA winds down (no copy in flight, TMEM freed):
+    the call returns and the context stays usable.  After the workspace is
+    zeroed again the same workspace gives oracle parity."""
+    w = wl.make_workload("to", context_lens=[300, 77, 1000, 40], q_lens=[1, 1, 1, 1], num_q_heads=32,
+                         num_kv_heads=8, head_dim=128, kv_dtype=dtype, seed=95)
+    dw = DeviceWorkload(w)
+    dw.prefill()
+    dw.append_step()
+    hold = torch.zeros(1, dtype=torch.int32, device="cuda")
+    try:
+        nat.debug_set_wait_limit(200_000, hold)
+        dw.attend()
+        torch.cuda.synchronize()
+    finally:
+        nat.debug_set_wait_limit(0, None)
+    assert nat.read_device_error(dw.workspace) == nat.DEVERR_TIMEOUT
+    nat.workspace_init(dw.workspace)
+    out = dw.attend()
+    kc, vc = oracle.build_cache(w)
+    ref, _ = oracle.attend(w, kc, vc)
+    assert_attention_close(out_bits(out), ref, "after a timeout")
+    assert dw.errors() == (0, 0)

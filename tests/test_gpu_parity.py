@@ -61,6 +61,9 @@ SWEEP = [
     (64, 8, 2, [1, 15, 16, 17, 31, 32, 33, 100], [1] * 8, "bf16"),
     (128, 8, 8, [1, 15, 16, 17, 64, 257], [1] * 6, "bf16"),
     (128, 8, 2, [5, 40, 77, 300], [5, 3, 8, 2], "bf16"),
+    (128, 16, 2, [5, 40, 77, 300], [5, 3, 8, 2], "bf16"),  # G = 8, R up to 64: two virtual kv-heads per kv-head
+    (64, 32, 2, [9, 130, 33], [4, 2, 3], "bf16"),          # G = 16, R up to 64
+    (128, 32, 4, [20, 300], [5, 2], "fp8"),                # FP8, G = 8, R = 40 (CUDA-core kernel)
     (64, 4, 4, [9, 10, 11], [8, 4, 2], "bf16"),
     (128, 32, 8, [600, 3, 1200], [1, 1, 1], "fp8"),
     (64, 8, 1, [33, 17, 129], [4, 1, 2], "fp8"),
@@ -92,6 +95,21 @@ def test_sweep(case):
         gk, gv = dw.cache_bytes()
         assert caches_equal(gk, kc, dt == "fp8") and caches_equal(gv, vc, dt == "fp8")
         assert_attention_close(got, ref, f"sweep {case} ncta {ncta}")
+
+
+def test_verify_g8_q5_full_size():
+    """A 64 / 8-head model verifying 5 draft tokens on the verify batch's shape
+    (32 sequences, lengths U[512, 4096]): R = G * Q = 40 rows per kv-head, so
+    each kv-head's 8 query heads run as two virtual groups of 4."""
+    rng = np.random.Generator(np.random.PCG64(1004))
+    L = rng.integers(512, 4097, size=32).astype(np.int32)
+    w = wl.make_workload("verify_g8", context_lens=L, q_lens=np.full(32, 5, np.int32), num_q_heads=64,
+                         num_kv_heads=8, head_dim=128, seed=104)
+    kc, vc = oracle.build_cache(w)
+    ref, _ = oracle.attend(w, kc, vc)
+    dw, got = run_gpu(w)
+    assert_attention_close(got, ref, "verify G=8 Q=5")
+    assert dw.errors() == (0, 0)
 
 
 def test_fp8_subnormal_codes():
