@@ -202,12 +202,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// OR of v over the n threads of named barrier `id` (non-.aligned, like
-// named_bar_sync).
+// OR of v over the n threads of named barrier `id` (one role, uniform
+// control flow: the .aligned form, like named_bar_sync).
 __device__ __forceinline__ bool bar_red_or(int id, int n, bool v) {
     uint32_t r;
     asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbarrier.red.or.pred p, %2, %3, q;\nselp.u32 %0, 1, 0, p;\n}\n"
+        "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbar.red.or.pred p, %2, %3, q;\nselp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(r)
         : "r"((uint32_t)v), "r"(id), "r"(n)
         : "memory");
@@ -255,8 +255,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // low exponent bits and the top mantissa bits of a bf16, which then reads as
 // the code's value times 2^-120 (its bf16 subnormals are the e4m3 subnormals);
 // a bf16x2 multiply by 2^120 restores the value.  The NaN codes (0x7f, 0xff;
-// the append keeps a NaN source value NaN) would come out as +-480 (0x43f0):
-// OR-ing 0x7fc0 into their lanes turns that into a bf16 NaN of the same sign.
+// the append keeps a NaN source value NaN) come out as +-480 (magnitude
+// 0x43f0), a value no finite code reaches (the largest is 448): see
+// fix_nan_lanes.
 __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
     const uint32_t hb = ((w >> 4) & 0x07070707u) | (w & 0x80808080u);   // per byte: sign, 3 high exponent bits
     const uint32_t lb = (w << 4) & 0xF0F0F0F0u;                          // per byte: low exponent bit, mantissa
@@ -264,10 +265,27 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
     const __nv_bfloat162 k2 = __halves2bfloat162(__ushort_as_bfloat16(0x7B80), __ushort_as_bfloat16(0x7B80));
     const __nv_bfloat162 ra = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), k2);
     const __nv_bfloat162 rb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), k2);
-    const uint32_t nan = __vcmpeq4(w & 0x7F7F7F7Fu, 0x7F7F7F7Fu);        // 0xff in the bytes holding a NaN code
-    lo = *reinterpret_cast<const uint32_t*>(&ra) | (__byte_perm(nan, 0u, 0x1100) & 0x7FC07FC0u);
-    hi = *reinterpret_cast<const uint32_t*>(&rb) | (__byte_perm(nan, 0u, 0x3322) & 0x7FC07FC0u);
+    lo = *reinterpret_cast<const uint32_t*>(&ra);
+    hi = *reinterpret_cast<const uint32_t*>(&rb);
 }
+
+// The rare path of the V widening: turns the +-480 lanes that NaN codes
+// produced in the 16-byte chunk at c into bf16 NaN of the same sign.
+__device__ __forceinline__ void fix_nan_lanes(uint8_t* c) {
+    uint4 w = *reinterpret_cast<const uint4*>(c);
+    uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if ((x[j] & 0x7FFFu) == 0x43F0u) x[j] |= 0x7FC0u;
+        if ((x[j] & 0x7FFF0000u) == 0x43F00000u) x[j] |= 0x7FC00000u;
+    }
+    *reinterpret_cast<uint4*>(c) = make_uint4(x[0], x[1], x[2], x[3]);
+}
+
+// Bit 7 of byte i of the result is set iff byte i of w is an E4M3 NaN code
+// (low seven bits all ones): (b & 0x7f) + 1 reaches 0x80 only for those, and
+// never carries into the next byte.
+__device__ __forceinline__ uint32_t e4m3_nan_bits(uint32_t w) { return (w & 0x7F7F7F7Fu) + 0x01010101u; }
 
 // Pieces of a CTA's unit range [u0, u1), in processing order: the piece
 // holding u1 - 1 first (when it does not start at u0), then [u0, start of
@@ -546,6 +564,13 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         for (int k = 0; k < kTP; ++k)
             v[k] = *reinterpret_cast<const uint4*>(slot + K::OFF_LAND + k * K::PAGE8 + tt * 16);
         named_bar_sync(bid, kSoftThreads);
+        // NaN codes are rare (a NaN value stored in the cache; the unwritten slots of a
+        // sequence's last page may hold anything): a cheap test over the thread's own
+        // chunks, and the exact fix of the chunks it wrote only when it hits
+        uint32_t nb = 0;
+#pragma unroll
+        for (int k = 0; k < kTP; ++k)
+            nb |= e4m3_nan_bits(v[k].x) | e4m3_nan_bits(v[k].y) | e4m3_nan_bits(v[k].z) | e4m3_nan_bits(v[k].w);
         const int r = tt & 7, c = (tt >> 3) % NC16, oh = tt / (8 * NC16);
         uint8_t* d0 = slot + ((oh * (D / 8) + 2 * c) * 8 + r) * 16;
 #pragma unroll
@@ -556,6 +581,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             for (int j = 0; j < 4; ++j) e4m3x4_to_bf16x4(wv[j], o[2 * j], o[2 * j + 1]);
             *reinterpret_cast<uint4*>(d0 + k * K::PAGE) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(d0 + k * K::PAGE + 128) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        if (nb & 0x80808080u) {      // (stale pages past the tile's page count may hit too: harmless)
+#pragma unroll 1
+            for (int i = 0; i < 2 * kTP; ++i) fix_nan_lanes(d0 + (i >> 1) * K::PAGE + (i & 1) * 128);
         }
         fence_proxy_async_smem();             // the MMA reads the slot through the async proxy
     };

@@ -128,14 +128,14 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
-// Named barrier over `threads` threads.  The non-.aligned form: the
-// threads of a warp-specialised kernel may reach a barrier through different
-// code paths (the compiler is free to duplicate a role's tail), which the
-// .aligned form (bar.sync, __syncthreads) leaves undefined.
+// Named barrier over the `threads` threads of one role (a warpgroup), which
+// reach it in uniform control flow: the .aligned form (bar.sync).
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("barrier.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
-// The whole CTA, non-.aligned (see named_bar_sync).
+// The whole CTA, where every role arrives from its own code path: the
+// non-.aligned form.  (With __syncthreads, the .aligned form, thread 0 was
+// traced passing the final barrier while the epilogue warpgroup still ran.)
 __device__ __forceinline__ void cta_bar_sync() { asm volatile("barrier.sync 0;\n" ::: "memory"); }
 
 // ------------------------------------------------------------------ TMEM
