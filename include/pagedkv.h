@@ -74,7 +74,9 @@ typedef enum pkv_status {
     PKV_ERR_WORKSPACE = 3,     /* workspace missing or too small */
     PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
     PKV_ERR_DEVICE_INDEX = 5,  /* device error word: bad block id / slot / length */
-    PKV_ERR_TIMEOUT = 6        /* device error word: a bounded wait gave up */
+    PKV_ERR_TIMEOUT = 6,       /* device error word: a bounded wait gave up */
+    PKV_ERR_NO_BLOCKS = 7,     /* block manager: no free block and none evictable */
+    PKV_ERR_UNKNOWN_SEQ = 8    /* block manager: no sequence with that id (or it exists already) */
 } pkv_status;
 
 typedef enum pkv_kv_dtype { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;

@@ -20,7 +20,8 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "pagedkv.h")
 
 KV_BF16, KV_FP8_E4M3 = 0, 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "workspace missing or too small",
-          4: "CUDA error", 5: "device-side index or length error", 6: "device-side wait timed out"}
+          4: "CUDA error", 5: "device-side index or length error", 6: "device-side wait timed out",
+          7: "no free cache block and none evictable", 8: "unknown (or already registered) sequence id"}
 DEVERR_BLOCK_ID, DEVERR_LENGTH, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 _lock = threading.Lock()
@@ -63,6 +64,29 @@ def lib():
             L.pkv_paged_attention_noalloc.restype = c.c_int
             L.pkv_paged_attention_noalloc.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, i32, vp, vp, i32, i32,
                                                       c.c_float, vp, i32, vp, vp]
+            L.pkv_kvmgr_create.restype = vp
+            L.pkv_kvmgr_create.argtypes = [i64]
+            L.pkv_kvmgr_destroy.restype = None
+            L.pkv_kvmgr_destroy.argtypes = [vp]
+            L.pkv_kvmgr_add_sequence.restype = c.c_int
+            L.pkv_kvmgr_add_sequence.argtypes = [vp, i64, vp, i64, c.POINTER(i64), vp]
+            L.pkv_kvmgr_append.restype = c.c_int
+            L.pkv_kvmgr_append.argtypes = [vp, i64, vp, i64, vp, vp, c.POINTER(i32)]
+            for nm in ("pkv_kvmgr_commit", "pkv_kvmgr_release"):
+                getattr(L, nm).restype = c.c_int
+                getattr(L, nm).argtypes = [vp, i64]
+            L.pkv_kvmgr_fork.restype = c.c_int
+            L.pkv_kvmgr_fork.argtypes = [vp, i64, i64]
+            L.pkv_kvmgr_tables.restype = c.c_int
+            L.pkv_kvmgr_tables.argtypes = [vp, vp, i32, i32, vp, vp]
+            L.pkv_kvmgr_num_free.restype = i64
+            L.pkv_kvmgr_num_free.argtypes = [vp]
+            L.pkv_kvmgr_num_cached.restype = i64
+            L.pkv_kvmgr_num_cached.argtypes = [vp]
+            L.pkv_kvmgr_refcount.restype = i32
+            L.pkv_kvmgr_refcount.argtypes = [vp, i32]
+            L.pkv_copy_blocks.restype = c.c_int
+            L.pkv_copy_blocks.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, vp, vp]
             L.pkv_debug_set_wait_limit.restype = None
             L.pkv_debug_set_wait_limit.argtypes = [c.c_uint64, vp]
             L.pkv_read_device_error.restype = c.c_int
@@ -201,6 +225,97 @@ def read_device_error(error_word, stream=None) -> int:
     if st not in (0, 5, 6):
         _check(st, "pkv_read_device_error")
     return int(code.value)
+
+
+class KVManager:
+    """The library's host-side block manager (pkv_kvmgr_*): block allocation,
+    reference counts, copy-on-write and radix prefix reuse; it hands out the
+    slots and block tables the append and attention calls take.  Host memory
+    only (numpy arrays in and out)."""
+
+    def __init__(self, num_blocks: int):
+        self._lib = lib()
+        self._h = self._lib.pkv_kvmgr_create(int(num_blocks))
+        if not self._h:
+            raise PagedKVError(1, "pkv_kvmgr_create")
+        self.num_blocks = int(num_blocks)
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_kvmgr_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _i32(a):
+        import numpy as np
+        return np.ascontiguousarray(a, dtype=np.int32)
+
+    def add_sequence(self, seq: int, tokens):
+        """-> (cached_tokens, slots of the other prompt tokens: int64 array)."""
+        import numpy as np
+        t = self._i32(tokens)
+        slots = np.zeros(len(t), dtype=np.int64)
+        cached = ctypes.c_int64(0)
+        _check(self._lib.pkv_kvmgr_add_sequence(self._h, int(seq), t.ctypes.data, len(t), ctypes.byref(cached),
+                                                slots.ctypes.data), "pkv_kvmgr_add_sequence")
+        return int(cached.value), slots[:len(t) - int(cached.value)].copy()
+
+    def append(self, seq: int, tokens):
+        """-> (slots: int64 array, copy-on-write pair (src, dst) or None)."""
+        import numpy as np
+        t = self._i32(tokens)
+        slots = np.zeros(len(t), dtype=np.int64)
+        copy = np.zeros(2, dtype=np.int32)
+        ncopy = ctypes.c_int32(0)
+        _check(self._lib.pkv_kvmgr_append(self._h, int(seq), t.ctypes.data, len(t), slots.ctypes.data,
+                                          copy.ctypes.data, ctypes.byref(ncopy)), "pkv_kvmgr_append")
+        return slots, (int(copy[0]), int(copy[1])) if ncopy.value else None
+
+    def commit(self, seq: int):
+        _check(self._lib.pkv_kvmgr_commit(self._h, int(seq)), "pkv_kvmgr_commit")
+
+    def fork(self, parent: int, child: int):
+        _check(self._lib.pkv_kvmgr_fork(self._h, int(parent), int(child)), "pkv_kvmgr_fork")
+
+    def release(self, seq: int):
+        _check(self._lib.pkv_kvmgr_release(self._h, int(seq)), "pkv_kvmgr_release")
+
+    def tables(self, seqs, max_blocks: int):
+        """-> (block_tables int32 [n, max_blocks] (-1 padded), context_lens int32 [n])."""
+        import numpy as np
+        s = np.ascontiguousarray(seqs, dtype=np.int64)
+        bt = np.zeros((len(s), max_blocks), dtype=np.int32)
+        lens = np.zeros(len(s), dtype=np.int32)
+        _check(self._lib.pkv_kvmgr_tables(self._h, s.ctypes.data, len(s), int(max_blocks), bt.ctypes.data,
+                                          lens.ctypes.data), "pkv_kvmgr_tables")
+        return bt, lens
+
+    def num_free(self) -> int:
+        return int(self._lib.pkv_kvmgr_num_free(self._h))
+
+    def num_cached(self) -> int:
+        return int(self._lib.pkv_kvmgr_num_cached(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pkv_kvmgr_refcount(self._h, int(block)))
+
+
+def copy_blocks(cache: PagedKVCache, pairs, stream=None):
+    """pkv_copy_blocks: device int32 [n, 2] (src, dst) block pairs; an FP8
+    cache's scales are copied too."""
+    if pairs.dtype != torch.int32 or not pairs.is_contiguous():
+        raise ValueError("pairs must be contiguous int32 [n, 2]")
+    d = cache.desc()
+    fp8 = cache.kv_dtype == "fp8"
+    _check(lib().pkv_copy_blocks(ctypes.byref(d), _ptr(pairs), int(pairs.shape[0]),
+                                 _ptr(cache.k_scales) if fp8 else None, _ptr(cache.v_scales) if fp8 else None,
+                                 _stream(stream)), "pkv_copy_blocks")
 
 
 def debug_set_wait_limit(limit_ns: int = 0, hold_flag=None):

@@ -1,7 +1,8 @@
 """Build libpagedkv.so in-tree with nvcc for sm_103a (GB300).
 
 Each .cu translation unit compiles in parallel to an object file under
-``_build/``; the objects link into ``paged_kv_decode_14_gb300/libpagedkv.so``.
+``_build/`` (the host-only block manager, ``kvmgr.cpp``, with the host C++
+compiler); the objects link into ``paged_kv_decode_14_gb300/libpagedkv.so``.
 """
 
 from __future__ import annotations
@@ -18,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "api_noalloc.cu", "append.cu", "attn_simt.cu", "attn_tc.cu"]
+SOURCES = ["api.cu", "api_noalloc.cu", "append.cu", "attn_simt.cu", "attn_tc.cu", "kvmgr.cpp"]
 
 
 def nvcc() -> str:
@@ -26,6 +27,13 @@ def nvcc() -> str:
         if cand and os.path.exists(cand):
             return cand
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libpagedkv")
+
+
+def cxx() -> str:
+    for cand in (os.environ.get("CXX"), shutil.which("g++"), shutil.which("c++")):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("no host C++ compiler found (g++)")
 
 
 def _flags(verbose_ptxas: bool = False):
@@ -51,10 +59,14 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
     objs, cmds = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or verbose_ptxas or not _newer(o, [s] + headers):
-            cmds.append([nv, *_flags(verbose_ptxas), "-c", s, "-o", o])
+            if src.endswith(".cpp"):      # host-only C++ (the block manager): the host compiler
+                cmds.append([cxx(), "-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall",
+                             "-I", os.path.join(ROOT, "include"), "-c", s, "-o", o])
+            else:
+                cmds.append([nv, *_flags(verbose_ptxas), "-c", s, "-o", o])
     if cmds:
         with cf.ThreadPoolExecutor(max_workers=jobs or min(len(cmds), os.cpu_count() or 1)) as ex:
             futs = [ex.submit(subprocess.run, c, capture_output=True, text=True) for c in cmds]

@@ -4,10 +4,13 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "../../include/pagedkv_kvmgr.h"
 
 namespace pkv {
 cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_new, const int64_t* slots,
                           int64_t num_tokens, int* err, cudaStream_t st, int num_sms);
+cudaError_t launch_copy_blocks(const pkv_cache& c, const int32_t* pairs, int n, float* k_scales, float* v_scales,
+                               cudaStream_t st, int num_sms);
 cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st);
 int simt_rows_pad(int rows);
@@ -163,6 +166,8 @@ PKV_API const char* pkv_status_string(pkv_status s) {
         case PKV_ERR_CUDA: return "CUDA error";
         case PKV_ERR_DEVICE_INDEX: return "device-side index or length error";
         case PKV_ERR_TIMEOUT: return "device-side wait timed out";
+        case PKV_ERR_NO_BLOCKS: return "no free cache block and none evictable";
+        case PKV_ERR_UNKNOWN_SEQ: return "unknown (or already registered) sequence id";
     }
     return "unknown status";
 }
@@ -181,6 +186,20 @@ PKV_API pkv_status pkv_paged_kv_append(const pkv_cache* cache, const void* k_new
     cudaError_t e = launch_append(*cache, k_new, v_new, slot_mapping, num_tokens, device_error,
                                   (cudaStream_t)stream, sms);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+PKV_API pkv_status pkv_copy_blocks(const pkv_cache* cache, const int32_t* pairs, int32_t n, float* k_scales,
+                                   float* v_scales, void* stream) {
+    pkv_status s = check_cache(cache);
+    if (s != PKV_OK) return s;
+    if (n < 0) return PKV_ERR_INVALID_ARG;
+    if (n == 0) return PKV_OK;
+    if (!pairs) return PKV_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    return launch_copy_blocks(*cache, pairs, n, k_scales, v_scales, (cudaStream_t)stream, sms) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
 }
 
 PKV_API size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

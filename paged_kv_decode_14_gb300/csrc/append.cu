@@ -65,6 +65,48 @@ __global__ void __launch_bounds__(256) append_kernel(const uint8_t* __restrict__
     }
 }
 
+// Copy-on-write of whole blocks: pairs[2i] -> pairs[2i + 1], every kv-head's
+// K and V page (16-byte chunks, one per thread), and the FP8 scales.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restrict__ pairs, int n, int Hkv,
+                                                          int page_chunks, int64_t num_blocks, uint8_t* k_cache,
+                                                          uint8_t* v_cache, float* k_scales, float* v_scales) {
+    griddep_launch();
+    griddep_wait();                              // the previous kernel's reads of these pages are done
+    const int64_t per_pair = (int64_t)2 * Hkv * page_chunks;
+    const int64_t total = (int64_t)n * per_pair;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int i = (int)(idx / per_pair);
+        const int64_t rem = idx % per_pair;
+        const int which = (int)(rem / ((int64_t)Hkv * page_chunks));      // 0 = K, 1 = V
+        const int64_t within = rem % ((int64_t)Hkv * page_chunks);       // (head, chunk) of the block
+        const int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) continue;
+        uint8_t* base = which ? v_cache : k_cache;
+        const size_t blk_bytes = (size_t)Hkv * page_chunks * 16;
+        const uint4 x = *reinterpret_cast<const uint4*>(base + (size_t)src * blk_bytes + within * 16);
+        *reinterpret_cast<uint4*>(base + (size_t)dst * blk_bytes + within * 16) = x;
+        float* sc = which ? v_scales : k_scales;
+        if (sc && within % page_chunks == 0) {           // the head's first chunk also copies its scale
+            const int64_t head = within / page_chunks;
+            sc[(size_t)dst * Hkv + head] = sc[(size_t)src * Hkv + head];
+        }
+    }
+}
+
+cudaError_t launch_copy_blocks(const pkv_cache& c, const int32_t* pairs, int n, float* k_scales, float* v_scales,
+                               cudaStream_t st, int num_sms) {
+    const int E = c.kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
+    const int page_chunks = kBlock * c.head_dim * E / 16;
+    const int64_t total = (int64_t)n * 2 * c.num_kv_heads * page_chunks;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(copy_blocks_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pairs, n, (int)c.num_kv_heads,
+                      page_chunks, (int64_t)c.num_blocks, (uint8_t*)c.k_cache, (uint8_t*)c.v_cache,
+                      E == 1 ? k_scales : (float*)nullptr, E == 1 ? v_scales : (float*)nullptr);
+}
+
 cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_new, const int64_t* slots,
                           int64_t num_tokens, int* err, cudaStream_t st, int num_sms) {
     const int E = c.kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;

@@ -11,12 +11,17 @@ import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+INCLUDE = os.path.join(ROOT, "include")
 
 
 def declared_symbols():
-    src = open(HEADER).read()
-    return re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", src)
+    """Every entry point any header under include/ declares."""
+    syms = []
+    for n in sorted(os.listdir(INCLUDE)):
+        if n.endswith(".h"):
+            src = open(os.path.join(INCLUDE, n)).read()
+            syms += re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", src)
+    return syms
 
 
 def _built_lib():
@@ -31,7 +36,9 @@ def _built_lib():
 def test_header_declares_the_boundary():
     syms = declared_symbols()
     for s in ("pkv_paged_kv_append", "pkv_paged_attention", "pkv_attention_workspace_size",
-              "pkv_workspace_init", "pkv_read_device_error", "pkv_status_string", "pkv_version"):
+              "pkv_workspace_init", "pkv_read_device_error", "pkv_status_string", "pkv_version",
+              "pkv_kvmgr_create", "pkv_kvmgr_add_sequence", "pkv_kvmgr_append", "pkv_kvmgr_tables",
+              "pkv_copy_blocks"):
         assert s in syms
 
 
