@@ -57,6 +57,11 @@ def lib():
                                                  c.c_int64, c.c_int, c.c_int, c.c_void_p, c.c_int,
                                                  c.c_void_p, c.c_int, c.c_void_p, c.c_void_p, c.c_int,
                                                  c.c_float, c.c_void_p, c.c_void_p, c.c_int]
+            L.oracle_rope.restype = None
+            L.oracle_rope.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64, c.c_int, c.c_int, c.c_double]
+            L.oracle_fp8_autoscale.restype = None
+            L.oracle_fp8_autoscale.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64, c.c_int, c.c_int,
+                                               c.c_int64, c.c_void_p, c.c_void_p]
             _lib = L
     return _lib
 
@@ -128,6 +133,29 @@ def paged_attention(kv_dtype, k_cache, v_cache, k_scales, v_scales, num_blocks, 
     if st != 0:
         raise ValueError(f"oracle attention failed with status {st}")
     return out, outb
+
+
+def rope(x, positions, theta: float) -> np.ndarray:
+    """Rotate-half RoPE of bf16 rows x [T, H, D] at positions [T], fp64 then
+    bf16 RNE (oracle_rope)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    y = np.empty_like(x)
+    T, H, D = x.shape
+    lib().oracle_rope(_ptr(x), _ptr(y), _ptr(pos), T, H, D, float(theta))
+    return y
+
+
+def fp8_autoscale(k_new, v_new, slots, num_blocks, k_scales, v_scales):
+    """In-place: the scales of the blocks this append starts, from its values
+    (oracle_fp8_autoscale)."""
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    slots = np.ascontiguousarray(slots, dtype=np.int64)
+    assert k_scales.flags.c_contiguous and v_scales.flags.c_contiguous
+    T, Hkv, D = k_new.shape
+    lib().oracle_fp8_autoscale(_ptr(k_new), _ptr(v_new), _ptr(slots), T, Hkv, D, int(num_blocks),
+                               _ptr(k_scales), _ptr(v_scales))
 
 
 # ---------------------------------------------------------------- workload helpers

@@ -289,3 +289,66 @@ int oracle_paged_attention(int kv_dtype, const void* k_cache, const void* v_cach
     free(th);
     return st;
 }
+
+/* ---------------------------------------------------------------- RoPE */
+
+/* Rotary position embedding, rotate-half form (the lfm25-inference file list
+ * names kernels/rope.cu; the pages fix no form, this is the reading): for a
+ * row x of head_dim D at position p and i < D/2, with angle = p * theta^(-2i/D),
+ *   y_i       = x_i * cos(angle) - x_{i+D/2} * sin(angle)
+ *   y_{i+D/2} = x_{i+D/2} * cos(angle) + x_i * sin(angle)
+ * evaluated in fp64 and rounded once to bf16 (nearest even).
+ * x, y: [T][H][D] bf16 bits (may be the same buffer); positions: [T]. */
+void oracle_rope(const uint16_t* x, uint16_t* y, const int32_t* positions, int64_t T, int H, int D,
+                 double theta) {
+    int half = D / 2;
+    double* row = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!row) return;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int h = 0; h < H; ++h) {
+            const uint16_t* src = x + ((size_t)t * H + h) * D;
+            uint16_t* dst = y + ((size_t)t * H + h) * D;
+            for (int d = 0; d < D; ++d) row[d] = bf16_value(src[d]);
+            for (int i = 0; i < half; ++i) {
+                double inv_freq = pow(theta, -2.0 * (double)i / (double)D);
+                double angle = (double)positions[t] * inv_freq;
+                double c = cos(angle), s = sin(angle);
+                double a = row[i], b = row[i + half];
+                dst[i] = oracle_bf16_round(a * c - b * s);
+                dst[i + half] = oracle_bf16_round(b * c + a * s);
+            }
+        }
+    }
+    free(row);
+}
+
+/* FP8 scales chosen at append time: for every (block, kv-head) whose
+ * offset-0 slot this call writes (a block the call starts), the scale is the
+ * largest |value| among this call's values stored in that block and head,
+ * NaN ignored, divided by 448 in IEEE fp32 (1.0 if that maximum is 0); other
+ * blocks keep their scale.  k_new / v_new: [T][Hkv][D] bf16 bits (K already
+ * rotated when RoPE is fused); slots as for the append. */
+void oracle_fp8_autoscale(const uint16_t* k_new, const uint16_t* v_new, const int64_t* slots, int64_t T,
+                          int Hkv, int D, int64_t num_blocks, float* k_scales, float* v_scales) {
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t s = slots[t];
+        if (s < 0 || s / ORACLE_BLOCK >= num_blocks || s % ORACLE_BLOCK != 0) continue;
+        int64_t blk = s / ORACLE_BLOCK;
+        for (int g = 0; g < Hkv; ++g) {
+            double mk = 0.0, mv = 0.0;
+            for (int64_t u = 0; u < T; ++u) {
+                if (slots[u] < 0 || slots[u] / ORACLE_BLOCK != blk) continue;
+                for (int d = 0; d < D; ++d) {
+                    double a = fabs(bf16_value(k_new[((size_t)u * Hkv + g) * D + d]));
+                    double b = fabs(bf16_value(v_new[((size_t)u * Hkv + g) * D + d]));
+                    if (a > mk) mk = a;                 /* (NaN compares false: ignored) */
+                    if (b > mv) mv = b;
+                }
+            }
+            volatile float fk = (float)mk, fv = (float)mv;   /* exact: bf16 values */
+            volatile float sk = fk / 448.0f, sv = fv / 448.0f;
+            k_scales[blk * Hkv + g] = fk > 0.0f ? sk : 1.0f;
+            v_scales[blk * Hkv + g] = fv > 0.0f ? sv : 1.0f;
+        }
+    }
+}

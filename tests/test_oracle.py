@@ -428,3 +428,79 @@ def test_oracle_reports_bad_inputs():
     w.block_tables[0, 1] = w.num_blocks + 5
     with pytest.raises(ValueError, match="status 3"):
         oracle.attend(w, kc, vc)
+
+
+# ------------------------------------------------------------------------- RoPE, FP8 scales
+
+def test_rope_golden_hand_worked():
+    for ln in open(os.path.join(GOLDEN, "rope_example.txt")):
+        if ln.startswith("#") or not ln.strip():
+            continue
+        f = ln.split()
+        theta, pos = float(f[0]), int(f[1])
+        x = np.array([int(v, 16) for v in f[2:6]], np.uint16).reshape(1, 1, 4)
+        want = np.array([int(v, 16) for v in f[6:10]], np.uint16)
+        assert oracle.rope(x, [pos], theta).reshape(-1).tolist() == want.tolist()
+
+
+def _bf16_rows(rng, shape):
+    return wl.bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+
+
+def test_rope_invariants():
+    """Position 0 is the identity; each (i, i + D/2) pair keeps its norm; a
+    rotation by p1 then by p2 equals one by p1 + p2; and scores of rotated
+    rows depend only on the positions' difference (up to bf16 rounding)."""
+    rng = np.random.default_rng(11)
+    T, H, D = 6, 3, 64
+    x = _bf16_rows(rng, (T, H, D))
+    assert np.array_equal(oracle.rope(x, np.zeros(T, np.int32), 1e4), x)
+    pos = rng.integers(0, 40000, T).astype(np.int32)
+    y = oracle.rope(x, pos, 1e4)
+    fx, fy = wl.bf16_to_f32(x).astype(np.float64), wl.bf16_to_f32(y).astype(np.float64)
+    nx = fx[..., :D // 2] ** 2 + fx[..., D // 2:] ** 2
+    ny = fy[..., :D // 2] ** 2 + fy[..., D // 2:] ** 2
+    assert np.all(np.abs(ny - nx) <= 2.0 ** -6 * nx + 1e-30)
+    p1, p2 = rng.integers(0, 3000, T).astype(np.int32), rng.integers(0, 3000, T).astype(np.int32)
+    two = wl.bf16_to_f32(oracle.rope(oracle.rope(x, p1, 1e4), p2, 1e4)).astype(np.float64)
+    one = wl.bf16_to_f32(oracle.rope(x, p1 + p2, 1e4)).astype(np.float64)
+    assert np.max(np.abs(two - one)) <= 2.0 ** -6 * np.max(np.abs(one))
+    q = _bf16_rows(rng, (1, 1, D))
+    k = _bf16_rows(rng, (1, 1, D))
+    def score(a, b):
+        qa = wl.bf16_to_f32(oracle.rope(q, [a], 1e4)).astype(np.float64).reshape(-1)
+        kb = wl.bf16_to_f32(oracle.rope(k, [b], 1e4)).astype(np.float64).reshape(-1)
+        return float(qa @ kb)
+    base = score(100, 37)
+    for shift in (1, 50, 9000):
+        assert abs(score(100 + shift, 37 + shift) - base) <= 0.05 * (1.0 + abs(base))
+
+
+def test_fp8_autoscale_recipe():
+    """Blocks this append starts get absmax / 448 (fp32) over the call's values
+    in that block and head (NaN ignored, 1.0 if all zero) -- the same recipe
+    as the input generator's, computed here with numpy; others keep theirs."""
+    rng = np.random.default_rng(12)
+    Hkv, D, NB = 2, 64, 6
+    T = 40                                                     # block 1: offsets 0..15, block 2: 0..15, block 4: 0..7
+    slots = np.concatenate([16 + np.arange(16), 32 + np.arange(16), 64 + np.arange(8)]).astype(np.int64)
+    k = _bf16_rows(rng, (T, Hkv, D))
+    v = _bf16_rows(rng, (T, Hkv, D))
+    v[16:32, 1] = 0                                            # block 2, head 1: all zero V
+    k[3, 0, 5] = np.uint16(0x7FC0)                             # a NaN in block 1, head 0
+    extra = np.array([[5 * 16 + 3]], np.int64).reshape(-1)     # block 5 continued (offset 3): keeps its scale
+    slots = np.concatenate([slots, extra])
+    k = np.concatenate([k, _bf16_rows(rng, (1, Hkv, D))])
+    v = np.concatenate([v, _bf16_rows(rng, (1, Hkv, D))])
+    ks = np.full((NB, Hkv), 7.0, np.float32)
+    vs = np.full((NB, Hkv), 7.0, np.float32)
+    oracle.fp8_autoscale(k, v, slots, NB, ks, vs)
+    fk, fv = wl.bf16_to_f32(k), wl.bf16_to_f32(v)
+    for blk, rows in ((1, slice(0, 16)), (2, slice(16, 32)), (4, slice(32, 40))):
+        for g in range(Hkv):
+            ak = np.nanmax(np.abs(fk[rows, g]))
+            av = np.nanmax(np.abs(fv[rows, g]))
+            assert ks[blk, g] == (np.float32(ak) / np.float32(448.0) if ak > 0 else np.float32(1.0))
+            assert vs[blk, g] == (np.float32(av) / np.float32(448.0) if av > 0 else np.float32(1.0))
+    assert vs[2, 1] == 1.0
+    assert np.all(ks[[0, 3, 5]] == 7.0) and np.all(vs[[0, 3, 5]] == 7.0)
