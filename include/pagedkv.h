@@ -121,6 +121,41 @@ PKV_API pkv_status pkv_paged_kv_append(const pkv_cache* cache, const void* k_new
                                        int32_t* device_error, void* stream);
 
 /*
+ * paged_kv_append with rotary position embedding fused in, and optionally
+ * FP8 scales chosen from the values (lfm25-inference file list:
+ * kernels/rope.cu, kernels/kv_cache.cu; the pages fix neither the rotation's
+ * form nor a scale rule -- these are the library's readings).
+ *
+ *   positions      device int32 [num_tokens]: each new token's position in its
+ *                  sequence.  NULL: no rotation (a plain append, which can
+ *                  still choose FP8 scales).
+ *   rope_theta     the rotation base (e.g. 10000, 1e6); > 0 with positions.
+ *                  Rotate-half form: for i < head_dim / 2 and angle
+ *                  a = position * rope_theta^(-2i / head_dim),
+ *                  y_i = x_i cos a - x_{i+D/2} sin a, y_{i+D/2} = x_{i+D/2} cos a + x_i sin a,
+ *                  evaluated in fp64 and rounded once to bf16.  K is rotated
+ *                  before it is stored; V is stored as given.
+ *   q, num_q_heads optional device bf16 [num_tokens][num_q_heads][head_dim]: the
+ *                  same tokens' query rows, rotated in place (NULL: none).
+ *   fp8_scales_from_values   FP8 caches only (else PKV_ERR_INVALID_ARG): for every
+ *                  (block, kv-head) whose offset-0 slot this call writes (a block
+ *                  the call starts), the scale becomes the largest |value| among
+ *                  this call's (rotated) values in that block and head, NaN
+ *                  ignored, divided by 448 in IEEE fp32 (1.0 if that maximum is 0),
+ *                  and the values are encoded with it; the cache's k_scales /
+ *                  v_scales arrays are written.  A block continued by a later call
+ *                  keeps its scale (values beyond it saturate).  0: the scales are
+ *                  inputs, as for pkv_paged_kv_append.
+ * Other arguments and the slot rules as for pkv_paged_kv_append.  Supported
+ * up to 32 kv-heads (else PKV_ERR_UNSUPPORTED).  Launches one CTA per token
+ * (plus two short kernels when FP8 scales are chosen here).
+ */
+PKV_API pkv_status pkv_paged_kv_append_rope(const pkv_cache* cache, const void* k_new, const void* v_new,
+                                            const int64_t* slot_mapping, int64_t num_tokens, const int32_t* positions,
+                                            float rope_theta, void* q, int32_t num_q_heads,
+                                            int32_t fp8_scales_from_values, int32_t* device_error, void* stream);
+
+/*
  * Workspace for pkv_paged_attention, in bytes.  The workspace holds the
  * device error word, one merge ticket per (sequence, kv-head) and the split
  * partial results.  It must be zeroed once before first use

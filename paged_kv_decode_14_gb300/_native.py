@@ -85,6 +85,9 @@ def lib():
             L.pkv_kvmgr_num_cached.argtypes = [vp]
             L.pkv_kvmgr_refcount.restype = i32
             L.pkv_kvmgr_refcount.argtypes = [vp, i32]
+            L.pkv_paged_kv_append_rope.restype = c.c_int
+            L.pkv_paged_kv_append_rope.argtypes = [c.POINTER(CacheDesc), vp, vp, vp, i64, vp, c.c_float, vp, i32,
+                                                   i32, vp, vp]
             L.pkv_copy_blocks.restype = c.c_int
             L.pkv_copy_blocks.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, vp, vp]
             L.pkv_debug_set_wait_limit.restype = None
@@ -156,6 +159,29 @@ def append(cache: PagedKVCache, k_new, v_new, slot_mapping, device_error=None, s
     st = lib().pkv_paged_kv_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
                                    int(slot_mapping.numel()), _ptr(device_error), _stream(stream))
     _check(st, "pkv_paged_kv_append")
+
+
+def append_rope(cache: PagedKVCache, k_new, v_new, slot_mapping, positions=None, theta: float = 10000.0, q=None,
+                fp8_scales_from_values: bool = False, device_error=None, stream=None):
+    """pkv_paged_kv_append_rope: append with K rotated at `positions` (int32
+    [T], None = no rotation), q rows [T, Hq, D] rotated in place, and
+    optionally the FP8 scales of the blocks this call starts chosen from the
+    values (written into cache.k_scales / v_scales)."""
+    for t in (k_new, v_new):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("k_new / v_new must be contiguous bfloat16")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    if positions is not None and (positions.dtype != torch.int32 or not positions.is_contiguous()):
+        raise ValueError("positions must be contiguous int32")
+    if q is not None and (q.dtype != torch.bfloat16 or not q.is_contiguous()):
+        raise ValueError("q must be contiguous bfloat16")
+    d = cache.desc()
+    st = lib().pkv_paged_kv_append_rope(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                        int(slot_mapping.numel()), _ptr(positions), float(theta), _ptr(q),
+                                        int(q.shape[1]) if q is not None else 0, int(bool(fp8_scales_from_values)),
+                                        _ptr(device_error), _stream(stream))
+    _check(st, "pkv_paged_kv_append_rope")
 
 
 def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_q_len, num_ctas=0) -> int:

@@ -9,6 +9,9 @@
 namespace pkv {
 cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_new, const int64_t* slots,
                           int64_t num_tokens, int* err, cudaStream_t st, int num_sms);
+cudaError_t launch_append_rope(const pkv_cache& c, const void* k_new, const void* v_new, const int64_t* slots,
+                               int64_t T, const int32_t* positions, double theta, void* q, int Hq, bool autoscale,
+                               int* err, cudaStream_t st, int num_sms);
 cudaError_t launch_copy_blocks(const pkv_cache& c, const int32_t* pairs, int n, float* k_scales, float* v_scales,
                                cudaStream_t st, int num_sms);
 cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
@@ -186,6 +189,28 @@ PKV_API pkv_status pkv_paged_kv_append(const pkv_cache* cache, const void* k_new
     cudaError_t e = launch_append(*cache, k_new, v_new, slot_mapping, num_tokens, device_error,
                                   (cudaStream_t)stream, sms);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+PKV_API pkv_status pkv_paged_kv_append_rope(const pkv_cache* cache, const void* k_new, const void* v_new,
+                                            const int64_t* slot_mapping, int64_t num_tokens, const int32_t* positions,
+                                            float rope_theta, void* q, int32_t num_q_heads,
+                                            int32_t fp8_scales_from_values, int32_t* device_error, void* stream) {
+    pkv_status s = check_cache(cache);
+    if (s != PKV_OK) return s;
+    if (num_tokens < 0 || num_tokens > 0x7fffffff) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (positions && !(rope_theta > 0.f)) return PKV_ERR_INVALID_ARG;
+    if (q && (!positions || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads)) return PKV_ERR_INVALID_ARG;
+    if (fp8_scales_from_values && cache->kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+    if (cache->num_kv_heads > 32) return PKV_ERR_UNSUPPORTED;
+    const int sms = num_sms_current();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    return launch_append_rope(*cache, k_new, v_new, slot_mapping, num_tokens, positions, (double)rope_theta, q,
+                              q ? num_q_heads : 0, fp8_scales_from_values != 0, device_error, (cudaStream_t)stream,
+                              sms) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
 }
 
 PKV_API pkv_status pkv_copy_blocks(const pkv_cache* cache, const int32_t* pairs, int32_t n, float* k_scales,
