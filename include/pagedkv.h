@@ -236,6 +236,48 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
                                        void* stream);
 
 /*
+ * Shared-prefix cascade: pkv_paged_attention for a batch whose sequences come
+ * in groups that share their leading blocks (the turns of a conversation
+ * reusing one system prompt through the radix tree: lfm25-inference README,
+ * "Radix Tree Prefix Caching"; inferd backlog, prefix sharing).  Same result
+ * as pkv_paged_attention over the same tables (up to the order of fp32 sums),
+ * but each shared block is read and attended once for the whole group: a
+ * first pass attends each group's prefix with all the group's query rows at
+ * once and keeps a per-row state (normalised fp32 output and log-sum-exp);
+ * a second pass attends every sequence's remaining pages and merges each row
+ * with its prefix state before writing out.
+ *
+ *   group_starts       device int32 [num_groups + 1]: group g is sequences
+ *                      [group_starts[g], group_starts[g + 1]); the groups cover
+ *                      0 .. num_seqs - 1 in order (a sequence sharing nothing
+ *                      is a group of its own with prefix 0).
+ *   group_prefix_lens  device int32 [num_groups]: tokens of the shared prefix,
+ *                      a multiple of 16; every sequence of the group holds the
+ *                      same blocks in the first prefix/16 entries of its table,
+ *                      and prefix <= context_len - q_len for each of them (the
+ *                      query window lies after the prefix).  Violations set
+ *                      PKV_DEVERR_LENGTH.
+ *   max_group_q_len    host bound on the sum of q_lens over a group (<= 32).
+ *   workspace          >= pkv_cascade_workspace_size(...) bytes, zeroed once
+ *                      (pkv_workspace_init); it holds both passes' merge state
+ *                      and the prefix states.
+ * Other arguments as for pkv_paged_attention (default grid).  Both passes must
+ * fit the tensor-core kernel: bf16 caches, or FP8 caches with head_dim 128 and
+ * at most 8 query rows per kv-head in each pass; otherwise
+ * PKV_ERR_UNSUPPORTED.  Two launches on `stream`.
+ */
+PKV_API size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_groups, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, int32_t max_q_len,
+                                          int32_t max_group_q_len);
+PKV_API pkv_status pkv_paged_attention_cascade(const pkv_cache* cache, const void* q, int32_t num_q_heads,
+                                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t* context_lens, const int32_t* q_lens, int32_t num_seqs,
+                                               int32_t max_q_len, const int32_t* group_starts,
+                                               const int32_t* group_prefix_lens, int32_t num_groups,
+                                               int32_t max_group_q_len, float scale, void* out, void* workspace,
+                                               size_t workspace_bytes, void* stream);
+
+/*
  * pkv_paged_attention_noalloc -- pkv_paged_attention for callers that cannot
  * allocate device memory (the pages have no counterpart of this entry point).
  *

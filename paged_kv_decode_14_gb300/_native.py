@@ -85,6 +85,11 @@ def lib():
             L.pkv_kvmgr_num_cached.argtypes = [vp]
             L.pkv_kvmgr_refcount.restype = i32
             L.pkv_kvmgr_refcount.argtypes = [vp, i32]
+            L.pkv_cascade_workspace_size.restype = c.c_size_t
+            L.pkv_cascade_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.pkv_paged_attention_cascade.restype = c.c_int
+            L.pkv_paged_attention_cascade.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, i32, vp, vp, i32, i32, vp, vp,
+                                                      i32, i32, c.c_float, vp, vp, c.c_size_t, vp]
             L.pkv_paged_kv_append_rope.restype = c.c_int
             L.pkv_paged_kv_append_rope.argtypes = [c.POINTER(CacheDesc), vp, vp, vp, i64, vp, c.c_float, vp, i32,
                                                    i32, vp, vp]
@@ -220,6 +225,41 @@ def attention(cache: PagedKVCache, q, block_tables, context_lens, q_lens, max_q_
                                    int(context_lens.numel()), int(max_q_len), float(scale), _ptr(out),
                                    _ptr(workspace), int(workspace.numel()), int(num_ctas), _stream(stream))
     _check(st, "pkv_paged_attention")
+    return out
+
+
+def make_cascade_workspace(num_seqs, num_groups, num_q_heads, num_kv_heads, head_dim, max_q_len, max_group_q_len,
+                           device="cuda", stream=None):
+    n = lib().pkv_cascade_workspace_size(num_seqs, num_groups, num_q_heads, num_kv_heads, head_dim, max_q_len,
+                                         max_group_q_len)
+    if n == 0:
+        raise PagedKVError(1, "pkv_cascade_workspace_size")
+    ws = torch.empty(int(n), dtype=torch.uint8, device=device)
+    _check(lib().pkv_workspace_init(_ptr(ws), int(n), _stream(stream)), "pkv_workspace_init")
+    return ws
+
+
+def attention_cascade(cache: PagedKVCache, q, block_tables, context_lens, q_lens, max_q_len: int, group_starts,
+                      group_prefix_lens, max_group_q_len: int, scale: float, workspace, out=None, stream=None):
+    """pkv_paged_attention_cascade: attention with each group's shared prefix
+    attended once for the whole group (group_starts int32 [G + 1],
+    group_prefix_lens int32 [G], device)."""
+    if q.dtype != torch.bfloat16 or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be contiguous bfloat16 [rows, Hq, D]")
+    for t, name in ((block_tables, "block_tables"), (context_lens, "context_lens"), (q_lens, "q_lens"),
+                    (group_starts, "group_starts"), (group_prefix_lens, "group_prefix_lens")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+    if out is None:
+        out = torch.empty_like(q)
+    d = cache.desc()
+    st = lib().pkv_paged_attention_cascade(ctypes.byref(d), _ptr(q), int(q.shape[1]), _ptr(block_tables),
+                                           int(block_tables.shape[1]), _ptr(context_lens), _ptr(q_lens),
+                                           int(context_lens.numel()), int(max_q_len), _ptr(group_starts),
+                                           _ptr(group_prefix_lens), int(group_prefix_lens.numel()),
+                                           int(max_group_q_len), float(scale), _ptr(out), _ptr(workspace),
+                                           int(workspace.numel()), _stream(stream))
+    _check(st, "pkv_paged_attention_cascade")
     return out
 
 

@@ -100,7 +100,7 @@ int default_ctas(int num_sms) { return 4 * num_sms; }
 pkv_status attention_setup(const pkv_cache* cache, const void* q, int num_q_heads, const int32_t* block_tables,
                            int max_blocks_per_seq, const int32_t* context_lens, const int32_t* q_lens, int num_seqs,
                            int max_q_len, float scale, void* out, int num_ctas, int num_sms, AttnParams* p,
-                           AttnLaunch* L, WorkspaceLayout* wl, bool* empty) {
+                           AttnLaunch* L, WorkspaceLayout* wl, bool* empty, int max_q_limit) {
     *empty = false;
     pkv_status s = check_cache(cache);
     if (s != PKV_OK) return s;
@@ -112,7 +112,7 @@ pkv_status attention_setup(const pkv_cache* cache, const void* q, int num_q_head
     if (!q || !out || !block_tables || !context_lens || !q_lens) return PKV_ERR_INVALID_ARG;
     if (max_blocks_per_seq <= 0 || max_q_len < 1 || num_ctas < 0) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
-    if (max_q_len > 16) return PKV_ERR_UNSUPPORTED;
+    if (max_q_len > max_q_limit) return PKV_ERR_UNSUPPORTED;
     const int group = num_q_heads / cache->num_kv_heads;
     const int ks = kv_split_for(group, max_q_len);
     const int vgroup = group / ks, vheads = cache->num_kv_heads * ks;
@@ -148,6 +148,13 @@ pkv_status attention_setup(const pkv_cache* cache, const void* q, int num_q_head
     p->hg = L->hg;
     p->kv_split = ks;
     p->cache_kv_heads = cache->num_kv_heads;
+    p->cascade = 0;
+    p->group_starts = nullptr;
+    p->group_prefix_lens = nullptr;
+    p->num_groups = 0;
+    p->num_seqs_total = num_seqs;
+    p->state_o = nullptr;
+    p->state_lse = nullptr;
     fill_debug(*p);
     return PKV_OK;
 }
@@ -255,7 +262,7 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
     bool empty = false;
     const pkv_status s = attention_setup(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, q_lens,
                                          num_seqs, max_q_len, scale, out, num_ctas, num_sms_current(), &p, &L, &wl,
-                                         &empty);
+                                         &empty, 16);
     if (s != PKV_OK || empty) return s;
     if (!workspace) return PKV_ERR_INVALID_ARG;
     if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
@@ -271,6 +278,84 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
 PKV_API void pkv_debug_set_wait_limit(uint64_t limit_ns, const int32_t* hold_flag) {
     g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
     g_hold.store(hold_flag, std::memory_order_relaxed);
+}
+
+// Workspace of a cascade call: the prefix pass's (groups as sequences), the
+// suffix pass's, then the prefix states (fp32 output rows and their
+// log2-sum-exp), each 256-byte aligned.
+struct CascadeLayout {
+    size_t a_off, b_off, o_off, lse_off, total;
+};
+static CascadeLayout cascade_layout(size_t a_bytes, size_t b_bytes, int64_t rows, int Hq, int D) {
+    CascadeLayout c;
+    c.a_off = 0;
+    c.b_off = align_up(a_bytes, 256);
+    c.o_off = align_up(c.b_off + b_bytes, 256);
+    c.lse_off = align_up(c.o_off + (size_t)rows * Hq * D * 4, 256);
+    c.total = align_up(c.lse_off + (size_t)rows * Hq * 4, 256);
+    return c;
+}
+
+PKV_API size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_groups, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, int32_t max_q_len,
+                                          int32_t max_group_q_len) {
+    if (num_groups < 0 || max_group_q_len < 1 || max_q_len < 1) return 0;
+    const size_t a = pkv_attention_workspace_size(num_groups, num_q_heads, num_kv_heads, head_dim, max_group_q_len, 0);
+    const size_t b = pkv_attention_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_q_len, 0);
+    if (!a || !b) return 0;
+    return cascade_layout(a, b, (int64_t)num_seqs * max_q_len, num_q_heads, head_dim).total;
+}
+
+PKV_API pkv_status pkv_paged_attention_cascade(const pkv_cache* cache, const void* q, int32_t num_q_heads,
+                                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t* context_lens, const int32_t* q_lens, int32_t num_seqs,
+                                               int32_t max_q_len, const int32_t* group_starts,
+                                               const int32_t* group_prefix_lens, int32_t num_groups,
+                                               int32_t max_group_q_len, float scale, void* out, void* workspace,
+                                               size_t workspace_bytes, void* stream) {
+    if (num_groups < 1 || !group_starts || !group_prefix_lens || max_group_q_len < 1) return PKV_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    AttnParams pa, pb;
+    AttnLaunch la, lb;
+    WorkspaceLayout wa, wb;
+    bool empty = false;
+    // the prefix pass: groups as sequences, their whole q windows (up to 32 rows), prefix lengths as contexts
+    pkv_status s = attention_setup(cache, q, num_q_heads, block_tables, max_blocks_per_seq, group_prefix_lens, q_lens,
+                                   num_groups, max_group_q_len, scale, out, 0, sms, &pa, &la, &wa, &empty, 32);
+    if (s != PKV_OK) return s;
+    s = attention_setup(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, q_lens, num_seqs,
+                        max_q_len, scale, out, 0, sms, &pb, &lb, &wb, &empty, 16);
+    if (s != PKV_OK || empty) return s;
+    if (!la.tc || !lb.tc) return PKV_ERR_UNSUPPORTED;          // both passes on the tensor-core kernel
+    const CascadeLayout cl = cascade_layout(wa.total, wb.total, (int64_t)num_seqs * max_q_len, num_q_heads,
+                                            cache->head_dim);
+    if (workspace_bytes < cl.total) return PKV_ERR_WORKSPACE;
+    uint8_t* w = (uint8_t*)workspace;
+    float* so = (float*)(w + cl.o_off);
+    float* sl = (float*)(w + cl.lse_off);
+    pa.err = (int*)(w + cl.a_off);
+    pa.tickets = (int*)(w + cl.a_off + wa.tickets_off);
+    pa.partials = (float*)(w + cl.a_off + wa.partials_off);
+    pa.cascade = 1;
+    pa.group_starts = group_starts;
+    pa.num_groups = num_groups;
+    pa.num_seqs_total = num_seqs;
+    pa.state_o = so;
+    pa.state_lse = sl;
+    pb.err = (int*)(w + cl.a_off);                             // one error word for both passes
+    pb.tickets = (int*)(w + cl.b_off + wb.tickets_off);
+    pb.partials = (float*)(w + cl.b_off + wb.partials_off);
+    pb.cascade = 2;
+    pb.group_starts = group_starts;
+    pb.group_prefix_lens = group_prefix_lens;
+    pb.num_groups = num_groups;
+    pb.state_o = so;
+    pb.state_lse = sl;
+    const int E = cache->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
+    cudaError_t e = launch_attention(la, pa, cache->head_dim, E, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = launch_attention(lb, pb, cache->head_dim, E, (cudaStream_t)stream);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 PKV_API pkv_status pkv_read_device_error(void* error_word, int32_t* code, void* stream) {

@@ -23,7 +23,7 @@ namespace pkv {
 pkv_status attention_setup(const pkv_cache* cache, const void* q, int num_q_heads, const int32_t* block_tables,
                            int max_blocks_per_seq, const int32_t* context_lens, const int32_t* q_lens, int num_seqs,
                            int max_q_len, float scale, void* out, int num_ctas, int num_sms, AttnParams* p,
-                           AttnLaunch* L, WorkspaceLayout* wl, bool* empty);
+                           AttnLaunch* L, WorkspaceLayout* wl, bool* empty, int max_q_limit);
 cudaError_t launch_attention(const AttnLaunch& L, const AttnParams& p, int head_dim, int elem_bytes, cudaStream_t st);
 }  // namespace pkv
 
@@ -75,7 +75,7 @@ extern "C" PKV_API pkv_status pkv_paged_attention_noalloc(
     pkv_status s = device_setup(&scratch, &sms);
     if (s != PKV_OK) return s;
     s = pkv::attention_setup(c, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, q_lens, num_seqs,
-                             max_q_len, scale, out, num_ctas, sms, &p, &L, &wl, &empty);
+                             max_q_len, scale, out, num_ctas, sms, &p, &L, &wl, &empty, 16);
     if (s != PKV_OK || empty) return s;
     if (wl.total > (size_t)PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;   // beyond the fixed maximum
 

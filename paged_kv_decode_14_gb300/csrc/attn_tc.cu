@@ -161,7 +161,7 @@ struct Bars {
 
 // A finished piece, as its epilogue needs it.
 struct PieceDesc {
-    int b, hg, qoff, Q, S0, S1, pc;
+    int b, hg, qoff, Q, S0, S1, pc, pb;
     bool last;
 };
 
@@ -363,11 +363,35 @@ __device__ __forceinline__ float merge_acc(float x, float wo, float y, float wn)
     return __fmaf_rn(y, wn, __fmul_rn(x, wo));
 }
 
+// Final store of one output element: the row at element offset `off` of
+// out (sequence row, query head, dim 0), dim d, value num / den with
+// reference max M (log2 units).  In a cascade's prefix pass the value and
+// its log2-sum-exp M + log2(den) go to the state arrays instead; in its
+// suffix pass a row whose sequence has a group prefix (pb > 0) is merged
+// with that prefix state first (the same LSE rule as the split merge).
+template <int D>
+__device__ __forceinline__ void store_out(const AttnParams& p, size_t off, int d, float num, float den, float M,
+                                          int pb) {
+    const float o = __fdividef(num, den);
+    if (p.cascade == 1) {
+        p.state_o[off + d] = o;
+        if (d == 0) p.state_lse[off / D] = M + __log2f(den);
+        return;
+    }
+    if (p.cascade == 2 && pb > 0) {
+        const float ls = M + __log2f(den), lp = __ldcg(p.state_lse + off / D), op = __ldcg(p.state_o + off + d);
+        const float mx = fmaxf(ls, lp), ws = fast_exp2(ls - mx), wp = fast_exp2(lp - mx);
+        p.out[off + d] = __float2bfloat16_rn(__fdividef(__fmaf_rn(o, ws, __fmul_rn(op, wp)), ws + wp));
+        return;
+    }
+    p.out[off + d] = __float2bfloat16_rn(o);
+}
+
 // Merge the partials of segment [S0, S1) (NCOL columns) into out; one warp,
 // one round trip of loads per piece, pieces in CTA order.
 template <int D>
 __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q, int S0, int S1, const Part& part,
-                                   int lane) {
+                                   int lane, int pb) {
     constexpr int DPL = D / 32;
     const int c_first = part.owner(S0), c_last = part.owner(S1 - 1);
     const int R = p.group * Q, ncol = p.hg * R;
@@ -407,9 +431,8 @@ __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q,
             const int n = n0 + k;
             const size_t off = __shfl_sync(0xffffffffu, my_off, k);
             if (n < ncol) {
-                __nv_bfloat16* o = p.out + off;
 #pragma unroll
-                for (int x = 0; x < DPL; ++x) o[lane + 32 * x] = __float2bfloat16_rn(__fdividef(num[k][x], den[k]));
+                for (int x = 0; x < DPL; ++x) store_out<D>(p, off, lane + 32 * x, num[k][x], den[k], M[k], pb);
             }
         }
     }
@@ -520,7 +543,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     const bool has_work = plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt,
                                                 seqtab, bndtab, K::TABMAX, 24, &tab_used,
                                                 reinterpret_cast<int4*>(smem + K::OFF_P),   // (P ring unused yet)
-                                                &lq);
+                                                p.cascade == 0 ? &lq : nullptr);
     const Part part{W, P, tab_used ? bndtab : nullptr};
     if (!has_work) {             // uniform across the CTA
         tc_fence_before();
@@ -667,7 +690,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
 #pragma unroll
             for (int n = 0; n < RMAX; ++n) {
                 const size_t off = __shfl_sync(0xffffffffu, my_off, n);
-                if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(acc[n], Lsum[n]));
+                if (n < ncol && tt < D) store_out<D>(p, off, tt, acc[n], Lsum[n], Mx[n], d.pb);
             }
             return;
         }
@@ -683,7 +706,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     den = merge_acc(den, wo, Lsum[n], wn);
                     num = merge_acc(num, wo, acc[n], wn);
                     const size_t off = __shfl_sync(0xffffffffu, my_off, n);
-                    if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(num, den));
+                    if (n < ncol && tt < D) store_out<D>(p, off, tt, num, den, M, d.pb);
                 }
                 return;
             }
@@ -716,6 +739,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     task[3] = d.Q;
                     task[4] = d.S0;
                     task[5] = d.S1;
+                    task[6] = d.pb;
                 }
                 mbar_arrive(bar(B::MQFULL + (n_tasks & 3)));
                 ++n_tasks;
@@ -771,7 +795,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 for (int x = 0; x < 8; ++x) {
                     const int n = n0 + x;
                     const size_t off = __shfl_sync(0xffffffffu, my_off, n);
-                    if (n < ncol && tt < D) p.out[off + tt] = __float2bfloat16_rn(__fdividef(num[x], den[x]));
+                    if (n < ncol && tt < D) store_out<D>(p, off, tt, num[x], den[x], M[x], d.pb);
                 }
             }
             if (tt == 0) *ticket = 0;              // ready for the next launch
@@ -807,7 +831,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         };
         // block-table entries [ws, ws + 32) of piece `pi`'s sequence, entry ws + lane per lane
         auto load_win = [&](const PieceIter& pi, int ws) -> int {
-            const int32_t* table = p.block_tables + (size_t)pi.cur.b * p.max_blocks_per_seq;
+            // (a cascade's prefix pass reads its group's first sequence's row; a suffix
+            // pass starts after the group prefix's pages)
+            const int row = p.cascade == 1 ? __ldg(p.group_starts + pi.cur.b) : pi.cur.b;
+            const int32_t* table = p.block_tables + (size_t)row * p.max_blocks_per_seq + pi.cur.pb;
             return ws + lane < pi.cur.nb ? __ldg(table + ws + lane) : 0;
         };
         uint4 qv[QV];
@@ -1147,7 +1174,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             __syncwarp();
-            if (last) merge_segment_warp<D>(p, hg, task[2], task[3], S0, S1, part, lane);
+            if (last) merge_segment_warp<D>(p, hg, task[2], task[3], S0, S1, part, lane, task[6]);
         }
         if constexpr (SPLIT) {
             if (ok && w.S0 < u0 && w.S1 <= u1) {
@@ -1252,10 +1279,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 const int qu = it.pg0 + jt * kTP + k;
                 const int qpg = div_small(qu, HG);
                 const int hh = qu - qpg * HG;
-                const int pos = qpg * kBlock + (tt & 15);
+                const int pos = (it.cur.pb + qpg) * kBlock + (tt & 15);
                 const bool tok_ok = k < np && pos < L;
                 // visible columns: [lo, hi) of this head's R rows (causal within the window)
-                const int lo = hh * R + max(0, pos - lim0) * G, hi = hh * R + R;
+                const int lo = hh * R + (p.cascade == 1 ? 0 : max(0, pos - lim0) * G), hi = hh * R + R;
 
                 bool okw = wait_bar(bar(B::SFULL + t % NSB), (t / NSB) & 1, ctl);
                 // (FP8) this token's page scales and the columns' factors: S^T holds
@@ -1436,6 +1463,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 pd.S0 = it.S0;
                 pd.S1 = it.S1;
                 pd.pc = pc;
+                pd.pb = it.cur.pb;
 #pragma unroll
                 for (int n = 0; n < RMAX; ++n) {
                     m_ref[n] = -INFINITY;
@@ -1456,6 +1484,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         q[4] = pd.S0;
                         q[5] = pd.S1;
                         q[6] = in_piece ? 0 : 1;
+                        q[7] = pd.pb;
                     }
                     mbar_arrive(bar(B::PREADY + par));
                 } else {
@@ -1478,6 +1507,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 d.S0 = q[4];
                 d.S1 = q[5];
                 d.last = q[6] != 0;
+                d.pb = q[7];
                 d.pc = pc;
                 return d;
             };

@@ -154,6 +154,22 @@ struct AttnParams {
     // the pages of cache kv-head (virtual head) / kv_split.
     int kv_split;
     int cache_kv_heads;        // kv-heads of the cache (num_kv_heads / kv_split)
+    // Shared-prefix cascade (pkv_paged_attention_cascade).  0: plain call.
+    // 1, the prefix pass: "sequence" g is group g = sequences
+    //    [group_starts[g], group_starts[g + 1]), context_lens holds the groups'
+    //    shared prefix lengths, its query window is all the group's q rows
+    //    (consecutive in q), its block-table row is its first sequence's, no
+    //    causal mask (every row sees the whole prefix), and the results go to
+    //    state_o / state_lse instead of out.
+    // 2, the suffix pass: a sequence's pages start after its group's prefix,
+    //    and its rows are merged with the prefix pass's states before out.
+    int cascade;
+    const int32_t* group_starts;       // [num_groups + 1]
+    const int32_t* group_prefix_lens;  // [num_groups] (suffix pass)
+    int num_groups;
+    int num_seqs_total;                // sequences of the batch (the prefix pass's num_seqs counts groups)
+    float* state_o;                    // [rows][Hq][D] fp32: normalised output of the prefix pass
+    float* state_lse;                  // [rows][Hq] fp32: its log2-sum-exp (scale * log2 e units)
 };
 
 // Virtual kv-heads per cache kv-head: the smallest divisor of the GQA group
@@ -250,14 +266,48 @@ struct Part {
     }
 };
 
+// A sequence's length, query rows and first page (pages before it belong to
+// its group's shared prefix, attended by the cascade's prefix pass).
+struct SeqInfo {
+    int L, Q, pb;
+};
+__device__ __forceinline__ SeqInfo seq_info(const AttnParams& p, int b) {
+    SeqInfo r{p.context_lens[b], 0, 0};
+    if (p.cascade == 1) {
+        const int s0 = max(0, p.group_starts[b]), e = min(p.group_starts[b + 1], p.num_seqs_total);
+        for (int s = s0; s < e; ++s) r.Q += p.q_lens[s];
+        if (p.group_starts[b] < 0 || p.group_starts[b] >= p.num_seqs_total) r.Q = 0;   // (no rows to read)
+        return r;
+    }
+    r.Q = p.q_lens[b];
+    if (p.cascade == 2) {            // the group holding b: the last g with group_starts[g] <= b
+        int lo = 0, hi = p.num_groups - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.group_starts[mid] <= b) lo = mid;
+            else hi = mid - 1;
+        }
+        r.pb = p.group_prefix_lens[lo] / kBlock;
+    }
+    return r;
+}
+
 // Units (pages x kv-heads) of sequence b; sequences with no query rows or
 // invalid lengths (Q > L, Q above the launch's max_q_len, more pages than a
-// block-table row holds) contribute none.
-__device__ __forceinline__ bool seq_valid(const AttnParams& p, int L, int Q) {
-    return Q > 0 && Q <= L && Q <= p.max_q_len && (L + kBlock - 1) / kBlock <= p.max_blocks_per_seq;
+// block-table row holds, a group prefix reaching into the query window)
+// contribute none.  In the prefix pass a group with no prefix has no units
+// and is not an error.
+__device__ __forceinline__ bool seq_valid(const AttnParams& p, int L, int Q, int pb) {
+    const bool fits = Q > 0 && Q <= p.max_q_len && (L + kBlock - 1) / kBlock <= p.max_blocks_per_seq;
+    if (p.cascade == 1) return fits && L > 0 && L % kBlock == 0;     // (prefixes are whole blocks)
+    return fits && Q <= L && pb * kBlock <= L - Q;
 }
-__device__ __forceinline__ int seq_units(const AttnParams& p, int L, int Q) {
-    return seq_valid(p, L, Q) ? ((L + kBlock - 1) / kBlock) * p.num_kv_heads : 0;
+__device__ __forceinline__ bool seq_error(const AttnParams& p, int L, int Q, int pb) {
+    if (p.cascade == 1) return L != 0 && !seq_valid(p, L, Q, pb);
+    return Q != 0 && !seq_valid(p, L, Q, pb);
+}
+__device__ __forceinline__ int seq_units(const AttnParams& p, int L, int Q, int pb) {
+    return seq_valid(p, L, Q, pb) ? ((L + kBlock - 1) / kBlock - pb) * p.num_kv_heads : 0;
 }
 // q rows of sequence b in the packed q / out tensors.
 __device__ __forceinline__ int seq_qrows(int Q) { return Q > 0 ? Q : 0; }
@@ -266,7 +316,8 @@ struct Cursor {
     int b;          // current sequence
     int Ub;         // units before sequence b
     int qoff;       // first q row of sequence b
-    int L, Q, nb;   // its context length, query length, pages
+    int L, Q, nb;   // its context length, query length, pages it attends (from page pb on)
+    int pb;         // its first page (0 unless a cascade's suffix pass)
 };
 
 // Block-wide inclusive scan of one int per thread (NT threads, NT % 32 == 0).
@@ -354,21 +405,23 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         __shared__ int2 s2[NT / 32 + 1];
         __shared__ Cursor s_cur1, s_tail1;
         const int b = tid;
-        int L = 0, Q = 0, u = 0, q = 0;
+        int L = 0, Q = 0, pb = 0, u = 0, q = 0;
         if (b < p.num_seqs) {
             if (pre_lq) {
                 L = pre_lq->x;
                 Q = pre_lq->y;
             } else {
-                L = p.context_lens[b];
-                Q = p.q_lens[b];
+                const SeqInfo si = seq_info(p, b);
+                L = si.L;
+                Q = si.Q;
+                pb = si.pb;
             }
-            if (cta == 0 && Q != 0 && !seq_valid(p, L, Q)) raise_error(p.err, PKV_DEVERR_LENGTH);
-            u = seq_units(p, L, Q);
+            if (cta == 0 && seq_error(p, L, Q, pb)) raise_error(p.err, PKV_DEVERR_LENGTH);
+            u = seq_units(p, L, Q, pb);
             q = seq_qrows(Q);
         }
         const int2 inc = block_scan2_incl<NT>(make_int2(u, q), s2);
-        if (seqtab && b < p.num_seqs) seqtab[b] = make_int4(L, Q, inc.x - u, inc.y - q);
+        if (seqtab && b < p.num_seqs) seqtab[b] = make_int4(L, Q | (pb << 8), inc.x - u, inc.y - q);
         const int W = s2[NT / 32].x;
         const int nseg = p.num_kv_heads / p.hg;                             // segments of a sequence
         const int S = __syncthreads_count(u > 0) * nseg;                   // non-empty segments
@@ -423,7 +476,8 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
             c.qoff = inc.y - q;
             c.L = L;
             c.Q = Q;
-            c.nb = (L + kBlock - 1) / kBlock;
+            c.pb = pb;
+            c.nb = (L + kBlock - 1) / kBlock - pb;
             if (Ub <= u0 && u0 < Ub + u) s_cur1 = c;
             if (Ub <= u1 - 1 && u1 - 1 < Ub + u) s_tail1 = c;
         }
@@ -433,18 +487,19 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         return true;
     }
     const bool one_chunk = p.num_seqs <= NT;      // lengths stay in registers between the passes
-    int Lc = 0, Qc = 0;
+    int Lc = 0, Qc = 0, Pc = 0;
     // pass 1: total units
     int total = 0, nonempty = 0;
     for (int base = 0; base < p.num_seqs; base += NT) {
         int b = base + tid;
         int u = 0;
         if (b < p.num_seqs) {
-            int L = p.context_lens[b], Q = p.q_lens[b];
-            if (cta == 0 && Q != 0 && !seq_valid(p, L, Q)) raise_error(p.err, PKV_DEVERR_LENGTH);
-            u = seq_units(p, L, Q);
-            Lc = L;
-            Qc = Q;
+            const SeqInfo si = seq_info(p, b);
+            if (cta == 0 && seq_error(p, si.L, si.Q, si.pb)) raise_error(p.err, PKV_DEVERR_LENGTH);
+            u = seq_units(p, si.L, si.Q, si.pb);
+            Lc = si.L;
+            Qc = si.Q;
+            Pc = si.pb;
         }
         block_scan_incl<NT>(u, scratch);
         total += scratch[NT / 32];
@@ -465,16 +520,19 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
     int run_u = 0, run_q = 0;
     for (int base = 0; base < p.num_seqs; base += NT) {
         int b = base + tid;
-        int u = 0, q = 0, L = 0, Q = 0;
+        int u = 0, q = 0, L = 0, Q = 0, pb = 0;
         if (b < p.num_seqs) {
             if (one_chunk) {
                 L = Lc;
                 Q = Qc;
+                pb = Pc;
             } else {
-                L = p.context_lens[b];
-                Q = p.q_lens[b];
+                const SeqInfo si = seq_info(p, b);
+                L = si.L;
+                Q = si.Q;
+                pb = si.pb;
             }
-            u = seq_units(p, L, Q);
+            u = seq_units(p, L, Q, pb);
             q = seq_qrows(Q);
         }
         int iu = block_scan_incl<NT>(u, scratch);
@@ -491,7 +549,8 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
             c.qoff = run_q + iq - q;
             c.L = L;
             c.Q = Q;
-            c.nb = (L + kBlock - 1) / kBlock;
+            c.pb = pb;
+            c.nb = (L + kBlock - 1) / kBlock - pb;
             if (Ub <= u0 && u0 < Ub + u) s_cur = c;
             if (Ub <= u1 - 1 && u1 - 1 < Ub + u) s_tail = c;
         }
@@ -516,13 +575,16 @@ __device__ __forceinline__ void cursor_next(const AttnParams& p, Cursor& c, cons
         if (tab) {
             const int4 e = tab[c.b];
             c.L = e.x;
-            c.Q = e.y;
+            c.Q = e.y & 0xff;
+            c.pb = e.y >> 8;
         } else {
-            c.L = p.context_lens[c.b];
-            c.Q = p.q_lens[c.b];
+            const SeqInfo si = seq_info(p, c.b);
+            c.L = si.L;
+            c.Q = si.Q;
+            c.pb = si.pb;
         }
-        if (seq_units(p, c.L, c.Q) > 0) {
-            c.nb = (c.L + kBlock - 1) / kBlock;
+        if (seq_units(p, c.L, c.Q, c.pb) > 0) {
+            c.nb = (c.L + kBlock - 1) / kBlock - c.pb;
             return;
         }
         c.qoff += seq_qrows(c.Q);       // skipped sequence: its rows stay packed in q / out

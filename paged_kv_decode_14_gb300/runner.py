@@ -92,6 +92,23 @@ class DeviceWorkload:
                              out=self.out if out is None else out,
                              num_ctas=self.num_ctas if num_ctas is None else num_ctas, stream=stream)
 
+    def attend_cascade(self, out=None, stream=None):
+        """Attention with each shared-prefix group's prefix attended once
+        (pkv_paged_attention_cascade); the groups come from the workload."""
+        w = self.w
+        if not hasattr(self, "cascade_ws"):
+            gs, gp = w.prefix_groups()
+            self.group_starts = torch.from_numpy(gs).to(self.device)
+            self.group_prefix_lens = torch.from_numpy(gp).to(self.device)
+            self.max_group_q = int(max(int(w.q_lens[gs[g]:gs[g + 1]].sum()) for g in range(len(gp))))
+            self.cascade_ws = nat.make_cascade_workspace(w.num_seqs, len(gp), w.num_q_heads, w.num_kv_heads,
+                                                         w.head_dim, max(1, w.max_q_len), self.max_group_q,
+                                                         device=self.device)
+        return nat.attention_cascade(self.cache, self.q, self.block_tables, self.context_lens, self.q_lens,
+                                     max(1, w.max_q_len), self.group_starts, self.group_prefix_lens,
+                                     self.max_group_q, w.scale, self.cascade_ws,
+                                     out=self.out if out is None else out, stream=stream)
+
     def step(self, stream=None):
         """One decode step: append the new tokens, then attend."""
         self.append_step(stream)

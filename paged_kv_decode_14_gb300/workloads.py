@@ -134,6 +134,19 @@ class Workload:
             b += len(used) * self.num_kv_heads * 2 * 4
         return b
 
+    def prefix_groups(self):
+        """(group_starts [G + 1], group_prefix_lens [G]) int32: the batch cut
+        into consecutive groups, each a shared_prefix group or a sequence on
+        its own (prefix 0)."""
+        starts, plens, b = [0], [], 0
+        groups = {first: (n, ptoks) for first, n, ptoks in self.info.get("shared_prefix", [])}
+        while b < self.num_seqs:
+            n, ptoks = groups.get(b, (1, 0))
+            b += n
+            starts.append(b)
+            plens.append(ptoks)
+        return np.asarray(starts, np.int32), np.asarray(plens, np.int32)
+
     def step_io_bytes(self) -> tuple[int, int]:
         """(host->device, device->host) bytes of one decode step's per-step inputs
         and output: q, new K/V, slots, block tables, lens in; out back."""
@@ -247,7 +260,7 @@ def make_workload(name: str, *, context_lens, q_lens, num_q_heads: int, num_kv_h
                     kv_dtype=kv_dtype, scale=float(np.float32(scale)), num_blocks=num_blocks,
                     context_lens=L, q_lens=Q, block_tables=tables, prefill_k=pk, prefill_v=pv,
                     prefill_slots=pre_slots, q=q, k_new=nk, v_new=nv, slots=step_slots,
-                    k_scales=ks, v_scales=vs, info={"seed": seed})
+                    k_scales=ks, v_scales=vs, info={"seed": seed, "shared_prefix": list(shared_prefix or [])})
 
 
 # ----------------------------------------------------------------------------------
@@ -308,6 +321,23 @@ def long_fp8_b128_d128(seed: int = 5, num_seqs: int = 128, n_long: int = 4,
     return make_workload("long_fp8_b128_d128", context_lens=L, q_lens=np.ones(num_seqs, np.int32),
                          num_q_heads=32, num_kv_heads=8, head_dim=128, kv_dtype="fp8", seed=seed,
                          pool_factor=1.1, outlier_p=0.01)
+
+
+def long_prefix_reuse(prefix_tokens: int = 8192, seed: int = 7, conversations: int = 8,
+                      turns: int = 4) -> Workload:
+    """Conversations x turns sharing a long system prompt (prefix_tokens,
+    block aligned) plus private suffixes U[32, 256]; 32/8 heads, d=64: the
+    regime of the shared-prefix cascade (not one of the five named
+    configurations)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens, groups = [], []
+    for c in range(conversations):
+        groups.append((turns * c, turns, prefix_tokens))
+        for _ in range(turns):
+            lens.append(prefix_tokens + int(rng.integers(32, 257)))
+    return make_workload(f"long_prefix_{prefix_tokens}_{conversations}x{turns}_d64", context_lens=lens,
+                         q_lens=[1] * len(lens), num_q_heads=32, num_kv_heads=8, head_dim=64, seed=seed,
+                         shared_prefix=groups)
 
 
 # The five named workloads, by number.
