@@ -261,10 +261,8 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
  *   workspace          >= pkv_cascade_workspace_size(...) bytes, zeroed once
  *                      (pkv_workspace_init); it holds both passes' merge state
  *                      and the prefix states.
- * Other arguments as for pkv_paged_attention (default grid).  Both passes must
- * fit the tensor-core kernel: bf16 caches, or FP8 caches with head_dim 128 and
- * at most 8 query rows per kv-head in each pass; otherwise
- * PKV_ERR_UNSUPPORTED.  Two launches on `stream`.
+ * Other arguments as for pkv_paged_attention (default grid).  bf16 caches
+ * only (FP8: PKV_ERR_UNSUPPORTED).  Two launches on `stream`.
  */
 PKV_API size_t pkv_cascade_workspace_size(int32_t num_seqs, int32_t num_groups, int32_t num_q_heads,
                                           int32_t num_kv_heads, int32_t head_dim, int32_t max_q_len,

@@ -327,7 +327,7 @@ PKV_API pkv_status pkv_paged_attention_cascade(const pkv_cache* cache, const voi
     s = attention_setup(cache, q, num_q_heads, block_tables, max_blocks_per_seq, context_lens, q_lens, num_seqs,
                         max_q_len, scale, out, 0, sms, &pb, &lb, &wb, &empty, 16);
     if (s != PKV_OK || empty) return s;
-    if (!la.tc || !lb.tc) return PKV_ERR_UNSUPPORTED;          // both passes on the tensor-core kernel
+    if (!la.tc || !lb.tc || cache->kv_dtype != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;   // bf16, tensor-core passes
     const CascadeLayout cl = cascade_layout(wa.total, wb.total, (int64_t)num_seqs * max_q_len, num_q_heads,
                                             cache->head_dim);
     if (workspace_bytes < cl.total) return PKV_ERR_WORKSPACE;

@@ -291,6 +291,7 @@ __device__ __forceinline__ uint32_t e4m3_nan_bits(uint32_t w) { return (w & 0x7F
 // holding u1 - 1 first (when it does not start at u0), then [u0, start of
 // that piece) front to back.  Segment = (sequence, group of HG kv-heads), its
 // units = pages x HG in page-major order.  Every role walks it the same way.
+template <bool CASC>
 struct PieceIter {
     const int4* tab;            // per-sequence table in shared memory, or nullptr
     Cursor cur, fcur;
@@ -338,7 +339,7 @@ struct PieceIter {
             return;
         }
         u += npg;
-        if (u < stop && u == cur.Ub + cur.nb * Hkv) cursor_next(p, cur, tab);
+        if (u < stop && u == cur.Ub + cur.nb * Hkv) cursor_next<CASC>(p, cur, tab);
         if (u < stop) load_at(u, stop);
     }
 };
@@ -369,10 +370,14 @@ __device__ __forceinline__ float merge_acc(float x, float wo, float y, float wn)
 // its log2-sum-exp M + log2(den) go to the state arrays instead; in its
 // suffix pass a row whose sequence has a group prefix (pb > 0) is merged
 // with that prefix state first (the same LSE rule as the split merge).
-template <int D>
+template <int D, bool CASC>
 __device__ __forceinline__ void store_out(const AttnParams& p, size_t off, int d, float num, float den, float M,
                                           int pb) {
     const float o = __fdividef(num, den);
+    if constexpr (!CASC) {                     // (the plain kernels carry none of the cascade's code)
+        p.out[off + d] = __float2bfloat16_rn(o);
+        return;
+    }
     if (p.cascade == 1) {
         p.state_o[off + d] = o;
         if (d == 0) p.state_lse[off / D] = M + __log2f(den);
@@ -389,7 +394,7 @@ __device__ __forceinline__ void store_out(const AttnParams& p, size_t off, int d
 
 // Merge the partials of segment [S0, S1) (NCOL columns) into out; one warp,
 // one round trip of loads per piece, pieces in CTA order.
-template <int D>
+template <int D, bool CASC>
 __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q, int S0, int S1, const Part& part,
                                    int lane, int pb) {
     constexpr int DPL = D / 32;
@@ -432,13 +437,16 @@ __device__ void merge_segment_warp(const AttnParams& p, int hg, int qoff, int Q,
             const size_t off = __shfl_sync(0xffffffffu, my_off, k);
             if (n < ncol) {
 #pragma unroll
-                for (int x = 0; x < DPL; ++x) store_out<D>(p, off, lane + 32 * x, num[k][x], den[k], M[k], pb);
+                for (int x = 0; x < DPL; ++x) store_out<D, CASC>(p, off, lane + 32 * x, num[k][x], den[k], M[k], pb);
             }
         }
     }
 }
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8>
+// CASC: the instantiations a shared-prefix cascade launches (prefix pass:
+// group rows, no causal mask, states out; suffix pass: a first page per
+// sequence, rows merged with the prefix states); plain calls use CASC = false.
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8, bool CASC>
 __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const AttnParams p) {
     using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>;
     using B = Bars<NSK, NSV, FP8>;
@@ -540,10 +548,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     // which needs no table at the start.
     int* bndtab = (K::PTAB && !EWG) ? reinterpret_cast<int*>(smem + K::OFF_BND) : nullptr;
     bool tab_used = false;
-    const bool has_work = plan_locate<kThreads>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt,
+    const bool has_work = plan_locate<kThreads, CASC>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt,
                                                 seqtab, bndtab, K::TABMAX, 24, &tab_used,
                                                 reinterpret_cast<int4*>(smem + K::OFF_P),   // (P ring unused yet)
-                                                p.cascade == 0 ? &lq : nullptr);
+                                                CASC ? nullptr : &lq);
     const Part part{W, P, tab_used ? bndtab : nullptr};
     if (!has_work) {             // uniform across the CTA
         tc_fence_before();
@@ -558,7 +566,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     const uint32_t tmem = *tmem_slot;
     const int G = p.group, Hkv = p.num_kv_heads, HG = p.hg;
 
-    PieceIter it;
+    PieceIter<CASC> it;
     it.tab = seqtab;
     it.init(p, cur0, curt, u0, u1);
 
@@ -566,7 +574,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     // Tiles of the CTA (every role walks the same pieces).
     auto tile_count = [&]() {
         int n = 0;
-        PieceIter w = it;
+        PieceIter<CASC> w = it;
         while (w.valid()) {
             n += (w.npg + kTP - 1) / kTP;
             w.advance(p);
@@ -690,7 +698,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
 #pragma unroll
             for (int n = 0; n < RMAX; ++n) {
                 const size_t off = __shfl_sync(0xffffffffu, my_off, n);
-                if (n < ncol && tt < D) store_out<D>(p, off, tt, acc[n], Lsum[n], Mx[n], d.pb);
+                if (n < ncol && tt < D) store_out<D, CASC>(p, off, tt, acc[n], Lsum[n], Mx[n], d.pb);
             }
             return;
         }
@@ -706,7 +714,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     den = merge_acc(den, wo, Lsum[n], wn);
                     num = merge_acc(num, wo, acc[n], wn);
                     const size_t off = __shfl_sync(0xffffffffu, my_off, n);
-                    if (n < ncol && tt < D) store_out<D>(p, off, tt, num, den, M, d.pb);
+                    if (n < ncol && tt < D) store_out<D, CASC>(p, off, tt, num, den, M, d.pb);
                 }
                 return;
             }
@@ -795,7 +803,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 for (int x = 0; x < 8; ++x) {
                     const int n = n0 + x;
                     const size_t off = __shfl_sync(0xffffffffu, my_off, n);
-                    if (n < ncol && tt < D) store_out<D>(p, off, tt, num[x], den[x], M[x], d.pb);
+                    if (n < ncol && tt < D) store_out<D, CASC>(p, off, tt, num[x], den[x], M[x], d.pb);
                 }
             }
             if (tt == 0) *ticket = 0;              // ready for the next launch
@@ -816,7 +824,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         bool ok = true;
         float cur_c = 1.f;                // (FP8) lane n < 8: column n's factor 2^-E_n in the current piece
         // q rows of piece `pi` in column order, 16 bytes per lane and step
-        auto load_q = [&](const PieceIter& pi, uint4 (&v)[QV]) {
+        auto load_q = [&](const PieceIter<CASC>& pi, uint4 (&v)[QV]) {
             const int R = G * pi.cur.Q, ncol = HG * R;
 #pragma unroll
             for (int k = 0; k < QV; ++k) {
@@ -830,11 +838,11 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             }
         };
         // block-table entries [ws, ws + 32) of piece `pi`'s sequence, entry ws + lane per lane
-        auto load_win = [&](const PieceIter& pi, int ws) -> int {
+        auto load_win = [&](const PieceIter<CASC>& pi, int ws) -> int {
             // (a cascade's prefix pass reads its group's first sequence's row; a suffix
             // pass starts after the group prefix's pages)
-            const int row = p.cascade == 1 ? __ldg(p.group_starts + pi.cur.b) : pi.cur.b;
-            const int32_t* table = p.block_tables + (size_t)row * p.max_blocks_per_seq + pi.cur.pb;
+            const int row = (CASC && p.cascade == 1) ? __ldg(p.group_starts + pi.cur.b) : pi.cur.b;
+            const int32_t* table = p.block_tables + (size_t)row * p.max_blocks_per_seq + (CASC ? pi.cur.pb : 0);
             return ws + lane < pi.cur.nb ? __ldg(table + ws + lane) : 0;
         };
         uint4 qv[QV];
@@ -867,7 +875,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             ok = __shfl_sync(0xffffffffu, w, 0);
         }
         while (ok && it.valid()) {
-            PieceIter nx = it;
+            PieceIter<CASC> nx = it;
             uint4 qn[kQAhead ? QV : 1];
             int winn = 0;
             if constexpr (!kQAhead) load_q(it, qv);
@@ -1143,9 +1151,9 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         // epilogue only adds its own part.
         griddep_wait();                   // tickets and partials of the previous launch are settled
         int n_expect = 0;
-        PieceIter w = it;                 // -> the last piece
+        PieceIter<CASC> w = it;                 // -> the last piece
         for (;;) {
-            PieceIter nx = w;
+            PieceIter<CASC> nx = w;
             nx.advance(p);
             if (!nx.valid()) break;
             if (w.S0 < u0 || w.S1 > u1) ++n_expect;
@@ -1174,7 +1182,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             __syncwarp();
-            if (last) merge_segment_warp<D>(p, hg, task[2], task[3], S0, S1, part, lane, task[6]);
+            if (last) merge_segment_warp<D, CASC>(p, hg, task[2], task[3], S0, S1, part, lane, task[6]);
         }
         if constexpr (SPLIT) {
             if (ok && w.S0 < u0 && w.S1 <= u1) {
@@ -1279,10 +1287,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 const int qu = it.pg0 + jt * kTP + k;
                 const int qpg = div_small(qu, HG);
                 const int hh = qu - qpg * HG;
-                const int pos = (it.cur.pb + qpg) * kBlock + (tt & 15);
+                const int pos = ((CASC ? it.cur.pb : 0) + qpg) * kBlock + (tt & 15);
                 const bool tok_ok = k < np && pos < L;
                 // visible columns: [lo, hi) of this head's R rows (causal within the window)
-                const int lo = hh * R + (p.cascade == 1 ? 0 : max(0, pos - lim0) * G), hi = hh * R + R;
+                const int lo = hh * R + ((CASC && p.cascade == 1) ? 0 : max(0, pos - lim0) * G), hi = hh * R + R;
 
                 bool okw = wait_bar(bar(B::SFULL + t % NSB), (t / NSB) & 1, ctl);
                 // (FP8) this token's page scales and the columns' factors: S^T holds
@@ -1583,11 +1591,11 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     }
 }
 
-template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8 = false>
+template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8 = false, bool CASC = false>
 static cudaError_t launch_t(const AttnParams& p, int ncta, cudaStream_t st) {
     using K = Cfg<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>;
     static std::atomic<uint64_t> attr_set{0};
-    return launch_pdl_bigsmem(attr_set, attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV, EWG, FP8>, dim3(ncta),
+    return launch_pdl_bigsmem(attr_set, attn_tc_kernel<D, NPAD, SPLIT, NSK, NSV, EWG, FP8, CASC>, dim3(ncta),
                               dim3(threads_of<EWG>()), (size_t)K::SMEM, st, p);
 }
 
@@ -1614,6 +1622,14 @@ int tc_heads_per_segment(int num_kv_heads, int rows) {
 // needs more registers than a 384-thread block leaves, in the softmax warps.
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st) {
     const bool split = tc_col_limit(p.rows) == 8;
+    if (p.cascade != 0) {                      // (bf16 caches only: the host checks)
+        if (fp8) return cudaErrorInvalidValue;
+        if (head_dim == 128)
+            return split ? tc::launch_t<128, 16, true, 2, 4, true, false, true>(p, ncta, st)
+                         : tc::launch_t<128, 32, false, 2, 2, false, false, true>(p, ncta, st);
+        return split ? tc::launch_t<64, 16, true, 4, 6, true, false, true>(p, ncta, st)
+                     : tc::launch_t<64, 32, false, 4, 4, false, false, true>(p, ncta, st);
+    }
     if (head_dim == 128)
         return fp8     ? tc::launch_t<128, 16, true, 4, 4, true, true>(p, ncta, st)
                : split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)

@@ -271,8 +271,15 @@ struct Part {
 struct SeqInfo {
     int L, Q, pb;
 };
+// CASC: compiled for a kernel that a cascade launches (else p.cascade is 0
+// and none of its code is there).
+template <bool CASC = false>
 __device__ __forceinline__ SeqInfo seq_info(const AttnParams& p, int b) {
     SeqInfo r{p.context_lens[b], 0, 0};
+    if constexpr (!CASC) {
+        r.Q = p.q_lens[b];
+        return r;
+    }
     if (p.cascade == 1) {
         const int s0 = max(0, p.group_starts[b]), e = min(p.group_starts[b + 1], p.num_seqs_total);
         for (int s = s0; s < e; ++s) r.Q += p.q_lens[s];
@@ -297,17 +304,21 @@ __device__ __forceinline__ SeqInfo seq_info(const AttnParams& p, int b) {
 // block-table row holds, a group prefix reaching into the query window)
 // contribute none.  In the prefix pass a group with no prefix has no units
 // and is not an error.
+template <bool CASC = false>
 __device__ __forceinline__ bool seq_valid(const AttnParams& p, int L, int Q, int pb) {
     const bool fits = Q > 0 && Q <= p.max_q_len && (L + kBlock - 1) / kBlock <= p.max_blocks_per_seq;
+    if constexpr (!CASC) return fits && Q <= L;
     if (p.cascade == 1) return fits && L > 0 && L % kBlock == 0;     // (prefixes are whole blocks)
     return fits && Q <= L && pb * kBlock <= L - Q;
 }
+template <bool CASC = false>
 __device__ __forceinline__ bool seq_error(const AttnParams& p, int L, int Q, int pb) {
-    if (p.cascade == 1) return L != 0 && !seq_valid(p, L, Q, pb);
-    return Q != 0 && !seq_valid(p, L, Q, pb);
+    if (CASC && p.cascade == 1) return L != 0 && !seq_valid<CASC>(p, L, Q, pb);
+    return Q != 0 && !seq_valid<CASC>(p, L, Q, pb);
 }
+template <bool CASC = false>
 __device__ __forceinline__ int seq_units(const AttnParams& p, int L, int Q, int pb) {
-    return seq_valid(p, L, Q, pb) ? ((L + kBlock - 1) / kBlock - pb) * p.num_kv_heads : 0;
+    return seq_valid<CASC>(p, L, Q, pb) ? ((L + kBlock - 1) / kBlock - (CASC ? pb : 0)) * p.num_kv_heads : 0;
 }
 // q rows of sequence b in the packed q / out tensors.
 __device__ __forceinline__ int seq_qrows(int Q) { return Q > 0 ? Q : 0; }
@@ -393,7 +404,7 @@ __device__ __forceinline__ int2 block_scan2_incl(int2 v, int2* scratch /* NT/32 
 // per sequence, scratch for the call) for the sequences' weight prefixes.  A
 // range may come out empty only at a segment boundary, and such a CTA has no
 // work.
-template <int NT>
+template <int NT, bool CASC = false>
 __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch, Cursor* cur,
                             int* u0_out, int* u1_out, int* W_out, int* P_out, Cursor* tail = nullptr,
                             int4* seqtab = nullptr, int* bnd = nullptr, int bnd_max = 0, int ce = 0,
@@ -411,13 +422,13 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
                 L = pre_lq->x;
                 Q = pre_lq->y;
             } else {
-                const SeqInfo si = seq_info(p, b);
+                const SeqInfo si = seq_info<CASC>(p, b);
                 L = si.L;
                 Q = si.Q;
                 pb = si.pb;
             }
-            if (cta == 0 && seq_error(p, L, Q, pb)) raise_error(p.err, PKV_DEVERR_LENGTH);
-            u = seq_units(p, L, Q, pb);
+            if (cta == 0 && seq_error<CASC>(p, L, Q, pb)) raise_error(p.err, PKV_DEVERR_LENGTH);
+            u = seq_units<CASC>(p, L, Q, pb);
             q = seq_qrows(Q);
         }
         const int2 inc = block_scan2_incl<NT>(make_int2(u, q), s2);
@@ -494,9 +505,9 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
         int b = base + tid;
         int u = 0;
         if (b < p.num_seqs) {
-            const SeqInfo si = seq_info(p, b);
-            if (cta == 0 && seq_error(p, si.L, si.Q, si.pb)) raise_error(p.err, PKV_DEVERR_LENGTH);
-            u = seq_units(p, si.L, si.Q, si.pb);
+            const SeqInfo si = seq_info<CASC>(p, b);
+            if (cta == 0 && seq_error<CASC>(p, si.L, si.Q, si.pb)) raise_error(p.err, PKV_DEVERR_LENGTH);
+            u = seq_units<CASC>(p, si.L, si.Q, si.pb);
             Lc = si.L;
             Qc = si.Q;
             Pc = si.pb;
@@ -527,12 +538,12 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
                 Q = Qc;
                 pb = Pc;
             } else {
-                const SeqInfo si = seq_info(p, b);
+                const SeqInfo si = seq_info<CASC>(p, b);
                 L = si.L;
                 Q = si.Q;
                 pb = si.pb;
             }
-            u = seq_units(p, L, Q, pb);
+            u = seq_units<CASC>(p, L, Q, pb);
             q = seq_qrows(Q);
         }
         int iu = block_scan_incl<NT>(u, scratch);
@@ -566,6 +577,7 @@ __device__ bool plan_locate(const AttnParams& p, int cta, int ncta, int* scratch
 // Advance the cursor to the next sequence with work (all threads, same
 // values).  tab: the per-sequence table of plan_locate, or nullptr to read the
 // lengths from global memory.
+template <bool CASC = false>
 __device__ __forceinline__ void cursor_next(const AttnParams& p, Cursor& c, const int4* tab = nullptr) {
     c.Ub += c.nb * p.num_kv_heads;
     c.qoff += seq_qrows(c.Q);
@@ -575,15 +587,15 @@ __device__ __forceinline__ void cursor_next(const AttnParams& p, Cursor& c, cons
         if (tab) {
             const int4 e = tab[c.b];
             c.L = e.x;
-            c.Q = e.y & 0xff;
-            c.pb = e.y >> 8;
+            c.Q = CASC ? (e.y & 0xff) : e.y;
+            c.pb = CASC ? (e.y >> 8) : 0;
         } else {
-            const SeqInfo si = seq_info(p, c.b);
+            const SeqInfo si = seq_info<CASC>(p, c.b);
             c.L = si.L;
             c.Q = si.Q;
             c.pb = si.pb;
         }
-        if (seq_units(p, c.L, c.Q, c.pb) > 0) {
+        if (seq_units<CASC>(p, c.L, c.Q, c.pb) > 0) {
             c.nb = (c.L + kBlock - 1) / kBlock - c.pb;
             return;
         }
