@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--l2", choices=["flush", "rotate"], default="rotate",
                     help="keep timed inputs out of L2: flush it before every step (a write of 2x its size), "
                          "or rotate over enough copies of the workload that the data read by a step is not in L2")
+    ap.add_argument("--cascade", action="store_true",
+                    help="attend through the shared-prefix cascade (workloads whose sequences share prefix blocks)")
     ap.add_argument("--soak-seconds", type=float, default=1.5,
                     help="untimed steps run right before the timed region while clocks are sampled")
     return ap.parse_args()
@@ -319,30 +321,41 @@ def run_ours(args):
     # and replayed.  By default steps launch through the binding.
     use_graph = args.graph
     g_step, g_app, g_att = [], [], []
+    if args.cascade and not w.info.get("shared_prefix"):
+        raise SystemExit("--cascade needs a workload whose sequences share prefix blocks")
     if use_graph:
         for d in dws:
             d.step()                      # first launches (attributes, lazy loads) outside capture
+            if args.cascade:
+                d.attend_cascade()
         torch.cuda.synchronize(dev)
         cs = torch.cuda.Stream(dev)
         for d in dws:
-            for lst, fn in ((g_step, d.step), (g_app, d.append_step), (g_att, d.attend)):
+            att = d.attend_cascade if args.cascade else d.attend
+            stp = (lambda d=d, att=att: (d.append_step(), att()))
+            for lst, fn in ((g_step, stp), (g_app, d.append_step), (g_att, att)):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=cs):
                     fn()
                 lst.append(g)
         torch.cuda.synchronize(dev)
 
+    def attend(d):
+        return d.attend_cascade() if args.cascade else d.attend()
+
     def run_step(i):
         if use_graph:
             g_step[i % n_copies].replay()
         else:
-            dws[i % n_copies].step()
+            d = dws[i % n_copies]
+            d.append_step()
+            attend(d)
 
     def run_attn(i):
         if use_graph:
             g_att[i % n_copies].replay()
         else:
-            dws[i % n_copies].attend()
+            attend(dws[i % n_copies])
 
     def run_app(i):
         if use_graph:
@@ -414,7 +427,8 @@ def run_ours(args):
     def e2e_step(i):
         d = dws[i % n_copies]
         d.io.copy_(pins[i % n_copies], non_blocking=True)
-        d.step()
+        d.append_step()
+        attend(d)
         host_out.copy_(d.out, non_blocking=True)
 
     for i in range(args.warmup):
@@ -440,6 +454,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3", "data": "synthetic",
             "config": {**workload_config(w), "l2": l2_note,
+                       **({"attention": "shared-prefix cascade (prefix pass + suffix pass)"} if args.cascade else {}),
                        "launch": "CUDA graph replay per step" if use_graph else "eager, through the binding",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_hbm_peak": 100.0 * value / peak,
