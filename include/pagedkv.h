@@ -276,6 +276,42 @@ PKV_API pkv_status pkv_paged_attention_cascade(const pkv_cache* cache, const voi
                                                size_t workspace_bytes, void* stream);
 
 /*
+ * Paged chunked prefill: pkv_paged_attention for long query windows -- a
+ * prompt processed in one call, or a chunk of it appended to a context that
+ * already holds the earlier chunks (lfm25-inference README, ragged/segmented
+ * prefill FlashAttention on tensor cores; inferd backlog, chunked prefill).
+ * The same definition as pkv_paged_attention: query i (0 <= i < Q_b) of head
+ * h sees positions 0 .. L_b - Q_b + i of kv-head h / G through the block
+ * table, fp32 accumulation, bf16 output (nearest even); the tensor-core
+ * products take the softmax weights rounded to bf16.
+ *
+ *   q, out, block_tables, context_lens, q_lens, scale
+ *                  as for pkv_paged_attention (q and out packed by sequence,
+ *                  sum(q_lens) rows).
+ *   max_q_len      host upper bound of q_lens (>= 1, no upper limit beyond
+ *                  the grid size: num_seqs * Hkv * ceil(max_q_len * G / 128)
+ *                  < 2^31 CTAs).
+ *   device_error   optional device int32 error word (PKV_DEVERR_* bits: bad
+ *                  block id, bad lengths, a wait that ran out); NULL: not
+ *                  reported.  No workspace.
+ *
+ * Supported: bf16 caches (FP8: PKV_ERR_UNSUPPORTED), head_dim 64 or 128, GQA
+ * groups G = Hq / Hkv that divide 128.  One launch on `stream` (programmatic
+ * dependent launch, as pkv_paged_attention; it reads nothing before the
+ * previous kernel completes): one CTA per 128 query rows (128 / G positions x
+ * the G heads) of one (sequence, kv-head).  Deterministic.  A NaN stored in
+ * the V row of a window token also reaches the queries of the same CTA that
+ * do not see it (their zero weights multiply it in the same tensor-core
+ * product), as for pkv_paged_attention's causal windows.  The wait limit and
+ * hold flag of pkv_debug_set_wait_limit apply to it too.
+ */
+PKV_API pkv_status pkv_paged_prefill(const pkv_cache* cache, const void* q, int32_t num_q_heads,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, const int32_t* q_lens, int32_t num_seqs,
+                                     int32_t max_q_len, float scale, void* out, int32_t* device_error,
+                                     void* stream);
+
+/*
  * pkv_paged_attention_noalloc -- pkv_paged_attention for callers that cannot
  * allocate device memory (the pages have no counterpart of this entry point).
  *
@@ -328,8 +364,9 @@ PKV_API pkv_status pkv_read_device_error(void* error_word, int32_t* code, void* 
  * down.  A non-NULL hold_flag (device int32) makes the kernel wait for
  * *hold_flag != 0 before its first K/V copy: a flag that nothing sets makes
  * that wait run out.  The settings are process-wide and apply to every
- * later pkv_paged_attention(_noalloc) launch (not to the CUDA-core kernel,
- * which has no waits) until they are set again; not for concurrent use.
+ * later pkv_paged_attention(_noalloc) and pkv_paged_prefill launch (not to
+ * the CUDA-core kernel, which has no waits) until they are set again; not for
+ * concurrent use.
  */
 PKV_API void pkv_debug_set_wait_limit(uint64_t limit_ns, const int32_t* hold_flag);
 

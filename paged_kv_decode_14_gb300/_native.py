@@ -64,6 +64,9 @@ def lib():
             L.pkv_paged_attention_noalloc.restype = c.c_int
             L.pkv_paged_attention_noalloc.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, i32, vp, vp, i32, i32,
                                                       c.c_float, vp, i32, vp, vp]
+            L.pkv_paged_prefill.restype = c.c_int
+            L.pkv_paged_prefill.argtypes = [c.POINTER(CacheDesc), vp, i32, vp, i32, vp, vp, i32, i32, c.c_float, vp,
+                                            vp, vp]
             L.pkv_kvmgr_create.restype = vp
             L.pkv_kvmgr_create.argtypes = [i64]
             L.pkv_kvmgr_destroy.restype = None
@@ -281,6 +284,27 @@ def attention_noalloc(cache: PagedKVCache, q, block_tables, context_lens, q_lens
                                            int(context_lens.numel()), int(max_q_len), float(scale), _ptr(out),
                                            int(num_ctas), _ptr(device_error), _stream(stream))
     _check(st, "pkv_paged_attention_noalloc")
+    return out
+
+
+def prefill(cache: PagedKVCache, q, block_tables, context_lens, q_lens, max_q_len: int, scale: float, out=None,
+            device_error=None, stream=None):
+    """pkv_paged_prefill: causal attention of long query windows (prompts or
+    prompt chunks) on the tensor cores; q bf16 [sum q_lens, Hq, D] -> out of
+    the same shape.  bf16 caches, Hq / Hkv dividing 128."""
+    if q.dtype != torch.bfloat16 or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be contiguous bfloat16 [rows, Hq, D]")
+    for t, name in ((block_tables, "block_tables"), (context_lens, "context_lens"), (q_lens, "q_lens")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+    if out is None:
+        out = torch.empty_like(q)
+    d = cache.desc()
+    st = lib().pkv_paged_prefill(ctypes.byref(d), _ptr(q), int(q.shape[1]), _ptr(block_tables),
+                                 int(block_tables.shape[1]), _ptr(context_lens), _ptr(q_lens),
+                                 int(context_lens.numel()), int(max_q_len), float(scale), _ptr(out),
+                                 _ptr(device_error), _stream(stream))
+    _check(st, "pkv_paged_prefill")
     return out
 
 

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "api_noalloc.cu", "append.cu", "attn_simt.cu", "attn_tc.cu", "rope_append.cu", "kvmgr.cpp"]
+SOURCES = ["api.cu", "api_noalloc.cu", "append.cu", "attn_simt.cu", "attn_tc.cu", "prefill.cu", "rope_append.cu", "kvmgr.cpp"]
 
 
 def nvcc() -> str:

@@ -16,6 +16,7 @@ cudaError_t launch_copy_blocks(const pkv_cache& c, const int32_t* pairs, int n, 
                                cudaStream_t st, int num_sms);
 cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st);
+cudaError_t launch_prefill(const AttnParams& p, int head_dim, cudaStream_t st);
 int simt_rows_pad(int rows);
 int tc_heads_per_segment(int num_kv_heads, int rows);
 
@@ -273,6 +274,49 @@ PKV_API pkv_status pkv_paged_attention(const pkv_cache* cache, const void* q, in
     const int E = cache->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
     cudaError_t e = launch_attention(L, p, cache->head_dim, E, (cudaStream_t)stream);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+PKV_API pkv_status pkv_paged_prefill(const pkv_cache* cache, const void* q, int32_t num_q_heads,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, const int32_t* q_lens, int32_t num_seqs,
+                                     int32_t max_q_len, float scale, void* out, int32_t* device_error,
+                                     void* stream) {
+    pkv_status s = check_cache(cache);
+    if (s != PKV_OK) return s;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
+    if (cache->kv_dtype != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
+    const int group = num_q_heads / cache->num_kv_heads;
+    if (128 % group) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !out || !block_tables || !context_lens || !q_lens) return PKV_ERR_INVALID_ARG;
+    if (max_blocks_per_seq <= 0 || max_q_len < 1) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+    const int64_t qblocks = ((int64_t)max_q_len * group + 127) / 128;
+    if ((int64_t)num_seqs * cache->num_kv_heads * qblocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+    AttnParams p = {};
+    p.k_cache = (const uint8_t*)cache->k_cache;
+    p.v_cache = (const uint8_t*)cache->v_cache;
+    p.q = (const __nv_bfloat16*)q;
+    p.out = (__nv_bfloat16*)out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.q_lens = q_lens;
+    p.err = device_error;
+    p.num_blocks = cache->num_blocks;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.group = group;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_q_len = max_q_len;
+    p.scale_log2 = scale * kLog2e;
+    p.hg = 1;
+    p.kv_split = 1;
+    p.cache_kv_heads = cache->num_kv_heads;
+    p.num_seqs_total = num_seqs;
+    fill_debug(p);
+    return launch_prefill(p, cache->head_dim, (cudaStream_t)stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 PKV_API void pkv_debug_set_wait_limit(uint64_t limit_ns, const int32_t* hold_flag) {

@@ -54,9 +54,14 @@ class DeviceWorkload:
                                       k_scales=ks, v_scales=vs)
         self.reset_cache()
         self.num_ctas = num_ctas
-        self.workspace = nat.make_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                            max(1, w.max_q_len), num_ctas, device=dev)
+        # the decode/verify kernels' workspace (their query windows are at most
+        # 16 long; longer windows go to the prefill kernel, which needs none)
+        self.workspace = None
+        if max(1, w.max_q_len) <= 16:
+            self.workspace = nat.make_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                max(1, w.max_q_len), num_ctas, device=dev)
         self.append_err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.prefill_err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty_like(self.q)
 
     def pinned_io(self) -> torch.Tensor:
@@ -109,6 +114,14 @@ class DeviceWorkload:
                                      self.max_group_q, w.scale, self.cascade_ws,
                                      out=self.out if out is None else out, stream=stream)
 
+    def attend_prefill(self, out=None, stream=None):
+        """Causal attention of the step's query windows on the chunked-prefill
+        kernel (pkv_paged_prefill; bf16 caches, any window length)."""
+        w = self.w
+        return nat.prefill(self.cache, self.q, self.block_tables, self.context_lens, self.q_lens,
+                           max(1, w.max_q_len), w.scale, out=self.out if out is None else out,
+                           device_error=self.prefill_err, stream=stream)
+
     def step(self, stream=None):
         """One decode step: append the new tokens, then attend."""
         self.append_step(stream)
@@ -124,10 +137,14 @@ class DeviceWorkload:
         return k, v
 
     def errors(self):
-        """(attention workspace error bits, append error bits); clears both.
+        """(attention error bits: workspace and prefill words, append error
+        bits); clears them.
         After a timeout the workspace may hold merge tickets of the aborted
         call: it is zeroed again, ready for the next call."""
-        a = nat.read_device_error(self.workspace)
-        if a & nat.DEVERR_TIMEOUT:
-            nat.workspace_init(self.workspace)
+        a = nat.read_device_error(self.prefill_err)
+        if self.workspace is not None:
+            ws = nat.read_device_error(self.workspace)
+            if ws & nat.DEVERR_TIMEOUT:
+                nat.workspace_init(self.workspace)
+            a |= ws
         return a, nat.read_device_error(self.append_err)
