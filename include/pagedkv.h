@@ -73,7 +73,7 @@ typedef enum pkv_status {
     PKV_ERR_UNSUPPORTED = 2,   /* head_dim / block_size / dtype / group size not built */
     PKV_ERR_WORKSPACE = 3,     /* workspace missing or too small */
     PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
-    PKV_ERR_DEVICE_INDEX = 5,  /* device error word: bad block id / slot / length */
+    PKV_ERR_DEVICE_INDEX = 5,  /* device error word: bad block id / slot / length / value range */
     PKV_ERR_TIMEOUT = 6,       /* device error word: a bounded wait gave up */
     PKV_ERR_NO_BLOCKS = 7,     /* block manager: no free block and none evictable */
     PKV_ERR_UNKNOWN_SEQ = 8    /* block manager: no sequence with that id (or it exists already) */
@@ -86,6 +86,7 @@ typedef enum pkv_kv_dtype { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
 #define PKV_DEVERR_LENGTH 2     /* q_len > context_len, or a negative length */
 #define PKV_DEVERR_SLOT 4       /* slot >= num_blocks * 16 in an append */
 #define PKV_DEVERR_TIMEOUT 8    /* a bounded wait inside a kernel expired */
+#define PKV_DEVERR_RANGE 16     /* pkv_paged_prefill: a finite V value of magnitude >= 65536 */
 
 /* One paged cache ("startup policy": fixed for its lifetime). */
 typedef struct pkv_cache {
@@ -282,23 +283,28 @@ PKV_API pkv_status pkv_paged_attention_cascade(const pkv_cache* cache, const voi
  * prefill FlashAttention on tensor cores; inferd backlog, chunked prefill).
  * The same definition as pkv_paged_attention: query i (0 <= i < Q_b) of head
  * h sees positions 0 .. L_b - Q_b + i of kv-head h / G through the block
- * table, fp32 accumulation, bf16 output (nearest even); the tensor-core
- * products take the softmax weights rounded to bf16.
+ * table, fp32 accumulation, bf16 output (nearest even).  Precision: q.k in
+ * bf16 x bf16 -> fp32; the weights times V in fp16 x fp16 -> fp32 (the
+ * weights rounded to fp16, 11 significant bits; V converted exactly, bf16
+ * values carrying 8), so an output is off by at most about 2^-11 * max|v|
+ * over the keys it sees, plus rounding of fp32 sums.  A finite V value of
+ * magnitude >= 65536 (beyond fp16) sets PKV_DEVERR_RANGE and the outputs of
+ * its CTA are unspecified.
  *
  *   q, out, block_tables, context_lens, q_lens, scale
  *                  as for pkv_paged_attention (q and out packed by sequence,
  *                  sum(q_lens) rows).
  *   max_q_len      host upper bound of q_lens (>= 1, no upper limit beyond
- *                  the grid size: num_seqs * Hkv * ceil(max_q_len * G / 128)
+ *                  the grid size: num_seqs * Hkv * ceil(max_q_len * G / 256)
  *                  < 2^31 CTAs).
  *   device_error   optional device int32 error word (PKV_DEVERR_* bits: bad
- *                  block id, bad lengths, a wait that ran out); NULL: not
- *                  reported.  No workspace.
+ *                  block id, bad lengths, a V value out of range, a wait
+ *                  that ran out); NULL: not reported.  No workspace.
  *
  * Supported: bf16 caches (FP8: PKV_ERR_UNSUPPORTED), head_dim 64 or 128, GQA
  * groups G = Hq / Hkv that divide 128.  One launch on `stream` (programmatic
  * dependent launch, as pkv_paged_attention; it reads nothing before the
- * previous kernel completes): one CTA per 128 query rows (128 / G positions x
+ * previous kernel completes): one CTA per 256 query rows (256 / G positions x
  * the G heads) of one (sequence, kv-head).  Deterministic.  A NaN stored in
  * the V row of a window token also reaches the queries of the same CTA that
  * do not see it (their zero weights multiply it in the same tensor-core

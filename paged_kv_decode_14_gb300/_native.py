@@ -22,7 +22,7 @@ KV_BF16, KV_FP8_E4M3 = 0, 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "workspace missing or too small",
           4: "CUDA error", 5: "device-side index or length error", 6: "device-side wait timed out",
           7: "no free cache block and none evictable", 8: "unknown (or already registered) sequence id"}
-DEVERR_BLOCK_ID, DEVERR_LENGTH, DEVERR_SLOT, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_BLOCK_ID, DEVERR_LENGTH, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_RANGE = 1, 2, 4, 8, 16
 
 _lock = threading.Lock()
 _lib = None

@@ -175,7 +175,7 @@ PKV_API const char* pkv_status_string(pkv_status s) {
         case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
         case PKV_ERR_WORKSPACE: return "workspace missing or too small";
         case PKV_ERR_CUDA: return "CUDA error";
-        case PKV_ERR_DEVICE_INDEX: return "device-side index or length error";
+        case PKV_ERR_DEVICE_INDEX: return "device-side index, length or value-range error";
         case PKV_ERR_TIMEOUT: return "device-side wait timed out";
         case PKV_ERR_NO_BLOCKS: return "no free cache block and none evictable";
         case PKV_ERR_UNKNOWN_SEQ: return "unknown (or already registered) sequence id";
@@ -292,7 +292,7 @@ PKV_API pkv_status pkv_paged_prefill(const pkv_cache* cache, const void* q, int3
     if (max_blocks_per_seq <= 0 || max_q_len < 1) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
     if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
-    const int64_t qblocks = ((int64_t)max_q_len * group + 127) / 128;
+    const int64_t qblocks = ((int64_t)max_q_len * group + 255) / 256;
     if ((int64_t)num_seqs * cache->num_kv_heads * qblocks > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
     AttnParams p = {};
     p.k_cache = (const uint8_t*)cache->k_cache;

@@ -6,27 +6,33 @@
 // table equals dense attention): query i of sequence b, query head h, sees
 // positions 0 .. L_b - Q_b + i of kv-head h / G.
 //
-// A CTA owns 128 query rows of one kv-head: 128 / G consecutive query
-// positions x the G heads of the group (row r = position r / G, head r % G),
-// so every K/V page it streams serves all of them.  It walks 128-key tiles
-// (8 pages) up to its rows' causal limit:
-//   S[128 rows, 128 keys] = Q[128, D] . K_tile^T      (M=128, N=128, K-major A and B from shared memory)
+// A CTA owns 256 query rows of one kv-head -- 256 / G consecutive query
+// positions x the G heads of the group (row r = position r / G, head r % G) --
+// as two 128-row tiles, so every K/V page it streams serves 256 rows.  It
+// walks 128-key tiles (8 pages) up to its rows' causal limit; per key tile t
+// and row tile i:
+//   S_i[128 rows, 128 keys] = Q_i . K_t^T          (M=128, N=128, K-major A and B in shared memory)
 //   softmax per row (one thread per row = TMEM lane, two reads of S: max, then P)
-//   O[128 rows, D] += P_hi . V_tile + P_lo . V_tile   (M=128, N=D, A from TMEM, B MN-major in shared memory)
-// S (two buffers), P and O live in TMEM.  P = 2^(s - m) is split into a bf16
-// high part and the bf16 rounding of its remainder, so the weights keep ~16
-// significant bits (one bf16 P misses the 2e-3 tolerance on rows that
-// average a handful of keys); P_hi is written over the S columns already
-// read, P_lo into its own columns.  The cache's page layout is already the
-// canonical no-swizzle operand layout: K pages are K-major B operands, V pages
-// MN-major B operands, so pages go HBM -> shared memory by 1-D bulk copies.
-// O is rescaled in TMEM only when a row's maximum rises by more than 2^8
-// (exp2 units).  Every mbarrier wait is bounded (the launch's wait limit).
+//   O_i[128 rows, D] += P_hi . V_t + P_lo . V_t    (M=128, N=D, A from TMEM, B MN-major in shared memory)
+// S, P and O live in TMEM (S_0, S_1: 128 columns each; O_0, O_1: D each).
+// P = 2^(s - m) is split into a bf16 high part and the bf16 rounding of its
+// remainder, so the weights keep ~16 significant bits (one bf16 P misses the
+// 2e-3 tolerance on rows that average a handful of keys).  Each 16-key chunk
+// of S is replaced in place by its 8 columns of P_hi pairs and 8 of P_lo
+// pairs.  The cache's page layout is already the canonical no-swizzle operand
+// layout: K pages are K-major B operands, V pages MN-major B operands, so
+// pages go HBM -> shared memory by 1-D bulk copies.  O is rescaled in TMEM
+// only when a row's maximum rises by more than 2^8 (exp2 units).
 //
-// Roles: warps 0-3 softmax and epilogue (thread = row), warp 4 producer (block
-// table, bulk copies), warp 5 MMA issuer (S of tile t, then P.V of tile t - 1;
-// tcgen05.mma ops of one thread run in issue order, so S of tile t + 2 is
-// written over P_hi of tile t only after P.V of tile t has read it).
+// Roles: warps 0-3 softmax of row tile 0, warps 4-7 of row tile 1 (thread =
+// row; they also run the epilogue), warp 8 producer (block table, bulk
+// copies), warp 9 MMA issuer, in the order
+//   S_0(0) S_1(0) | PV_0(0) S_0(1) PV_1(0) S_1(1) | PV_0(1) S_0(2) ...
+// so one row tile's softmax runs while the tensor core works for the other.
+// tcgen05.mma ops of one thread run in issue order: S_i(t + 1) overwrites P_i
+// only after PV_i(t) has read it, and when S_i(t + 1) signals, PV_i(t) has
+// completed, so the softmax may rescale O_i without another wait.  Every
+// mbarrier wait is bounded (the launch's wait limit).
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -35,11 +41,12 @@ namespace prefill {
 
 using namespace ptx;
 
-constexpr int kRows = 128;                // query rows per CTA (MMA M)
+constexpr int kRows = 128;                // rows per row tile (MMA M)
+constexpr int kCtaRows = 2 * kRows;       // rows per CTA
 constexpr int kTP = 8;                    // pages per key tile
 constexpr int kKeys = kTP * kBlock;       // 128 keys per tile (MMA N of S)
-constexpr int kThreads = 192;             // 4 softmax warps, producer, MMA issuer
-constexpr int kProducer = 4, kMma = 5;
+constexpr int kThreads = 384;             // 8 softmax warps, K producer, V producer, 2 MMA issuers
+constexpr int kProdK = 8, kProdV = 9, kMma = 10;   // MMA issuers: warps 10 and 11
 constexpr float kSlack = 8.f;             // rescale O only when a row's max rises by more than 2^8
 
 template <int D>
@@ -47,23 +54,24 @@ struct Cfg {
     static constexpr int NCH = D / 8;                     // 16-byte chunks per row of D bf16
     static constexpr int PAGE = kBlock * D * 2;           // a bf16 page
     static constexpr int TILE = kTP * PAGE;
-    static constexpr int NS = D == 128 ? 3 : 4;           // K and V ring depth (tiles)
-    static constexpr int OFF_Q = 0;                       // Q [16 row groups][D/8][8][8]
-    static constexpr int QBYTES = kRows * D * 2;
-    static constexpr int OFF_K = OFF_Q + QBYTES;          // K ring
-    static constexpr int OFF_V = OFF_K + NS * TILE;       // V ring
-    static constexpr int OFF_BAR = OFF_V + NS * TILE;
-    // barriers: KFULL[NS] VFULL[NS] KEMPTY[NS] VEMPTY[NS] SFULL[2] PFULL[2] PEMPTY[2] QFULL ODONE
-    static constexpr int KFULL = 0, VFULL = NS, KEMPTY = 2 * NS, VEMPTY = 3 * NS, SFULL = 4 * NS,
-                         PFULL = 4 * NS + 2, PEMPTY = 4 * NS + 4, QFULL = 4 * NS + 6, ODONE = 4 * NS + 7;
-    static constexpr int NBAR = 4 * NS + 8;
+    static constexpr int NSK = D == 128 ? 2 : 4;          // K ring depth (tiles)
+    static constexpr int NSV = D == 128 ? 3 : 4;          // V ring depth: V(t + 1) lands during tile t
+    static constexpr int QBYTES = kRows * D * 2;          // one row tile of Q: [16 row groups][D/8][8][8]
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + 2 * QBYTES;      // K ring
+    static constexpr int OFF_V = OFF_K + NSK * TILE;      // V ring
+    static constexpr int OFF_BAR = OFF_V + NSV * TILE;
+    // barriers: KFULL[NSK] KEMPTY[NSK] VFULL[NSV] VEMPTY[NSV] VREADY[NSV] SFULL[2] PFULL[2] QFULL ODONE[2] DRAIN
+    static constexpr int KFULL = 0, KEMPTY = NSK, VFULL = 2 * NSK, VEMPTY = 2 * NSK + NSV,
+                         VREADY = 2 * NSK + 2 * NSV, SFULL = 2 * NSK + 3 * NSV, PFULL = SFULL + 2,
+                         QFULL = SFULL + 4, ODONE = SFULL + 5, DRAIN = SFULL + 7;
+    static constexpr int NBAR = SFULL + 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem address, abort flags, qoff
     static constexpr int SMEM = OFF_MISC + 16 + 128;      // (+ alignment slack)
-    // TMEM columns: S / P_hi [2] x 128, O (D), P_lo [2] x 64
+    // TMEM columns: S/P_0, S/P_1 (128 each), O_0, O_1 (D each)
     static constexpr int COL_O = 2 * kKeys;
-    static constexpr int COL_LO = COL_O + D;
     static constexpr int TMEM_COLS = 512;
-    static_assert(COL_LO + 2 * (kKeys / 2) <= TMEM_COLS, "tensor memory budget");
+    static_assert(COL_O + 2 * D <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM <= 232448 - 1024, "shared memory budget");
 };
 
@@ -98,6 +106,26 @@ __device__ __forceinline__ float exp2_fast(float x) {
     return y;
 }
 
+// Two fp32 lanes in one 64-bit register (the sm_100 family's packed fp32 arithmetic).
+__device__ __forceinline__ uint64_t f2pack(uint32_t a, uint32_t b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p, int qblocks) {
     using K = Cfg<D>;
@@ -106,8 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
     const uint32_t sb = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     auto bar = [&](int i) -> uint32_t { return sb + K::OFF_BAR + 8 * i; };
-    constexpr int NS = K::NS, KFULL = K::KFULL, VFULL = K::VFULL, KEMPTY = K::KEMPTY, VEMPTY = K::VEMPTY,
-                  SFULL = K::SFULL, PFULL = K::PFULL, PEMPTY = K::PEMPTY, QFULL = K::QFULL, ODONE = K::ODONE;
+    constexpr int NSK = K::NSK, NSV = K::NSV, KFULL = K::KFULL, VFULL = K::VFULL, KEMPTY = K::KEMPTY,
+                  VEMPTY = K::VEMPTY, VREADY = K::VREADY,
+                  SFULL = K::SFULL, PFULL = K::PFULL, QFULL = K::QFULL, ODONE = K::ODONE,
+                  DRAIN = K::DRAIN;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 4);
     int* s_qoff = reinterpret_cast<int*>(smem + K::OFF_MISC + 8);
@@ -117,9 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
 
     griddep_launch();
     griddep_wait();
-    // this CTA: sequence b, kv-head g, query block qb of 128 / G positions (the
+    // this CTA: sequence b, kv-head g, query block qb of 256 / G positions (the
     // last blocks, which see the most keys, first)
-    const int G = p.group, QP = kRows / G;
+    const int G = p.group, QP = kCtaRows / G;
     const int qb = qblocks - 1 - (int)(blockIdx.x % qblocks), g = (blockIdx.x / qblocks) % p.num_kv_heads,
               b = blockIdx.x / (qblocks * p.num_kv_heads);
     const int L = p.context_lens[b], Q = p.q_lens[b];
@@ -129,24 +159,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
     if (bad && q0 == 0 && g == 0 && tid == 0 && Q != 0) raise_error(p.err, PKV_DEVERR_LENGTH);
     if (bad || q0 >= Q) return;
     const int nq = min(QP, Q - q0);                       // query positions of this CTA
+    const bool two = nq * G > kRows;                      // row tile 1 holds rows of the window
     const int lim_max = L - Q + q0 + nq - 1;              // last key any of its rows sees
     const int T = lim_max / kKeys + 1;                    // key tiles
     const int nb = (L + kBlock - 1) / kBlock;             // pages of the sequence
 
     if (tid == 0) {
-        for (int i = 0; i < NS; ++i) {
+        const int nt = two ? 2 : 1;                       // MMA issuers that release K and V slots
+        for (int i = 0; i < NSK; ++i) {
             mbar_init(bar(KFULL + i), 1);
+            mbar_init(bar(KEMPTY + i), nt);
+        }
+        for (int i = 0; i < NSV; ++i) {
             mbar_init(bar(VFULL + i), 1);
-            mbar_init(bar(KEMPTY + i), 1);
-            mbar_init(bar(VEMPTY + i), 1);
+            mbar_init(bar(VEMPTY + i), nt);
+            mbar_init(bar(VREADY + i), kRows);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(SFULL + i), 1);
             mbar_init(bar(PFULL + i), kRows);
-            mbar_init(bar(PEMPTY + i), 1);
         }
-        mbar_init(bar(QFULL), kRows);
+        mbar_init(bar(QFULL), kCtaRows);
         mbar_init(bar(ODONE), 1);
+        mbar_init(bar(ODONE + 1), 1);
+        mbar_init(bar(DRAIN), nt);
         *abort_flag = 0;
         *drain_flag = 0;
         mbar_fence_init();
@@ -167,20 +203,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
     const uint32_t tmem = *tmem_slot;
     const int qoff = *s_qoff;
 
-    if (warp < 4) {
-        // ------------------------------------------------ softmax / epilogue: thread r = row r
-        const int r = tid, qi = r / G, hl = r - qi * G;
+    if (warp < 8) {
+        // ------------------------------------------------ softmax / epilogue: row tile i, thread r = row r
+        const int i = warp >> 2, r = tid & (kRows - 1);
+        const int R = i * kRows + r, qi = R / G, hl = R - qi * G;
         const bool row_ok = qi < nq;
         const int qpos = L - Q + q0 + qi;                 // this row's query position (last key it sees)
-        const uint32_t lbase = (uint32_t)(warp * 32) << 16;
-        // q row -> Q tile (K-major core matrices), zeros for rows past the window
+        const uint32_t lbase = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t scol = tmem + lbase + i * kKeys;   // S_i / P_i
+        const uint32_t ocol = tmem + lbase + K::COL_O + i * D;
+        // q row -> Q tile i (K-major core matrices), zeros for rows past the window
         {
             const uint4* src = reinterpret_cast<const uint4*>(
                 p.q + ((size_t)(qoff + q0 + qi) * p.num_q_heads + g * G + hl) * D);
-            uint8_t* dst = smem + K::OFF_Q + (r >> 3) * (K::NCH * 128) + (r & 7) * 16;
-#pragma unroll 4
-            for (int c = 0; c < K::NCH; ++c)
-                *reinterpret_cast<uint4*>(dst + c * 128) = row_ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            uint8_t* dst = smem + K::OFF_Q + i * K::QBYTES + (r >> 3) * (K::NCH * 128) + (r & 7) * 16;
+            uint4 qv[K::NCH];                              // all loads in flight at once
+#pragma unroll
+            for (int c = 0; c < K::NCH; ++c) qv[c] = row_ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int c = 0; c < K::NCH; ++c) *reinterpret_cast<uint4*>(dst + c * 128) = qv[c];
             fence_proxy_async_smem();
             mbar_arrive(bar(QFULL));
         }
@@ -188,102 +229,279 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
         const int lim = row_ok ? qpos : -1;
         // every wait and every TMEM access of the loop is warp-uniform (tcgen05.ld/st are .aligned)
         auto wait_all = [&](uint32_t bb, uint32_t parity) { return __all_sync(0xffffffffu, wait(bb, parity, ctl)); };
-        float m = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int t = 0; t < T && ok; ++t) {
-            const int s = t & 1;
-            if (!(ok = wait_all(bar(SFULL + s), (t >> 1) & 1))) break;
-            tc_fence_after();
-            const uint32_t scol = tmem + lbase + s * kKeys;
-            const int rem = lim - t * kKeys;               // column c is visible iff c <= rem
-            // pass 1: the tile's maximum for this row
-            float tmax = -INFINITY;
+        const float sc = p.scale_log2;
+        int rem_c = 0;                                     // this tile: column c is visible iff c <= rem_c
+        // P of 32 keys (S values rr, columns c .. c + 31) -> 16 columns of fp16 pairs (the even key
+        // in the low half) at column c / 2, over S columns already read.  MASK: keys past this
+        // row's limit weigh 0.  Adds P to ls[].
+        auto emit = [&](const uint32_t (&rr)[32], int c, float mref, bool mask, float (&ls)[2]) {
+            uint32_t w[16];
 #pragma unroll
-            for (int c = 0; c < kKeys; c += 16) {
-                float v[16];
-                tmem_ld16(scol + c, v);
-#pragma unroll
-                for (int x = 0; x < 16; ++x) tmax = fmaxf(tmax, c + x <= rem ? v[x] * p.scale_log2 : -INFINITY);
-            }
-            // a new maximum more than 2^8 above the running one: rescale l and O
-            const bool grow = tmax > m + kSlack || (m == -INFINITY && tmax > -INFINITY);
-            const float alpha = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2_fast(m - tmax));
-            if (t > 0 && __any_sync(0xffffffffu, grow && m != -INFINITY)) {
-                // O *= alpha (1 for the warp's other rows), once the previous tile's P.V has landed
-                if (!(ok = wait_all(bar(PEMPTY + ((t - 1) & 1)), ((t - 1) >> 1) & 1))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < D; c += 16) {
-                    float o[16];
-                    tmem_ld16(tmem + lbase + K::COL_O + c, o);
-#pragma unroll
-                    for (int x = 0; x < 16; ++x) o[x] *= alpha;
-                    tmem_st16(tmem + lbase + K::COL_O + c, o);
+            for (int k = 0; k < 32; k += 2) {
+                float p0 = exp2_fast(fmaf(__uint_as_float(rr[k]), sc, -mref));
+                float p1 = exp2_fast(fmaf(__uint_as_float(rr[k + 1]), sc, -mref));
+                if (mask) {
+                    p0 = c + k <= rem_c ? p0 : 0.f;
+                    p1 = c + k + 1 <= rem_c ? p1 : 0.f;
                 }
+                ls[0] += p0;
+                ls[1] += p1;
+                const __half2 h = __floats2half2_rn(p0, p1);
+                w[k >> 1] = *reinterpret_cast<const uint32_t*>(&h);
             }
+            tmem_st16u(scol + (c >> 1), w);
+        };
+        // O_i *= alpha (1 for rows that keep their reference); warp-uniform
+        auto rescale_o = [&](float alpha) {
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                float o[32];
+                tmem_ld32(ocol + c, o);
+                uint32_t w[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) w[x] = __float_as_uint(o[x] * alpha);
+                tmem_st16u(ocol + c, w);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) w[x] = __float_as_uint(o[16 + x] * alpha);
+                tmem_st16u(ocol + c + 16, w);
+            }
+            tmem_wait_st();
+        };
+        // m: this row's reference maximum (exp2 units); pend: a maximum that the last tile raised
+        // by more than the slack, applied to l and O when the next tile starts (PV_i of the last
+        // tile has completed by then).  In one pass, P = 2^(s - m) is kept below 2^kBig (inside
+        // the fp16 range): a chunk that would exceed it first raises m by a whole number k of
+        // octaves, and the P this tile already holds, O and l are scaled by 2^-k (exact but for
+        // fp16 subnormals: weights below 2^-14 of the new maximum).
+        constexpr float kBig = 15.f;
+        float m = -INFINITY, l = 0.f, pend = -INFINITY;
+        auto raise_ref = [&](float target, int c, uint64_t& acc) {
+            const float inc = target > m + kBig ? fminf(ceilf(target - m), 254.f) : 0.f;
+            const int k = (int)inc;
+            const float alpha = k < 127 ? __uint_as_float((uint32_t)(127 - k) << 23) : 0.f;
+#pragma unroll 1
+            for (int cc = 0; cc < c / 2; cc += 16) {          // the P columns written so far
+                float o[16];
+                tmem_ld16(scol + cc, o);
+                uint32_t w[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const uint32_t u = __float_as_uint(o[x]);
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u));
+                    const __half2 h = __floats2half2_rn(f.x * alpha, f.y * alpha);
+                    w[x] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                tmem_st16u(scol + cc, w);
+            }
+            rescale_o(alpha);
             l *= alpha;
-            if (grow) m = tmax;
-            // pass 2: P = 2^(s - m) -> P_hi over the S columns already read, P_lo in its own
-            // columns (column j / 2 of a part holds keys j, j + 1; the even key in the low half).
-            // Their previous contents were read by the P.V of tile t - 2, which completed
-            // before S of tile t (issued after it) signalled SFULL.
-            const uint32_t phi = tmem + lbase + s * kKeys, plo = tmem + lbase + K::COL_LO + s * (kKeys / 2);
+            float a0, a1;
+            f2unpack(acc, a0, a1);
+            acc = f2pack(__float_as_uint(a0 * alpha), __float_as_uint(a1 * alpha));
+            m += inc;
+        };
+        // P of 32 keys no mask touches, two keys per packed fp32 operation; unless FORCE, nothing is
+        // stored (false) when some P would reach 2^kBig (or is NaN).  Adds the chunk's P to acc and
+        // the largest fp16 P bit pattern (P >= 0: integer order is value order) to pmaxw.
+        auto emit_fast = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, uint32_t& pmaxw, bool force) -> bool {
+            const uint64_t sc2 = f2pack(__float_as_uint(sc), __float_as_uint(sc));
+            const uint64_t nm2 = f2pack(__float_as_uint(-m), __float_as_uint(-m));
+            uint64_t ca = 0;                               // (+0, +0)
+            uint32_t w[16], cm = 0;
 #pragma unroll
-            for (int c = 0; c < kKeys; c += 16) {
-                float v[16];
-                tmem_ld16(scol + c, v);
-                uint32_t wh[8], wl[8];
+            for (int k = 0; k < 32; k += 2) {
+                float x0, x1;
+                f2unpack(f2fma(f2pack(rr[k], rr[k + 1]), sc2, nm2), x0, x1);
+                const float p0 = exp2_fast(x0), p1 = exp2_fast(x1);
+                ca = f2add(ca, f2pack(__float_as_uint(p0), __float_as_uint(p1)));
+                const __half2 h = __floats2half2_rn(p0, p1);
+                w[k >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+                cm = __vmaxu2(cm, w[k >> 1]);
+            }
+            if (!force && __any_sync(0xffffffffu, (cm & 0xffffu) >= 0x7800u || (cm >> 16) >= 0x7800u)) return false;
+            acc = f2add(acc, ca);
+            pmaxw = __vmaxu2(pmaxw, cm);
+            tmem_st16u(scol + (c >> 1), w);
+            return true;
+        };
+        auto chunk = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, uint32_t& pmaxw) {
+            if (emit_fast(rr, c, acc, pmaxw, false)) return;
+            // (rare) a logit more than 2^kBig above the reference: raise it first
+            float c0 = -INFINITY, c1 = -INFINITY;
 #pragma unroll
-                for (int x = 0; x < 16; x += 2) {
-                    const float p0 = c + x <= rem ? exp2_fast(v[x] * p.scale_log2 - m) : 0.f;
-                    const float p1 = c + x + 1 <= rem ? exp2_fast(v[x + 1] * p.scale_log2 - m) : 0.f;
-                    l += p0 + p1;
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                    const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(h), p1 - __high2float(h));
-                    wh[x >> 1] = *reinterpret_cast<const uint32_t*>(&h);
-                    wl[x >> 1] = *reinterpret_cast<const uint32_t*>(&lo);
+            for (int x = 0; x < 32; x += 2) {
+                c0 = fmaxf(c0, __uint_as_float(rr[x]));
+                c1 = fmaxf(c1, __uint_as_float(rr[x + 1]));
+            }
+            raise_ref(fmaxf(c0, c1) * sc, c, acc);
+            emit_fast(rr, c, acc, pmaxw, true);             // (P <= 1 now, but for NaN logits)
+        };
+        // one pass over a tile no mask touches, loads of the next 32 columns in flight while the
+        // previous 32 are turned into P; returns the tile's sum of P, and in pmaxw its largest P
+        auto fast_pass = [&](uint32_t& pmaxw) -> float {
+            uint64_t acc = 0;
+            pmaxw = 0;
+            uint32_t ra[32], rb[32];
+            tmem_ld32_async(scol, ra);
+            tmem_wait_ld_into(ra);
+#pragma unroll 1
+            for (int c = 0; c < kKeys; c += 64) {
+                tmem_ld32_async(scol + c + 32, rb);
+                chunk(ra, c, acc, pmaxw);
+                tmem_wait_ld_into(rb);
+                if (c + 64 < kKeys) tmem_ld32_async(scol + c + 64, ra);
+                chunk(rb, c + 32, acc, pmaxw);
+                if (c + 64 < kKeys) tmem_wait_ld_into(ra);
+            }
+            float a0, a1;
+            f2unpack(acc, a0, a1);
+            return a0 + a1;
+        };
+        // V(t), once landed, from bf16 to fp16 in place for the fp16 P.V products, by row tile 0:
+        // V(t + 1) right after it signals P_0(t), while its next S is computed, so that its P_0(t + 1)
+        // signal also says V(t + 1) is ready; VREADY tells row tile 1's MMA issuer.
+        // Exact for |v| < 65536
+        // (bf16 values carry 8 significant bits; below 2^-14 they become fp16 subnormals, off by
+        // less than 2^-25); a finite |v| >= 65536 sets PKV_DEVERR_RANGE.  The last page's
+        // unwritten slots become 0 (they may hold NaN).
+        constexpr int CPP = K::PAGE / 16;                  // 16-byte chunks per page
+        const int valid_last = L - (nb - 1) * kBlock;      // tokens of the sequence's last page
+        uint32_t vmaxbits = 0;                             // largest |bf16| bit patterns seen (two halves)
+        auto convert_v = [&](int t) -> bool {
+            const int s = t % NSV, np = min(kTP, nb - t * kTP), lastpg = nb - 1 - t * kTP;
+            if (!wait_all(bar(VFULL + s), (t / NSV) & 1)) return false;
+            uint4* base = reinterpret_cast<uint4*>(smem + K::OFF_V + s * K::TILE);
+            for (int pg = 0; pg < np; ++pg) {
+                uint4* pgp = base + pg * CPP;
+                const bool last = pg == lastpg && valid_last < kBlock;
+#pragma unroll
+                for (int e = r; e < CPP; e += kRows) {
+                    uint4 v = pgp[e];
+                    // chunk e of a page: token group e / (8 NCH), token (e % 8) of the group
+                    if (last && (e / (K::NCH * 8)) * 8 + (e & 7) >= valid_last) {
+                        v = make_uint4(0, 0, 0, 0);
+                    } else {
+                        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            vmaxbits = __vmaxu2(vmaxbits, w[j] & 0x7fff7fffu);
+                            const __half2 h = __floats2half2_rn(__uint_as_float(w[j] << 16),
+                                                                __uint_as_float(w[j] & 0xffff0000u));
+                            w[j] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                    }
+                    pgp[e] = v;
                 }
-                tmem_st8(phi + (c >> 1), wh);
-                tmem_st8(plo + (c >> 1), wl);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(VREADY + s));
+            return true;
+        };
+        bool ok = i == 0 || two;
+        if (ok && i == 0) ok = convert_v(0);
+        for (int t = 0; t < T && ok; ++t) {
+            if (!(ok = wait_all(bar(SFULL + i), t & 1))) break;
+            tc_fence_after();
+            rem_c = lim - t * kKeys;
+            if (__any_sync(0xffffffffu, pend > m + kSlack)) {
+                const bool up = pend > m + kSlack;
+                const float alpha = up ? exp2_fast(m - pend) : 1.f;
+                rescale_o(alpha);
+                l *= alpha;
+                if (up) m = pend;
+            }
+            pend = -INFINITY;
+            if (__all_sync(0xffffffffu, rem_c >= kKeys - 1 && m > -INFINITY) && sc > 0.f) {
+                // off the causal diagonal, reference known: one pass.  A largest P of 2^e or more
+                // (e >= kSlack) moves the reference up by e + 1 octaves at the next tile.
+                uint32_t pw;
+                l += fast_pass(pw);
+                const uint32_t pm = max(pw & 0xffffu, pw >> 16);
+                if (pm >= 0x5c00u && pm < 0x7c00u) pend = m + (float)((int)(pm >> 10) - 15 + 1);
+            } else {
+                // two passes (first tile, causal diagonal, rows past the window): the tile's
+                // maximum over the visible keys first, then P
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll 1
+                for (int c = 0; c < kKeys; c += 32) {
+                    float v[32];
+                    tmem_ld32(scol + c, v);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        mx[x & 1] = fmaxf(mx[x & 1], c + x <= rem_c ? v[x] * sc : -INFINITY);
+                }
+                const float tmax = fmaxf(mx[0], mx[1]);
+                const bool grow = tmax > m + kSlack || (m == -INFINITY && tmax > -INFINITY);
+                const float alpha = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2_fast(m - tmax));
+                if (t > 0 && __any_sync(0xffffffffu, grow && m != -INFINITY)) rescale_o(alpha);
+                l *= alpha;
+                if (grow) m = tmax;
+                // rows with nothing visible yet keep m = -inf: every P of theirs is masked to 0
+                const float mref = m == -INFINITY ? 0.f : m;
+                float ls[2] = {0.f, 0.f};
+#pragma unroll 1
+                for (int c = 0; c < kKeys; c += 32) {
+                    uint32_t rr[32];
+                    tmem_ld32_async(scol + c, rr);
+                    tmem_wait_ld_into(rr);
+                    emit(rr, c, mref, true, ls);
+                }
+                l += ls[0] + ls[1];
             }
             tmem_wait_st();
             tc_fence_before();
-            // the last page's unwritten slots: zero their V rows (they may hold NaN)
-            if (t == T - 1 && nb * kBlock > L && (nb - 1) / kTP == t) {
-                if (!(ok = wait_all(bar(VFULL + t % NS), (t / NS) & 1))) break;
-                const int tail = nb * kBlock - L, pg = (nb - 1) % kTP;
-                for (int i = r; i < tail * K::NCH; i += kRows) {
-                    const int key = kBlock - tail + i / K::NCH, c = i % K::NCH;
-                    uint8_t* vrow = smem + K::OFF_V + (t % NS) * K::TILE + pg * K::PAGE +
-                                    (key >> 3) * (K::NCH * 128) + c * 128 + (key & 7) * 16;
-                    *reinterpret_cast<uint4*>(vrow) = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
-            mbar_arrive(bar(PFULL + s));
+            mbar_arrive(bar(PFULL + i));
+            if (i == 0 && t + 1 < T && !(ok = convert_v(t + 1))) break;
         }
-        // epilogue: O / l -> out
-        if (ok && wait_all(bar(ODONE), 0)) {
+        {
+            const uint32_t lo = vmaxbits & 0xffffu, hi = vmaxbits >> 16;
+            if ((lo >= 0x4780u && lo < 0x7f80u) || (hi >= 0x4780u && hi < 0x7f80u)) raise_error(p.err, PKV_DEVERR_RANGE);
+        }
+        // epilogue: O_i / l -> bf16 rows [row][D] in the Q_i area (free: every S has completed when
+        // ODONE_i signals), then one bulk copy per run of a warp's rows that share a query position
+        // (its consecutive heads, contiguous in out)
+        if (ok && wait_all(bar(ODONE + i), 0)) {
             tc_fence_after();
-            __nv_bfloat16* dst = p.out + ((size_t)(qoff + q0 + qi) * p.num_q_heads + g * G + hl) * D;
+            uint8_t* stg = smem + K::OFF_Q + R * (D * 2);
+            const float inv = 1.f / l;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                float o[32];
+                tmem_ld32(ocol + c, o);
 #pragma unroll
-            for (int c = 0; c < D; c += 16) {
-                float o[16];
-                tmem_ld16(tmem + lbase + K::COL_O + c, o);
-                if (row_ok) {
-                    uint32_t w[8];
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t w[4];
 #pragma unroll
-                    for (int x = 0; x < 16; x += 2) {
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(__fdividef(o[x], l), __fdividef(o[x + 1], l));
-                        w[x >> 1] = *reinterpret_cast<uint32_t*>(&pr);
+                    for (int x = 0; x < 4; ++x) {
+                        __nv_bfloat162 pr = __floats2bfloat162_rn(o[h * 8 + 2 * x] * inv, o[h * 8 + 2 * x + 1] * inv);
+                        w[x] = *reinterpret_cast<uint32_t*>(&pr);
                     }
-                    *reinterpret_cast<uint4*>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4*>(dst + c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                    *reinterpret_cast<uint4*>(stg + (c + h * 8) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int R0 = R;                          // (lane 0: the warp's first row)
+                for (int Rr = R0; Rr < R0 + 32;) {
+                    const int qq = Rr / G, hh = Rr - qq * G, n = min(G - hh, R0 + 32 - Rr);
+                    if (qq < nq)
+                        bulk_s2g(p.out + ((size_t)(qoff + q0 + qq) * p.num_q_heads + g * G + hh) * D,
+                                 sb + K::OFF_Q + Rr * (D * 2), (uint32_t)(n * D * 2));
+                    Rr += n;
+                }
+                bulk_commit_group();
+                bulk_wait_all();
+            }
+            __syncwarp();
         }
-    } else if (warp == kProducer) {
-        // ------------------------------------------------ producer: K and V pages of each tile
+    } else if (warp == kProdK || warp == kProdV) {
+        // ------------------------------------------------ producers: K pages (warp 8) and V pages (warp 9)
+        // of each tile, each through its own ring (one lane per page)
+        const bool isv = warp == kProdV;
+        const int NSR = isv ? NSV : NSK, FULL = isv ? VFULL : KFULL, EMPTY = isv ? VEMPTY : KEMPTY;
+        const uint32_t ring = sb + (isv ? K::OFF_V : K::OFF_K);
+        const uint8_t* src = isv ? p.v_cache : p.k_cache;
         const int32_t* table = p.block_tables + (size_t)b * p.max_blocks_per_seq;
         int kc = 0;
         bool ok = true;
@@ -305,82 +523,84 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
             ok = __shfl_sync(0xffffffffu, w, 0);
         }
         for (int t = 0; t < T && ok; ++t) {
-            const int s = t % NS, p0 = t * kTP, np = min(kTP, nb - p0);
-            const int sl = lane & 7, kv = lane >> 3;      // lanes 0-7 copy K pages, 8-15 V pages
-            int blk = (kv < 2 && sl < np) ? __ldg(table + p0 + sl) : 0;
-            if (kv < 2 && sl < np && (blk < 0 || blk >= p.num_blocks)) {
-                if (kv == 0) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+            const int s = t % NSR, p0 = t * kTP, np = min(kTP, nb - p0);
+            int blk = lane < np ? __ldg(table + p0 + lane) : 0;
+            if (lane < np && (blk < 0 || blk >= p.num_blocks)) {
+                if (!isv) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
                 blk = 0;
             }
             bool w = true;
-            if (t >= NS) {
-                if (lane == 0) w = wait(bar(KEMPTY + s), ((t - NS) / NS) & 1, ctl);
-                if (lane == 8) w = wait(bar(VEMPTY + s), ((t - NS) / NS) & 1, ctl);
-            }
-            if (!(ok = __all_sync(0xffffffffu, w))) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(KFULL + s), np * K::PAGE);
-            if (lane == 8) mbar_arrive_expect_tx(bar(VFULL + s), np * K::PAGE);
+            if (t >= NSR && lane == 0) w = wait(bar(EMPTY + s), ((t - NSR) / NSR) & 1, ctl);
+            if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar(FULL + s), np * K::PAGE);
             __syncwarp();
-            if (kv < 2 && sl < np) {
-                const size_t off = ((size_t)blk * p.cache_kv_heads + g) * K::PAGE;
-                // (default cache policy: every query block of the sequence reads these pages, from L2)
-                bulk_g2s(sb + (kv ? K::OFF_V : K::OFF_K) + s * K::TILE + sl * K::PAGE,
-                         (kv ? p.v_cache : p.k_cache) + off, K::PAGE, bar((kv ? VFULL : KFULL) + s));
-            }
+            // (default cache policy: every query block of the sequence reads these pages, from L2)
+            if (lane < np)
+                bulk_g2s(ring + s * K::TILE + lane * K::PAGE, src + ((size_t)blk * p.cache_kv_heads + g) * K::PAGE,
+                         K::PAGE, bar(FULL + s));
             ++kc;
         }
         // drain: the copies in flight land before the CTA exits
         if (lane == 0) {
             const Ctl drain{drain_flag, p.err, p.wait_limit_ns};
-            for (int t = max(0, kc - NS); t < kc; ++t) {
-                wait(bar(KFULL + t % NS), (t / NS) & 1, drain);
-                wait(bar(VFULL + t % NS), (t / NS) & 1, drain);
-            }
+            for (int t = max(0, kc - NSR); t < kc; ++t) wait(bar(FULL + t % NSR), (t / NSR) & 1, drain);
         }
         __syncwarp();
-    } else if (warp == kMma) {
-        // ------------------------------------------------ MMA issuer: S of tile t, then P.V of tile t - 1
-        if (lane == 0) {
+    } else if (warp == kMma || warp == kMma + 1) {
+        // ------------------------------------------------ MMA issuers, one per row tile i (warp 10: i = 0,
+        // warp 11: i = 1): PV_i(t) once P_i(t) is written, then S_i(t + 1) once K(t + 1) has landed.
+        // Each row tile's S, P and O sit in its own TMEM columns and one thread's tcgen05.mma ops
+        // run in issue order; while one issuer waits for its P, the other keeps the tensor core fed.
+        const int i = warp - kMma, nt = two ? 2 : 1;    // row tiles with rows in the window
+        if (lane == 0 && i < nt) {
             constexpr uint32_t idS = idesc_bf16_f32(kRows, kKeys, false, false);
-            constexpr uint32_t idPV = idesc_bf16_f32(kRows, D, false, true);
-            const uint32_t qbase = sb + K::OFF_Q;
-            bool ok = wait(bar(QFULL), 0, ctl);
-            auto pv = [&](int u) -> bool {
-                const int su = u & 1, vs = u % NS, np = min(kTP, nb - u * kTP);
-                if (!wait(bar(PFULL + su), (u >> 1) & 1, ctl)) return false;
-                if (!wait(bar(VFULL + vs), (u / NS) & 1, ctl)) return false;
-                tc_fence_after();
-                const uint32_t vbase = sb + K::OFF_V + vs * K::TILE;
-                const uint32_t ahi = tmem + su * kKeys, alo = tmem + K::COL_LO + su * (kKeys / 2);
-                for (int pg = 0; pg < np; ++pg) {       // 16 keys per MMA: one page, 8 TMEM columns of P
-                    const uint64_t bv = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
-                    mma_bf16_tmem_a(tmem + K::COL_O, ahi + pg * 8, bv, idPV, (u > 0 || pg > 0) ? 1u : 0u);
-                    mma_bf16_tmem_a(tmem + K::COL_O, alo + pg * 8, bv, idPV, 1u);
-                }
-                mma_commit(bar(PEMPTY + su));
-                mma_commit(bar(VEMPTY + vs));
-                return true;
-            };
-            for (int t = 0; t < T && ok; ++t) {
-                const int s = t & 1, ks = t % NS;
-                if (!(ok = wait(bar(KFULL + ks), (t / NS) & 1, ctl))) break;
-                tc_fence_after();
-                const uint32_t kbase = sb + K::OFF_K + ks * K::TILE;
+            constexpr uint32_t idPV = idesc_f16_f32(kRows, D, false, true);
+            const uint32_t qbase = sb + K::OFF_Q + i * K::QBYTES, sfull = tmem + i * kKeys;
+            auto issue_s = [&](int t) {
+                const uint32_t kbase = sb + K::OFF_K + (t % NSK) * K::TILE;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint64_t a = smem_desc(qbase + k * 256, 128, K::NCH * 128);
                     const uint64_t bk = smem_desc(kbase + k * 256, 128, K::NCH * 128);
-                    mma_bf16(tmem + s * kKeys, a, bk, idS, k > 0 ? 1u : 0u);
+                    mma_bf16(sfull, a, bk, idS, k > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(SFULL + s));
-                mma_commit(bar(KEMPTY + ks));
-                if (t >= 1) ok = pv(t - 1);
+                mma_commit(bar(SFULL + i));
+                mma_commit(bar(KEMPTY + t % NSK));        // (K(t) is free once both row tiles' S(t) ran)
+            };
+            // PV_i(t): one page (16 keys = 8 columns of fp16 P_i pairs) per MMA
+            auto issue_pv = [&](int t) {
+                const int np = min(kTP, nb - t * kTP);
+                const uint32_t vbase = sb + K::OFF_V + (t % NSV) * K::TILE;
+                const uint32_t o = tmem + K::COL_O + i * D;
+                for (int pg = 0; pg < np; ++pg) {
+                    const uint64_t bv = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
+                    mma_bf16_tmem_a(o, sfull + pg * 8, bv, idPV, (t > 0 || pg > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(VEMPTY + t % NSV));
+            };
+            bool ok = wait(bar(QFULL), 0, ctl) && wait(bar(KFULL), 0, ctl);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
             }
-            if (ok) ok = pv(T - 1);
-            mma_commit(bar(ODONE));
+            for (int t = 0; t < T && ok; ++t) {
+                // row tile 0 converts V(t) (before it signals P_0(t)): row tile 1 waits for it
+                if (i == 1 && !(ok = wait(bar(VREADY + t % NSV), (t / NSV) & 1, ctl))) break;
+                if (!(ok = wait(bar(PFULL + i), t & 1, ctl))) break;
+                tc_fence_after();
+                issue_pv(t);
+                if (t + 1 < T) {
+                    if (!(ok = wait(bar(KFULL + (t + 1) % NSK), ((t + 1) / NSK) & 1, ctl))) break;
+                    tc_fence_after();
+                    issue_s(t + 1);
+                } else {
+                    mma_commit(bar(ODONE + i));
+                }
+            }
+            mma_commit(bar(DRAIN));
             // every MMA issued has completed before TMEM is freed
             const Ctl drain{drain_flag, p.err, p.wait_limit_ns};
-            wait(bar(ODONE), 0, drain);
+            wait(bar(DRAIN), 0, drain);
         }
         __syncwarp();
     }
@@ -398,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
 }  // namespace prefill
 
 cudaError_t launch_prefill(const AttnParams& p, int head_dim, cudaStream_t st) {
-    const int qblocks = (p.max_q_len * p.group + prefill::kRows - 1) / prefill::kRows;
+    const int qblocks = (int)(((int64_t)p.max_q_len * p.group + prefill::kCtaRows - 1) / prefill::kCtaRows);
     const int64_t grid = (int64_t)p.num_seqs * p.num_kv_heads * qblocks;
     if (grid < 1 || grid > 0x7fffffff) return cudaErrorInvalidValue;
     static std::atomic<uint64_t> set64{0}, set128{0};

@@ -167,3 +167,55 @@ def test_prefill_wait_timeout_reports_and_recovers():
     ref, _ = oracle.attend(w, kc, vc)
     assert_attention_close(out_bits(dw.attend_prefill()), ref, "after a timeout")
     assert dw.errors() == (0, 0)
+
+
+def test_prefill_large_logit_jumps():
+    """A key whose logits jump by tens of octaves (K = +-40 in every
+    dimension) far from the causal diagonal: rows whose running maximum
+    rises by more than 2^32 inside a tile re-reference the P already written
+    (exact power-of-two scaling), rows rising by 2^8 .. 2^32 rescale at the
+    next tile, and all stay within the tolerance of the fp64 oracle."""
+    w = wl.make_workload("jumps", context_lens=[1500, 900], q_lens=[300, 200], num_q_heads=16, num_kv_heads=4,
+                         head_dim=128, seed=716)
+    big, neg = np.uint16(0x4220), np.uint16(0xC220)        # bf16 40.0 and -40.0
+    w.prefill_k[600] = big                                 # sequence 0, position 600 (key tile 4)
+    w.prefill_k[1000] = neg                                # sequence 0, position 1000
+    w.prefill_k[1200 + 350] = big                          # sequence 1, position 350 (its prefill starts at 1200)
+    kc, vc = oracle.build_cache(w)
+    ref, _ = oracle.attend(w, kc, vc)
+    dw, got = run_prefill(w)
+    assert_attention_close(got, ref, "large logit jumps")
+    assert dw.errors() == (0, 0)
+
+
+def test_prefill_v_beyond_fp16_range_is_reported():
+    """The P.V products run in fp16: a finite V value of magnitude >= 65536
+    (here 98304) cannot be carried and sets PKV_DEVERR_RANGE; values just
+    inside the range (65280, the largest bf16 below 65504) are exact."""
+    w = wl.make_workload("range", context_lens=[300], q_lens=[100], num_q_heads=8, num_kv_heads=2, head_dim=64,
+                         seed=717)
+    w.prefill_v[50, 1, 7] = np.uint16(0x477F)              # 65280: inside the fp16 range
+    kc, vc = oracle.build_cache(w)
+    ref, _ = oracle.attend(w, kc, vc)
+    dw, got = run_prefill(w)
+    assert_attention_close(got, ref, "V = 65280")
+    assert dw.errors() == (0, 0)
+    w.prefill_v[60, 0, 3] = np.uint16(0x47C0)              # 98304
+    dw, _ = run_prefill(w)
+    a, _ = dw.errors()
+    assert a == nat.DEVERR_RANGE
+
+
+def test_prefill_nan_in_k_reaches_exactly_the_rows_that_see_it():
+    """A NaN stored in K makes every element of the rows that see that key
+    NaN (as in the definition) and leaves every other row exact: keys in
+    the one-pass tiles and on the causal diagonal, rows sharing a warp."""
+    w = wl.make_workload("nan_k", context_lens=[700, 400], q_lens=[500, 400], num_q_heads=16, num_kv_heads=4,
+                         head_dim=128, seed=718)
+    w.prefill_k[100, 2, 5] = np.uint16(0x7FC0)            # sequence 0, position 100 (resident), kv-head 2
+    w.k_new[300, 1, 0] = np.uint16(0x7FC0)                # sequence 0, position 500 (in the window), kv-head 1
+    kc, vc = oracle.build_cache(w)
+    ref, _ = oracle.attend(w, kc, vc)
+    assert np.isnan(ref).any() and not np.isnan(ref).all()
+    dw, got = run_prefill(w)
+    assert_attention_close(got, ref, "NaN in K", nan_aware=True)
