@@ -61,9 +61,27 @@ def parse():
                          "or rotate over enough copies of the workload that the data read by a step is not in L2")
     ap.add_argument("--cascade", action="store_true",
                     help="attend through the shared-prefix cascade (workloads whose sequences share prefix blocks)")
+    ap.add_argument("--prefill", nargs="?", const="prefill_b4_q2048_d128", default=None,
+                    help="time the paged chunked-prefill step (append of the window + pkv_paged_prefill) on a "
+                         "named prefill workload instead: prefill_b4_q2048_d128 (default) or "
+                         "chunked_prefill_b8_q512_d128")
     ap.add_argument("--soak-seconds", type=float, default=1.5,
                     help="untimed steps run right before the timed region while clocks are sampled")
     return ap.parse_args()
+
+
+PREFILL_METRIC = "causal prefill attention TFLOP/s (% of bf16 tensor peak)"
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def hbm_peak():
@@ -214,6 +232,192 @@ def cpu_baseline(w, seconds: float, seqs_per_step: int = 8):
         tot_t += t
         n += 1
     return tot_b / tot_t / 1e9, st.threads, n, tot_t, st.spp
+
+
+class PrefillOracleSample:
+    """The CPU oracle on a bounded slice of a prefill workload: for one
+    sequence at a time (rotating), its last `rows` queries against the whole
+    resident context (the most expensive rows).  FLOPs as causal_flops counts
+    them for those rows."""
+
+    def __init__(self, w, rows: int = 64):
+        import oracle
+        self.oracle, self.w = oracle, w
+        self.kc, self.vc = oracle.build_cache(w)
+        self.qoff = np.concatenate([[0], np.cumsum(w.q_lens)]).astype(np.int64)
+        # (the oracle spreads (sequence, kv-head) units over its threads: one sequence has Hkv of them)
+        self.threads = min(os.cpu_count() or 1, w.num_kv_heads)
+        self.rows, self.i = rows, 0
+
+    def step(self):
+        w, o = self.w, self.oracle
+        b = self.i % w.num_seqs
+        self.i += 1
+        L, Q = int(w.context_lens[b]), int(w.q_lens[b])
+        n = min(self.rows, Q)
+        rows = np.arange(self.qoff[b + 1] - n, self.qoff[b + 1])
+        t0 = time.perf_counter()
+        o.paged_attention(o.KV_BF16, self.kc, self.vc, None, None, w.num_blocks, w.num_kv_heads, w.head_dim,
+                          w.q[rows], w.num_q_heads, w.block_tables[b:b + 1], np.array([L], np.int32),
+                          np.array([n], np.int32), w.scale, self.threads)
+        el = time.perf_counter() - t0
+        keys = n * (L - n) + n * (n + 1) // 2
+        return 4 * w.head_dim * w.num_q_heads * keys, el
+
+
+def run_prefill(args):
+    """--prefill: one step = the append of every sequence's query window
+    (the prompt chunk's K/V) + pkv_paged_prefill over the batch."""
+    from paged_kv_decode_14_gb300 import workloads as wl
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.prefill not in wl.PREFILL_WORKLOADS:
+        raise SystemExit(f"unknown prefill workload {args.prefill}: {sorted(wl.PREFILL_WORKLOADS)}")
+    w = wl.PREFILL_WORKLOADS[args.prefill]()
+    flops = wl.causal_flops(w)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        st = PrefillOracleSample(w)
+        for _ in range(args.warmup):
+            st.step()
+        tf, tt = 0, 0.0
+        for _ in range(args.steps):
+            f_, t_ = st.step()
+            tf += f_
+            tt += t_
+        val = tf / tt / 1e12
+        line = {"impl": "reference", "metric": PREFILL_METRIC, "value": val, "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * flops / (val * 1e12), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(w),
+                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": st.threads, "kind": "oracle",
+                                 "sample": f"each step: the last {st.rows} queries of one sequence (rotating) "
+                                           f"against its whole context; ms_per_step scaled to the batch"},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    import torch.distributed as dist
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from paged_kv_decode_14_gb300 import _native as nat
+    from paged_kv_decode_14_gb300.runner import DeviceWorkload
+    nat.lib()
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    kvb = w.unique_kv_bytes()
+    n_copies = min(16, max(2, -(-3 * l2 // max(1, kvb))))
+    dws = []
+    for _ in range(n_copies):
+        d = DeviceWorkload(w, device=dev)
+        d.prefill()
+        dws.append(d)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        queue_ahead(torch)
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        barrier()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    def run_step(i):
+        d = dws[i % n_copies]
+        d.append_step()
+        d.attend_prefill()
+
+    def run_attn(i):
+        dws[i % n_copies].attend_prefill()
+
+    for i in range(max(args.warmup, 1)):
+        run_step(i)
+    barrier()
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.__enter__()
+        t_end = time.perf_counter() + args.soak_seconds
+        while time.perf_counter() < t_end:
+            for i in range(8):
+                run_step(i)
+            torch.cuda.synchronize(dev)
+    barrier()
+    step_us = timed(run_step, args.steps)
+    if clocks:
+        clocks.__exit__()
+    tot_ms = max_over_ranks(step_us * args.steps / 1e3, world, dev)
+    value = world * flops * args.steps / (tot_ms / 1e3) / 1e12
+    attn_us = timed(run_attn, args.steps)
+
+    pins = [d.pinned_io() for d in dws]
+    host_out = torch.empty(dws[0].out.shape, dtype=dws[0].out.dtype).pin_memory()
+
+    def e2e_step(i):
+        d = dws[i % n_copies]
+        d.io.copy_(pins[i % n_copies], non_blocking=True)
+        d.append_step()
+        d.attend_prefill()
+        host_out.copy_(d.out, non_blocking=True)
+
+    for i in range(max(args.warmup, 1)):
+        e2e_step(i)
+    barrier()
+    e2e_us = timed(e2e_step, args.steps)
+    e2e_tot = max_over_ranks(e2e_us * args.steps / 1e3, world, dev)
+    peak, kind = tensor_peak()
+    achieved = flops / (attn_us * 1e-6) / 1e12
+    line = {"metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 q.k, fp16 p.v", "data": "synthetic",
+            "config": {**workload_config(w),
+                       "l2": f"inputs rotated over {n_copies} copies ({n_copies * kvb / 1e6:.0f} MB of KV); "
+                             f"within a launch every query block of a sequence re-reads its K/V from L2",
+                       "launch": "eager, through the binding",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "flops_per_step": flops, "attention_us": attn_us, "append_us": step_us - attn_us,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_kind": f"{kind} (cuBLAS bf16 GEMM burst; fp16 runs at the same rate)",
+                         "kernel": "paged chunked prefill (tcgen05, two 128-row tiles per CTA)",
+                         "algorithmic_flops_per_launch": flops, "avg_launch_us": attn_us,
+                         "timing": "back-to-back launches over rotating copies, one event interval, host ahead"},
+            "e2e": {"value": world * flops * args.steps / (e2e_tot / 1e3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(dws[0].io.numel()),
+                    "d2h_bytes_per_step": int(dws[0].out.numel() * dws[0].out.element_size()),
+                    "ms_per_step": e2e_tot / args.steps},
+            "gpu_launches": 2 * args.steps}
+    if clocks:
+        line["clocks"] = clocks.summary()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        st = PrefillOracleSample(w)
+        tf, tt, n = 0, 0.0, 0
+        while tt < args.cpu_seconds:
+            f_, t_ = st.step()
+            tf += f_
+            tt += t_
+            n += 1
+        line["cpu_baseline"] = {"value": tf / tt / 1e12, "unit": "TFLOP/s", "cores": st.threads, "kind": "oracle",
+                                "sample": f"{n} oracle steps in {tt:.1f} s, each the last {st.rows} queries of "
+                                          f"one sequence (rotating) against its whole context"}
+    errs = [e for d in dws for e in d.errors()]
+    if any(errs):
+        line["device_errors"] = errs
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
 
 
 def run_reference(args):
@@ -504,6 +708,8 @@ def workload_config(w) -> dict:
 
 def main():
     args = parse()
+    if args.prefill:
+        return run_prefill(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

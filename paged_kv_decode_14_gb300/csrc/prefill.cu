@@ -300,10 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
             acc = f2pack(__float_as_uint(a0 * alpha), __float_as_uint(a1 * alpha));
             m += inc;
         };
-        // P of 32 keys no mask touches, two keys per packed fp32 operation; unless FORCE, nothing is
-        // stored (false) when some P would reach 2^kBig (or is NaN).  Adds the chunk's P to acc and
-        // the largest fp16 P bit pattern (P >= 0: integer order is value order) to pmaxw.
-        auto emit_fast = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, uint32_t& pmaxw, bool force) -> bool {
+        // P of 32 keys, two keys per packed fp32 operation (MASK: keys past this row's limit weigh
+        // 0); unless FORCE, nothing is stored (false) when some P would reach 2^kBig (or is NaN).
+        // Adds the chunk's P to acc and the largest fp16 P bit pattern (P >= 0: integer order is
+        // value order) to pmaxw.
+        auto emit_fast = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, uint32_t& pmaxw, bool force,
+                             bool mask) -> bool {
             const uint64_t sc2 = f2pack(__float_as_uint(sc), __float_as_uint(sc));
             const uint64_t nm2 = f2pack(__float_as_uint(-m), __float_as_uint(-m));
             uint64_t ca = 0;                               // (+0, +0)
@@ -312,7 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
             for (int k = 0; k < 32; k += 2) {
                 float x0, x1;
                 f2unpack(f2fma(f2pack(rr[k], rr[k + 1]), sc2, nm2), x0, x1);
-                const float p0 = exp2_fast(x0), p1 = exp2_fast(x1);
+                float p0 = exp2_fast(x0), p1 = exp2_fast(x1);
+                if (mask) {
+                    p0 = c + k <= rem_c ? p0 : 0.f;
+                    p1 = c + k + 1 <= rem_c ? p1 : 0.f;
+                }
                 ca = f2add(ca, f2pack(__float_as_uint(p0), __float_as_uint(p1)));
                 const __half2 h = __floats2half2_rn(p0, p1);
                 w[k >> 1] = *reinterpret_cast<const uint32_t*>(&h);
@@ -324,21 +330,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
             tmem_st16u(scol + (c >> 1), w);
             return true;
         };
-        auto chunk = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, uint32_t& pmaxw) {
-            if (emit_fast(rr, c, acc, pmaxw, false)) return;
+        auto chunk = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, uint32_t& pmaxw, bool mask) {
+            if (emit_fast(rr, c, acc, pmaxw, false, mask)) return;
             // (rare) a logit more than 2^kBig above the reference: raise it first
             float c0 = -INFINITY, c1 = -INFINITY;
 #pragma unroll
             for (int x = 0; x < 32; x += 2) {
-                c0 = fmaxf(c0, __uint_as_float(rr[x]));
-                c1 = fmaxf(c1, __uint_as_float(rr[x + 1]));
+                c0 = fmaxf(c0, !mask || c + x <= rem_c ? __uint_as_float(rr[x]) : -INFINITY);
+                c1 = fmaxf(c1, !mask || c + x + 1 <= rem_c ? __uint_as_float(rr[x + 1]) : -INFINITY);
             }
             raise_ref(fmaxf(c0, c1) * sc, c, acc);
-            emit_fast(rr, c, acc, pmaxw, true);             // (P <= 1 now, but for NaN logits)
+            emit_fast(rr, c, acc, pmaxw, true, mask);       // (P <= 1 now, but for NaN logits)
         };
-        // one pass over a tile no mask touches, loads of the next 32 columns in flight while the
-        // previous 32 are turned into P; returns the tile's sum of P, and in pmaxw its largest P
-        auto fast_pass = [&](uint32_t& pmaxw) -> float {
+        // one pass over a tile once the row's reference is known, loads of the next 32 columns in
+        // flight while the previous 32 are turned into P; returns the tile's sum of P, and in
+        // pmaxw its largest P
+        auto fast_pass = [&](uint32_t& pmaxw, bool mask) -> float {
             uint64_t acc = 0;
             pmaxw = 0;
             uint32_t ra[32], rb[32];
@@ -347,10 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
 #pragma unroll 1
             for (int c = 0; c < kKeys; c += 64) {
                 tmem_ld32_async(scol + c + 32, rb);
-                chunk(ra, c, acc, pmaxw);
+                chunk(ra, c, acc, pmaxw, mask);
                 tmem_wait_ld_into(rb);
                 if (c + 64 < kKeys) tmem_ld32_async(scol + c + 64, ra);
-                chunk(rb, c + 32, acc, pmaxw);
+                chunk(rb, c + 32, acc, pmaxw, mask);
                 if (c + 64 < kKeys) tmem_wait_ld_into(ra);
             }
             float a0, a1;
@@ -411,15 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                 if (up) m = pend;
             }
             pend = -INFINITY;
-            if (__all_sync(0xffffffffu, rem_c >= kKeys - 1 && m > -INFINITY) && sc > 0.f) {
-                // off the causal diagonal, reference known: one pass.  A largest P of 2^e or more
-                // (e >= kSlack) moves the reference up by e + 1 octaves at the next tile.
+            if (__all_sync(0xffffffffu, m > -INFINITY) && sc > 0.f) {
+                // reference known: one pass (masked on the causal diagonal).  A largest P of 2^e or
+                // more (e >= kSlack) moves the reference up by e + 1 octaves at the next tile.
                 uint32_t pw;
-                l += fast_pass(pw);
+                l += __all_sync(0xffffffffu, rem_c >= kKeys - 1) ? fast_pass(pw, false) : fast_pass(pw, true);
                 const uint32_t pm = max(pw & 0xffffu, pw >> 16);
                 if (pm >= 0x5c00u && pm < 0x7c00u) pend = m + (float)((int)(pm >> 10) - 15 + 1);
             } else {
-                // two passes (first tile, causal diagonal, rows past the window): the tile's
+                // two passes (a warp's first tile with keys, rows past the window): the tile's
                 // maximum over the visible keys first, then P
                 float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll 1

@@ -341,6 +341,36 @@ def long_prefix_reuse(prefix_tokens: int = 8192, seed: int = 7, conversations: i
 
 
 # The five named workloads, by number.
+def prefill_b4_q2048_d128(seed: int = 8) -> Workload:
+    """Four whole prompts of 2048 tokens processed at once (causal prefill):
+    32 query / 8 KV heads, head_dim 128, bf16 K/V ~ N(0, 1), pages from a
+    shuffled pool."""
+    return make_workload("prefill_b4_q2048_d128", context_lens=[2048] * 4, q_lens=[2048] * 4,
+                         num_q_heads=32, num_kv_heads=8, head_dim=128, seed=seed)
+
+
+def chunked_prefill_b8_q512_d128(seed: int = 9) -> Workload:
+    """Chunked prefill: eight sequences each appending a 512-token chunk after
+    3584 resident tokens (context 4096); 32/8 heads, head_dim 128."""
+    return make_workload("chunked_prefill_b8_q512_d128", context_lens=[4096] * 8, q_lens=[512] * 8,
+                         num_q_heads=32, num_kv_heads=8, head_dim=128, seed=seed)
+
+
+PREFILL_WORKLOADS = {
+    "prefill_b4_q2048_d128": prefill_b4_q2048_d128,
+    "chunked_prefill_b8_q512_d128": chunked_prefill_b8_q512_d128,
+}
+
+
+def causal_flops(w: Workload) -> int:
+    """Multiply-add FLOPs of the attention's two products (q.k and p.v) over
+    the keys each query sees: 4 * D * Hq per (query, visible key)."""
+    L = w.context_lens.astype(np.int64)
+    Q = w.q_lens.astype(np.int64)
+    keys = Q * (L - Q) + Q * (Q + 1) // 2
+    return int(4 * w.head_dim * w.num_q_heads * keys.sum())
+
+
 WORKLOADS = {
     1: tiny_decode,
     2: decode_b32_d128,
