@@ -16,7 +16,7 @@ cudaError_t launch_copy_blocks(const pkv_cache& c, const int32_t* pairs, int n, 
                                cudaStream_t st, int num_sms);
 cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_bytes, int ncta, cudaStream_t st);
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st);
-cudaError_t launch_prefill(const AttnParams& p, int head_dim, cudaStream_t st);
+cudaError_t launch_prefill(const AttnParams& p, int head_dim, int num_sms, cudaStream_t st);
 int simt_rows_pad(int rows);
 int tc_heads_per_segment(int num_kv_heads, int rows);
 
@@ -316,7 +316,9 @@ PKV_API pkv_status pkv_paged_prefill(const pkv_cache* cache, const void* q, int3
     p.cache_kv_heads = cache->num_kv_heads;
     p.num_seqs_total = num_seqs;
     fill_debug(p);
-    return launch_prefill(p, cache->head_dim, (cudaStream_t)stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const int sms = num_sms_current();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    return launch_prefill(p, cache->head_dim, sms, (cudaStream_t)stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 PKV_API void pkv_debug_set_wait_limit(uint64_t limit_ns, const int32_t* hold_flag) {

@@ -33,6 +33,8 @@
 // only after PV_i(t) has read it, and when S_i(t + 1) signals, PV_i(t) has
 // completed, so the softmax may rescale O_i without another wait.  Every
 // mbarrier wait is bounded (the launch's wait limit).
+#include <algorithm>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -61,11 +63,12 @@ struct Cfg {
     static constexpr int OFF_K = OFF_Q + 2 * QBYTES;      // K ring
     static constexpr int OFF_V = OFF_K + NSK * TILE;      // V ring
     static constexpr int OFF_BAR = OFF_V + NSV * TILE;
-    // barriers: KFULL[NSK] KEMPTY[NSK] VFULL[NSV] VEMPTY[NSV] VREADY[NSV] SFULL[2] PFULL[2] QFULL ODONE[2] DRAIN
+    // barriers: KFULL[NSK] KEMPTY[NSK] VFULL[NSV] VEMPTY[NSV] VREADY[NSV] SFULL[2] PFULL[2] QFULL ODONE[2]
+    // OFREE[2] DRAIN
     static constexpr int KFULL = 0, KEMPTY = NSK, VFULL = 2 * NSK, VEMPTY = 2 * NSK + NSV,
                          VREADY = 2 * NSK + 2 * NSV, SFULL = 2 * NSK + 3 * NSV, PFULL = SFULL + 2,
-                         QFULL = SFULL + 4, ODONE = SFULL + 5, DRAIN = SFULL + 7;
-    static constexpr int NBAR = SFULL + 8;
+                         QFULL = SFULL + 4, ODONE = SFULL + 5, OFREE = SFULL + 7, DRAIN = SFULL + 9;
+    static constexpr int NBAR = SFULL + 10;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem address, abort flags, qoff
     static constexpr int SMEM = OFF_MISC + 16 + 128;      // (+ alignment slack)
     // TMEM columns: S/P_0, S/P_1 (128 each), O_0, O_1 (D each)
@@ -126,6 +129,43 @@ __device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
     return d;
 }
 
+// One work item: 256 / G query positions (query block qb) of sequence b and kv-head g.  Items are
+// numbered heavy first -- the last query blocks, which see the most keys, of every (sequence,
+// kv-head), then the ones before -- and the persistent CTAs deal them out in serpentine rounds
+// (round k gives item k * grid + c to CTA c on even rounds, k * grid + grid - 1 - c on odd ones),
+// which keeps the CTAs' loads close when the items' costs fall off.
+struct Item {
+    int b, g, q0, nq, L, Q, T, nb;
+    bool two;           // row tile 1 holds rows of the window
+};
+__device__ __forceinline__ bool item_at(const AttnParams& p, int j, int qblocks, Item& it) {
+    const int bg = p.num_seqs * p.num_kv_heads;
+    const int qb = qblocks - 1 - j / bg;
+    it.b = (j % bg) / p.num_kv_heads;
+    it.g = (j % bg) % p.num_kv_heads;
+    it.L = p.context_lens[it.b];
+    it.Q = p.q_lens[it.b];
+    it.q0 = qb * (kCtaRows / p.group);
+    const bool bad = it.Q > it.L || it.Q < 0 || it.Q > p.max_q_len ||
+                     (it.L + kBlock - 1) / kBlock > p.max_blocks_per_seq;
+    if (bad || it.q0 >= it.Q) return false;
+    it.nq = min(kCtaRows / p.group, it.Q - it.q0);
+    it.two = it.nq * p.group > kRows;
+    it.T = (it.L - it.Q + it.q0 + it.nq - 1) / kKeys + 1;
+    it.nb = (it.L + kBlock - 1) / kBlock;
+    return true;
+}
+// This CTA's next item after its round k (k = -1: the first); k advances to the item's round.
+// Returns the item's number, or `total` when none is left.
+__device__ __forceinline__ int next_item(const AttnParams& p, int& k, int total, int qblocks, Item& it) {
+    const int grid = gridDim.x, c = blockIdx.x;
+    for (++k; (int64_t)k * grid < total; ++k) {
+        const int j = k * grid + ((k & 1) ? grid - 1 - c : c);
+        if (j < total && item_at(p, j, qblocks, it)) return j;
+    }
+    return total;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p, int qblocks) {
     using K = Cfg<D>;
@@ -137,52 +177,51 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
     constexpr int NSK = K::NSK, NSV = K::NSV, KFULL = K::KFULL, VFULL = K::VFULL, KEMPTY = K::KEMPTY,
                   VEMPTY = K::VEMPTY, VREADY = K::VREADY,
                   SFULL = K::SFULL, PFULL = K::PFULL, QFULL = K::QFULL, ODONE = K::ODONE,
-                  DRAIN = K::DRAIN;
+                  OFREE = K::OFREE, DRAIN = K::DRAIN;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 4);
-    int* s_qoff = reinterpret_cast<int*>(smem + K::OFF_MISC + 8);
     // abort flag of the drain waits at the end (set only when one of them runs out)
     volatile int* drain_flag = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 12);
     const Ctl ctl{abort_flag, p.err, p.wait_limit_ns};
 
     griddep_launch();
     griddep_wait();
-    // this CTA: sequence b, kv-head g, query block qb of 256 / G positions (the
-    // last blocks, which see the most keys, first)
-    const int G = p.group, QP = kCtaRows / G;
-    const int qb = qblocks - 1 - (int)(blockIdx.x % qblocks), g = (blockIdx.x / qblocks) % p.num_kv_heads,
-              b = blockIdx.x / (qblocks * p.num_kv_heads);
-    const int L = p.context_lens[b], Q = p.q_lens[b];
-    const int q0 = qb * QP;
-    // uniform over the CTA: nothing to do (past the window, or invalid lengths: the first CTA reports those)
-    const bool bad = Q > L || Q < 0 || Q > p.max_q_len || (L + kBlock - 1) / kBlock > p.max_blocks_per_seq;
-    if (bad && q0 == 0 && g == 0 && tid == 0 && Q != 0) raise_error(p.err, PKV_DEVERR_LENGTH);
-    if (bad || q0 >= Q) return;
-    const int nq = min(QP, Q - q0);                       // query positions of this CTA
-    const bool two = nq * G > kRows;                      // row tile 1 holds rows of the window
-    const int lim_max = L - Q + q0 + nq - 1;              // last key any of its rows sees
-    const int T = lim_max / kKeys + 1;                    // key tiles
-    const int nb = (L + kBlock - 1) / kBlock;             // pages of the sequence
+    const int G = p.group;
+    const int total = p.num_seqs * p.num_kv_heads * qblocks;
+    // invalid lengths are reported once, by the CTA that owns the sequence's first item of kv-head 0
+    if (tid == 0)
+        for (int k = 0; (int64_t)k * gridDim.x < total; ++k) {
+            const int j = k * gridDim.x + ((k & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+            const int bg = p.num_seqs * p.num_kv_heads, b = (j % bg) / p.num_kv_heads;
+            if (j < total && j / bg == qblocks - 1 && (j % bg) % p.num_kv_heads == 0) {
+                const int L = p.context_lens[b], Q = p.q_lens[b];
+                if (Q != 0 && (Q > L || Q < 0 || Q > p.max_q_len || (L + kBlock - 1) / kBlock > p.max_blocks_per_seq))
+                    raise_error(p.err, PKV_DEVERR_LENGTH);
+            }
+        }
+    Item first;
+    int k0 = -1;
+    const int j0 = next_item(p, k0, total, qblocks, first);
+    if (j0 >= total) return;                              // (uniform over the CTA)
 
     if (tid == 0) {
-        const int nt = two ? 2 : 1;                       // MMA issuers that release K and V slots
         for (int i = 0; i < NSK; ++i) {
             mbar_init(bar(KFULL + i), 1);
-            mbar_init(bar(KEMPTY + i), nt);
+            mbar_init(bar(KEMPTY + i), 2);                // both MMA issuers release every K tile
         }
         for (int i = 0; i < NSV; ++i) {
             mbar_init(bar(VFULL + i), 1);
-            mbar_init(bar(VEMPTY + i), nt);
+            mbar_init(bar(VEMPTY + i), 2);
             mbar_init(bar(VREADY + i), kRows);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(SFULL + i), 1);
             mbar_init(bar(PFULL + i), kRows);
+            mbar_init(bar(ODONE + i), 1);
+            mbar_init(bar(OFREE + i), kRows);
         }
         mbar_init(bar(QFULL), kCtaRows);
-        mbar_init(bar(ODONE), 1);
-        mbar_init(bar(ODONE + 1), 1);
-        mbar_init(bar(DRAIN), nt);
+        mbar_init(bar(DRAIN), 2);
         *abort_flag = 0;
         *drain_flag = 0;
         mbar_fence_init();
@@ -190,45 +229,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), K::TMEM_COLS);
         tmem_relinquish();
-        // first q row of sequence b
-        int s = 0;
-        for (int i = lane; i < b; i += 32) s += max(p.q_lens[i], 0);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) *s_qoff = s;
     }
     tc_fence_before();
     cta_bar_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int qoff = *s_qoff;
 
     if (warp < 8) {
         // ------------------------------------------------ softmax / epilogue: row tile i, thread r = row r
         const int i = warp >> 2, r = tid & (kRows - 1);
-        const int R = i * kRows + r, qi = R / G, hl = R - qi * G;
-        const bool row_ok = qi < nq;
-        const int qpos = L - Q + q0 + qi;                 // this row's query position (last key it sees)
+        const int R = i * kRows + r, qi = R / G, hl = R - qi * G;   // row R: query position qi of the item, head hl
         const uint32_t lbase = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t scol = tmem + lbase + i * kKeys;   // S_i / P_i
         const uint32_t ocol = tmem + lbase + K::COL_O + i * D;
-        // q row -> Q tile i (K-major core matrices), zeros for rows past the window
-        {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                p.q + ((size_t)(qoff + q0 + qi) * p.num_q_heads + g * G + hl) * D);
-            uint8_t* dst = smem + K::OFF_Q + i * K::QBYTES + (r >> 3) * (K::NCH * 128) + (r & 7) * 16;
-            uint4 qv[K::NCH];                              // all loads in flight at once
-#pragma unroll
-            for (int c = 0; c < K::NCH; ++c) qv[c] = row_ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int c = 0; c < K::NCH; ++c) *reinterpret_cast<uint4*>(dst + c * 128) = qv[c];
-            fence_proxy_async_smem();
-            mbar_arrive(bar(QFULL));
-        }
-        // keys 0 .. lim are visible to this row (lim <= L - 1; -1: a row past the window)
-        const int lim = row_ok ? qpos : -1;
         // every wait and every TMEM access of the loop is warp-uniform (tcgen05.ld/st are .aligned)
         auto wait_all = [&](uint32_t bb, uint32_t parity) { return __all_sync(0xffffffffu, wait(bb, parity, ctl)); };
+        int nb = 0, valid_last = kBlock;                   // the current item's pages, its last page's tokens
         const float sc = p.scale_log2;
         int rem_c = 0;                                     // this tile: column c is visible iff c <= rem_c
         // P of 32 keys (S values rr, columns c .. c + 31) -> 16 columns of fp16 pairs (the even key
@@ -372,11 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
         // less than 2^-25); a finite |v| >= 65536 sets PKV_DEVERR_RANGE.  The last page's
         // unwritten slots become 0 (they may hold NaN).
         constexpr int CPP = K::PAGE / 16;                  // 16-byte chunks per page
-        const int valid_last = L - (nb - 1) * kBlock;      // tokens of the sequence's last page
         uint32_t vmaxbits = 0;                             // largest |bf16| bit patterns seen (two halves)
-        auto convert_v = [&](int t) -> bool {
-            const int s = t % NSV, np = min(kTP, nb - t * kTP), lastpg = nb - 1 - t * kTP;
-            if (!wait_all(bar(VFULL + s), (t / NSV) & 1)) return false;
+        // tile t of the current item, the CTA's V tile number gt (ring slot and phase)
+        auto convert_v = [&](int gt, int t) -> bool {
+            const int s = gt % NSV, np = min(kTP, nb - t * kTP), lastpg = nb - 1 - t * kTP;
+            if (!wait_all(bar(VFULL + s), (gt / NSV) & 1)) return false;
             uint4* base = reinterpret_cast<uint4*>(smem + K::OFF_V + s * K::TILE);
             for (int pg = 0; pg < np; ++pg) {
                 uint4* pgp = base + pg * CPP;
@@ -404,103 +420,167 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
             mbar_arrive(bar(VREADY + s));
             return true;
         };
-        bool ok = i == 0 || two;
-        if (ok && i == 0) ok = convert_v(0);
-        for (int t = 0; t < T && ok; ++t) {
-            if (!(ok = wait_all(bar(SFULL + i), t & 1))) break;
-            tc_fence_after();
-            rem_c = lim - t * kKeys;
-            if (__any_sync(0xffffffffu, pend > m + kSlack)) {
-                const bool up = pend > m + kSlack;
-                const float alpha = up ? exp2_fast(m - pend) : 1.f;
-                rescale_o(alpha);
-                l *= alpha;
-                if (up) m = pend;
-            }
-            pend = -INFINITY;
-            if (__all_sync(0xffffffffu, m > -INFINITY) && sc > 0.f) {
-                // reference known: one pass (masked on the causal diagonal).  A largest P of 2^e or
-                // more (e >= kSlack) moves the reference up by e + 1 octaves at the next tile.
-                uint32_t pw;
-                l += __all_sync(0xffffffffu, rem_c >= kKeys - 1) ? fast_pass(pw, false) : fast_pass(pw, true);
-                const uint32_t pm = max(pw & 0xffffu, pw >> 16);
-                if (pm >= 0x5c00u && pm < 0x7c00u) pend = m + (float)((int)(pm >> 10) - 15 + 1);
-            } else {
-                // two passes (a warp's first tile with keys, rows past the window): the tile's
-                // maximum over the visible keys first, then P
-                float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll 1
-                for (int c = 0; c < kKeys; c += 32) {
-                    float v[32];
-                    tmem_ld32(scol + c, v);
+        // The CTA's items in order.  Per item: its q rows -> Q_i, (row tile 0) V of its first tile
+        // converted, the softmax of each key tile (row tile 0 converting the next tile's V after
+        // signalling P), and the epilogue, during which the next item's q rows are already loaded.
+        int scnt = 0, ocnt = 0, gv = 0;                    // this row tile's S tiles and items; V tiles
+        bool ok = true;
+        Item it = first;
+        int j = j0, kr = k0;
+        auto qsum = [&](int b) {                           // first q row of sequence b
+            int sum = 0;
+            for (int x = lane; x < b; x += 32) sum += max(p.q_lens[x], 0);
 #pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        mx[x & 1] = fmaxf(mx[x & 1], c + x <= rem_c ? v[x] * sc : -INFINITY);
-                }
-                const float tmax = fmaxf(mx[0], mx[1]);
-                const bool grow = tmax > m + kSlack || (m == -INFINITY && tmax > -INFINITY);
-                const float alpha = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2_fast(m - tmax));
-                if (t > 0 && __any_sync(0xffffffffu, grow && m != -INFINITY)) rescale_o(alpha);
-                l *= alpha;
-                if (grow) m = tmax;
-                // rows with nothing visible yet keep m = -inf: every P of theirs is masked to 0
-                const float mref = m == -INFINITY ? 0.f : m;
-                float ls[2] = {0.f, 0.f};
-#pragma unroll 1
-                for (int c = 0; c < kKeys; c += 32) {
-                    uint32_t rr[32];
-                    tmem_ld32_async(scol + c, rr);
-                    tmem_wait_ld_into(rr);
-                    emit(rr, c, mref, true, ls);
-                }
-                l += ls[0] + ls[1];
+            for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            return sum;
+        };
+        int qoff = qsum(it.b);
+        auto q_row = [&](const Item& x, int xoff) {       // this row's q in the item (row 0 past the window)
+            return reinterpret_cast<const uint4*>(
+                p.q + ((size_t)(xoff + x.q0 + (qi < x.nq ? qi : 0)) * p.num_q_heads + x.g * G + hl) * D);
+        };
+        while (ok && j < total) {
+            // q rows -> Q tile i (K-major core matrices), zeros for rows past the window.  This warp's
+            // rows of the Q_i area held its staged output of the last item: the bulk copies have read it.
+            {
+                const bool rok = qi < it.nq;
+                const uint4* src = q_row(it, qoff);
+                uint8_t* dst = smem + K::OFF_Q + i * K::QBYTES + (r >> 3) * (K::NCH * 128) + (r & 7) * 16;
+                uint4 qv[K::NCH];                          // all loads in flight at once
+#pragma unroll
+                for (int c = 0; c < K::NCH; ++c) qv[c] = rok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int c = 0; c < K::NCH; ++c) *reinterpret_cast<uint4*>(dst + c * 128) = qv[c];
+                fence_proxy_async_smem();
+                mbar_arrive(bar(QFULL));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(PFULL + i));
-            if (i == 0 && t + 1 < T && !(ok = convert_v(t + 1))) break;
+            const bool act = i == 0 || it.two;
+            const int T = it.T;
+            nb = it.nb;
+            valid_last = it.L - (it.nb - 1) * kBlock;
+            const bool row_ok = qi < it.nq;
+            // keys 0 .. lim are visible to this row (lim <= L - 1; -1: a row past the window)
+            const int lim = row_ok ? it.L - it.Q + it.q0 + qi : -1;
+            if (i == 0) ok = convert_v(gv, 0);
+            m = -INFINITY;
+            l = 0.f;
+            pend = -INFINITY;
+            for (int t = 0; act && t < T && ok; ++t) {
+                if (!(ok = wait_all(bar(SFULL + i), scnt & 1))) break;
+                tc_fence_after();
+                rem_c = lim - t * kKeys;
+                if (__any_sync(0xffffffffu, pend > m + kSlack)) {
+                    const bool up = pend > m + kSlack;
+                    const float alpha = up ? exp2_fast(m - pend) : 1.f;
+                    rescale_o(alpha);
+                    l *= alpha;
+                    if (up) m = pend;
+                }
+                pend = -INFINITY;
+                if (__all_sync(0xffffffffu, m > -INFINITY) && sc > 0.f) {
+                    // reference known: one pass (masked on the causal diagonal).  A largest P of 2^e
+                    // or more (e >= kSlack) moves the reference up by e + 1 octaves at the next tile.
+                    uint32_t pw;
+                    l += __all_sync(0xffffffffu, rem_c >= kKeys - 1) ? fast_pass(pw, false) : fast_pass(pw, true);
+                    const uint32_t pm = max(pw & 0xffffu, pw >> 16);
+                    if (pm >= 0x5c00u && pm < 0x7c00u) pend = m + (float)((int)(pm >> 10) - 15 + 1);
+                } else {
+                    // two passes (a warp's first tile with keys, rows past the window): the tile's
+                    // maximum over the visible keys first, then P
+                    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll 1
+                    for (int c = 0; c < kKeys; c += 32) {
+                        float v[32];
+                        tmem_ld32(scol + c, v);
+#pragma unroll
+                        for (int x = 0; x < 32; ++x)
+                            mx[x & 1] = fmaxf(mx[x & 1], c + x <= rem_c ? v[x] * sc : -INFINITY);
+                    }
+                    const float tmax = fmaxf(mx[0], mx[1]);
+                    const bool grow = tmax > m + kSlack || (m == -INFINITY && tmax > -INFINITY);
+                    const float alpha = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2_fast(m - tmax));
+                    if (t > 0 && __any_sync(0xffffffffu, grow && m != -INFINITY)) rescale_o(alpha);
+                    l *= alpha;
+                    if (grow) m = tmax;
+                    // rows with nothing visible yet keep m = -inf: every P of theirs is masked to 0
+                    const float mref = m == -INFINITY ? 0.f : m;
+                    float ls[2] = {0.f, 0.f};
+#pragma unroll 1
+                    for (int c = 0; c < kKeys; c += 32) {
+                        uint32_t rr[32];
+                        tmem_ld32_async(scol + c, rr);
+                        tmem_wait_ld_into(rr);
+                        emit(rr, c, mref, true, ls);
+                    }
+                    l += ls[0] + ls[1];
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(PFULL + i));
+                ++scnt;
+                if (i == 0 && t + 1 < T && !(ok = convert_v(gv + t + 1, t + 1))) break;
+            }
+            if (!ok) break;
+            gv += T;
+            // the next item: its q rows are brought to L2 while this item's epilogue runs
+            const Item cur = it;
+            const int cur_off = qoff;
+            j = next_item(p, kr, total, qblocks, it);
+            if (j < total) {
+                qoff = qsum(it.b);
+                if (qi < it.nq) {
+                    const char* a = reinterpret_cast<const char*>(q_row(it, qoff));
+#pragma unroll
+                    for (int c = 0; c < D * 2; c += 128) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a + c));
+                }
+            }
+            // epilogue: O_i / l -> bf16 rows [row][D] in the Q_i area (free: every S of the item has
+            // completed when ODONE_i signals), then one bulk copy per run of a warp's rows that share
+            // a query position (its consecutive heads, contiguous in out)
+            if (act) {
+                if (!(ok = wait_all(bar(ODONE + i), ocnt & 1))) break;
+                tc_fence_after();
+                uint8_t* stg = smem + K::OFF_Q + R * (D * 2);
+                const float inv = 1.f / l;
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    float o[32];
+                    tmem_ld32(ocol + c, o);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            __nv_bfloat162 pr = __floats2bfloat162_rn(o[h * 8 + 2 * x] * inv, o[h * 8 + 2 * x + 1] * inv);
+                            w[x] = *reinterpret_cast<uint32_t*>(&pr);
+                        }
+                        *reinterpret_cast<uint4*>(stg + (c + h * 8) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(OFREE + i));               // O_i read: the next item's PV may overwrite it
+                ++ocnt;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int R0 = R;                      // (lane 0: the warp's first row)
+                    for (int Rr = R0; Rr < R0 + 32;) {
+                        const int qq = Rr / G, hh = Rr - qq * G, n = min(G - hh, R0 + 32 - Rr);
+                        if (qq < cur.nq)
+                            bulk_s2g(p.out + ((size_t)(cur_off + cur.q0 + qq) * p.num_q_heads + cur.g * G + hh) * D,
+                                     sb + K::OFF_Q + Rr * (D * 2), (uint32_t)(n * D * 2));
+                        Rr += n;
+                    }
+                    bulk_commit_group();
+                    bulk_wait_read();                      // the staging rows are free again
+                }
+                __syncwarp();
+            }
         }
+        if (lane == 0) bulk_wait_all();                    // every output row written
         {
             const uint32_t lo = vmaxbits & 0xffffu, hi = vmaxbits >> 16;
             if ((lo >= 0x4780u && lo < 0x7f80u) || (hi >= 0x4780u && hi < 0x7f80u)) raise_error(p.err, PKV_DEVERR_RANGE);
-        }
-        // epilogue: O_i / l -> bf16 rows [row][D] in the Q_i area (free: every S has completed when
-        // ODONE_i signals), then one bulk copy per run of a warp's rows that share a query position
-        // (its consecutive heads, contiguous in out)
-        if (ok && wait_all(bar(ODONE + i), 0)) {
-            tc_fence_after();
-            uint8_t* stg = smem + K::OFF_Q + R * (D * 2);
-            const float inv = 1.f / l;
-#pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                float o[32];
-                tmem_ld32(ocol + c, o);
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(o[h * 8 + 2 * x] * inv, o[h * 8 + 2 * x + 1] * inv);
-                        w[x] = *reinterpret_cast<uint32_t*>(&pr);
-                    }
-                    *reinterpret_cast<uint4*>(stg + (c + h * 8) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                const int R0 = R;                          // (lane 0: the warp's first row)
-                for (int Rr = R0; Rr < R0 + 32;) {
-                    const int qq = Rr / G, hh = Rr - qq * G, n = min(G - hh, R0 + 32 - Rr);
-                    if (qq < nq)
-                        bulk_s2g(p.out + ((size_t)(qoff + q0 + qq) * p.num_q_heads + g * G + hh) * D,
-                                 sb + K::OFF_Q + Rr * (D * 2), (uint32_t)(n * D * 2));
-                    Rr += n;
-                }
-                bulk_commit_group();
-                bulk_wait_all();
-            }
-            __syncwarp();
         }
     } else if (warp == kProdK || warp == kProdV) {
         // ------------------------------------------------ producers: K pages (warp 8) and V pages (warp 9)
@@ -509,8 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
         const int NSR = isv ? NSV : NSK, FULL = isv ? VFULL : KFULL, EMPTY = isv ? VEMPTY : KEMPTY;
         const uint32_t ring = sb + (isv ? K::OFF_V : K::OFF_K);
         const uint8_t* src = isv ? p.v_cache : p.k_cache;
-        const int32_t* table = p.block_tables + (size_t)b * p.max_blocks_per_seq;
-        int kc = 0;
+        int kc = 0;                                       // tiles issued (over the CTA's items)
         bool ok = true;
         if (p.hold != nullptr) {
             // (tests of the timeout path only) wait, bounded, for a flag that nothing sets
@@ -529,23 +608,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
             }
             ok = __shfl_sync(0xffffffffu, w, 0);
         }
-        for (int t = 0; t < T && ok; ++t) {
-            const int s = t % NSR, p0 = t * kTP, np = min(kTP, nb - p0);
-            int blk = lane < np ? __ldg(table + p0 + lane) : 0;
-            if (lane < np && (blk < 0 || blk >= p.num_blocks)) {
-                if (!isv) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
-                blk = 0;
+        Item it = first;
+        int kr = k0;
+        for (int j = j0; j < total && ok; j = next_item(p, kr, total, qblocks, it)) {
+            const int32_t* table = p.block_tables + (size_t)it.b * p.max_blocks_per_seq;
+            for (int t = 0; t < it.T && ok; ++t) {
+                const int s = kc % NSR, p0 = t * kTP, np = min(kTP, it.nb - p0);
+                int blk = lane < np ? __ldg(table + p0 + lane) : 0;
+                if (lane < np && (blk < 0 || blk >= p.num_blocks)) {
+                    if (!isv) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+                    blk = 0;
+                }
+                bool w = true;
+                if (kc >= NSR && lane == 0) w = wait(bar(EMPTY + s), ((kc - NSR) / NSR) & 1, ctl);
+                if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar(FULL + s), np * K::PAGE);
+                __syncwarp();
+                // (default cache policy: every query block of the sequence reads these pages, from L2)
+                if (lane < np)
+                    bulk_g2s(ring + s * K::TILE + lane * K::PAGE,
+                             src + ((size_t)blk * p.cache_kv_heads + it.g) * K::PAGE, K::PAGE, bar(FULL + s));
+                ++kc;
             }
-            bool w = true;
-            if (t >= NSR && lane == 0) w = wait(bar(EMPTY + s), ((t - NSR) / NSR) & 1, ctl);
-            if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(FULL + s), np * K::PAGE);
-            __syncwarp();
-            // (default cache policy: every query block of the sequence reads these pages, from L2)
-            if (lane < np)
-                bulk_g2s(ring + s * K::TILE + lane * K::PAGE, src + ((size_t)blk * p.cache_kv_heads + g) * K::PAGE,
-                         K::PAGE, bar(FULL + s));
-            ++kc;
         }
         // drain: the copies in flight land before the CTA exits
         if (lane == 0) {
@@ -558,13 +642,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
         // warp 11: i = 1): PV_i(t) once P_i(t) is written, then S_i(t + 1) once K(t + 1) has landed.
         // Each row tile's S, P and O sit in its own TMEM columns and one thread's tcgen05.mma ops
         // run in issue order; while one issuer waits for its P, the other keeps the tensor core fed.
-        const int i = warp - kMma, nt = two ? 2 : 1;    // row tiles with rows in the window
-        if (lane == 0 && i < nt) {
+        const int i = warp - kMma;
+        if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kRows, kKeys, false, false);
             constexpr uint32_t idPV = idesc_f16_f32(kRows, D, false, true);
             const uint32_t qbase = sb + K::OFF_Q + i * K::QBYTES, sfull = tmem + i * kKeys;
+            int gk = 0, gvt = 0;                          // the CTA's K and V tiles so far (ring slots, phases)
+            int pcnt = 0, ocnt = 0, n = 0;                // this row tile's P tiles and items; the CTA's items
+            Item it = first;
             auto issue_s = [&](int t) {
-                const uint32_t kbase = sb + K::OFF_K + (t % NSK) * K::TILE;
+                const int kt = gk + t;
+                const uint32_t kbase = sb + K::OFF_K + (kt % NSK) * K::TILE;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint64_t a = smem_desc(qbase + k * 256, 128, K::NCH * 128);
@@ -572,37 +660,60 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                     mma_bf16(sfull, a, bk, idS, k > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(SFULL + i));
-                mma_commit(bar(KEMPTY + t % NSK));        // (K(t) is free once both row tiles' S(t) ran)
+                mma_commit(bar(KEMPTY + kt % NSK));       // (K(t) is free once both row tiles' S(t) ran)
             };
             // PV_i(t): one page (16 keys = 8 columns of fp16 P_i pairs) per MMA
             auto issue_pv = [&](int t) {
-                const int np = min(kTP, nb - t * kTP);
-                const uint32_t vbase = sb + K::OFF_V + (t % NSV) * K::TILE;
+                const int np = min(kTP, it.nb - t * kTP), vt = gvt + t;
+                const uint32_t vbase = sb + K::OFF_V + (vt % NSV) * K::TILE;
                 const uint32_t o = tmem + K::COL_O + i * D;
                 for (int pg = 0; pg < np; ++pg) {
                     const uint64_t bv = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
                     mma_bf16_tmem_a(o, sfull + pg * 8, bv, idPV, (t > 0 || pg > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(VEMPTY + t % NSV));
+                mma_commit(bar(VEMPTY + vt % NSV));
             };
-            bool ok = wait(bar(QFULL), 0, ctl) && wait(bar(KFULL), 0, ctl);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-            }
-            for (int t = 0; t < T && ok; ++t) {
-                // row tile 0 converts V(t) (before it signals P_0(t)): row tile 1 waits for it
-                if (i == 1 && !(ok = wait(bar(VREADY + t % NSV), (t / NSV) & 1, ctl))) break;
-                if (!(ok = wait(bar(PFULL + i), t & 1, ctl))) break;
-                tc_fence_after();
-                issue_pv(t);
-                if (t + 1 < T) {
-                    if (!(ok = wait(bar(KFULL + (t + 1) % NSK), ((t + 1) / NSK) & 1, ctl))) break;
+            bool ok = true;
+            int kr = k0;
+            for (int j = j0; j < total && ok; j = next_item(p, kr, total, qblocks, it), ++n) {
+                const int T = it.T;
+                if (!(ok = wait(bar(QFULL), n & 1, ctl))) break;
+                if (i == 0 || it.two) {
+                    if (!(ok = wait(bar(KFULL + gk % NSK), (gk / NSK) & 1, ctl))) break;
                     tc_fence_after();
-                    issue_s(t + 1);
+                    issue_s(0);
+                    for (int t = 0; t < T && ok; ++t) {
+                        // row tile 0 converts V(t) (before it signals P_0(t)): row tile 1 waits for it
+                        if (i == 1 && !(ok = wait(bar(VREADY + (gvt + t) % NSV), ((gvt + t) / NSV) & 1, ctl))) break;
+                        if (!(ok = wait(bar(PFULL + i), pcnt & 1, ctl))) break;
+                        ++pcnt;
+                        // the first PV of an item starts O_i afresh: the last item's epilogue has read it
+                        if (t == 0 && ocnt > 0 && !(ok = wait(bar(OFREE + i), (ocnt - 1) & 1, ctl))) break;
+                        tc_fence_after();
+                        issue_pv(t);
+                        if (t + 1 < T) {
+                            const int kt = gk + t + 1;
+                            if (!(ok = wait(bar(KFULL + kt % NSK), (kt / NSK) & 1, ctl))) break;
+                            tc_fence_after();
+                            issue_s(t + 1);
+                        } else {
+                            mma_commit(bar(ODONE + i));
+                        }
+                    }
+                    ++ocnt;
                 } else {
-                    mma_commit(bar(ODONE + i));
+                    // row tile 1 has no rows in this item: release its share of every K and V slot,
+                    // each once that slot's tile has landed (so the arrival counts for that tile)
+                    for (int t = 0; t < T && ok; ++t) {
+                        const int kt = gk + t, vt = gvt + t;
+                        if (!(ok = wait(bar(KFULL + kt % NSK), (kt / NSK) & 1, ctl))) break;
+                        mma_commit(bar(KEMPTY + kt % NSK));
+                        if (!(ok = wait(bar(VFULL + vt % NSV), (vt / NSV) & 1, ctl))) break;
+                        mma_commit(bar(VEMPTY + vt % NSV));
+                    }
                 }
+                gk += T;
+                gvt += T;
             }
             mma_commit(bar(DRAIN));
             // every MMA issued has completed before TMEM is freed
@@ -624,15 +735,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
 
 }  // namespace prefill
 
-cudaError_t launch_prefill(const AttnParams& p, int head_dim, cudaStream_t st) {
+cudaError_t launch_prefill(const AttnParams& p, int head_dim, int num_sms, cudaStream_t st) {
+    // persistent: one CTA per SM (at most one per work item), taking items round-robin
     const int qblocks = (int)(((int64_t)p.max_q_len * p.group + prefill::kCtaRows - 1) / prefill::kCtaRows);
-    const int64_t grid = (int64_t)p.num_seqs * p.num_kv_heads * qblocks;
-    if (grid < 1 || grid > 0x7fffffff) return cudaErrorInvalidValue;
+    const int64_t items = (int64_t)p.num_seqs * p.num_kv_heads * qblocks;
+    if (items < 1 || items > 0x7fffffff || num_sms < 1) return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)std::min<int64_t>(items, num_sms);
     static std::atomic<uint64_t> set64{0}, set128{0};
     if (head_dim == 128)
-        return launch_pdl_bigsmem(set128, prefill::prefill_kernel<128>, dim3((unsigned)grid), dim3(prefill::kThreads),
+        return launch_pdl_bigsmem(set128, prefill::prefill_kernel<128>, dim3(grid), dim3(prefill::kThreads),
                                   (size_t)prefill::Cfg<128>::SMEM, st, p, qblocks);
-    return launch_pdl_bigsmem(set64, prefill::prefill_kernel<64>, dim3((unsigned)grid), dim3(prefill::kThreads),
+    return launch_pdl_bigsmem(set64, prefill::prefill_kernel<64>, dim3(grid), dim3(prefill::kThreads),
                               (size_t)prefill::Cfg<64>::SMEM, st, p, qblocks);
 }
 
