@@ -63,12 +63,14 @@ struct Cfg {
     static constexpr int OFF_K = OFF_Q + 2 * QBYTES;      // K ring
     static constexpr int OFF_V = OFF_K + NSK * TILE;      // V ring
     static constexpr int OFF_BAR = OFF_V + NSV * TILE;
-    // barriers: KFULL[NSK] KEMPTY[NSK] VFULL[NSV] VEMPTY[NSV] VREADY[NSV] SFULL[2] PFULL[2] QFULL ODONE[2]
-    // OFREE[2] DRAIN
+    // barriers: KFULL[NSK] KEMPTY[NSK] VFULL[NSV] VEMPTY[NSV] VREADY[NSV] SFULL[2] PFA[2] PFB[2] PVA[2]
+    // QFULL ODONE[2] OFREE[2] DRAIN  (PFA / PFB: P of a tile's first / last 64 keys written; PVA: the
+    // P.V of its first 64 keys done)
     static constexpr int KFULL = 0, KEMPTY = NSK, VFULL = 2 * NSK, VEMPTY = 2 * NSK + NSV,
-                         VREADY = 2 * NSK + 2 * NSV, SFULL = 2 * NSK + 3 * NSV, PFULL = SFULL + 2,
-                         QFULL = SFULL + 4, ODONE = SFULL + 5, OFREE = SFULL + 7, DRAIN = SFULL + 9;
-    static constexpr int NBAR = SFULL + 10;
+                         VREADY = 2 * NSK + 2 * NSV, SFULL = 2 * NSK + 3 * NSV, PFA = SFULL + 2, PFB = SFULL + 4,
+                         PVA = SFULL + 6, QFULL = SFULL + 8, ODONE = SFULL + 9, OFREE = SFULL + 11,
+                         DRAIN = SFULL + 13;
+    static constexpr int NBAR = SFULL + 14;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem address, abort flags, qoff
     static constexpr int SMEM = OFF_MISC + 16 + 128;      // (+ alignment slack)
     // TMEM columns: S/P_0, S/P_1 (128 each), O_0, O_1 (D each)
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
     auto bar = [&](int i) -> uint32_t { return sb + K::OFF_BAR + 8 * i; };
     constexpr int NSK = K::NSK, NSV = K::NSV, KFULL = K::KFULL, VFULL = K::VFULL, KEMPTY = K::KEMPTY,
                   VEMPTY = K::VEMPTY, VREADY = K::VREADY,
-                  SFULL = K::SFULL, PFULL = K::PFULL, QFULL = K::QFULL, ODONE = K::ODONE,
+                  SFULL = K::SFULL, PFA = K::PFA, PFB = K::PFB, PVA = K::PVA, QFULL = K::QFULL, ODONE = K::ODONE,
                   OFREE = K::OFREE, DRAIN = K::DRAIN;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K::OFF_MISC + 4);
@@ -216,7 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(SFULL + i), 1);
-            mbar_init(bar(PFULL + i), kRows);
+            mbar_init(bar(PFA + i), kRows);
+            mbar_init(bar(PFB + i), kRows);
+            mbar_init(bar(PVA + i), 1);
             mbar_init(bar(ODONE + i), 1);
             mbar_init(bar(OFREE + i), kRows);
         }
@@ -291,12 +295,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
         // fp16 subnormals: weights below 2^-14 of the new maximum).
         constexpr float kBig = 15.f;
         float m = -INFINITY, l = 0.f, pend = -INFINITY;
+        // (sent_a: this tile's first 64 keys' P has been signalled; its P.V then also reads them, so
+        // once that P.V has completed, O holds them and only the P written since is rescaled)
+        bool sent_a = false;
+        int cur_tile = 0;                                  // this row tile's tile number (PVA phase)
         auto raise_ref = [&](float target, int c, uint64_t& acc) {
             const float inc = target > m + kBig ? fminf(ceilf(target - m), 254.f) : 0.f;
             const int k = (int)inc;
             const float alpha = k < 127 ? __uint_as_float((uint32_t)(127 - k) << 23) : 0.f;
+            int c0 = 0;
+            if (sent_a) {
+                wait_all(bar(PVA + i), cur_tile & 1);
+                tc_fence_after();
+                c0 = kKeys / 4;                            // (P of the first 64 keys: 32 columns)
+            }
 #pragma unroll 1
-            for (int cc = 0; cc < c / 2; cc += 16) {          // the P columns written so far
+            for (int cc = c0; cc < c / 2; cc += 16) {         // the P columns written so far
                 float o[16];
                 tmem_ld16(scol + cc, o);
                 uint32_t w[16];
@@ -374,6 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                 tmem_wait_ld_into(rb);
                 if (c + 64 < kKeys) tmem_ld32_async(scol + c + 64, ra);
                 chunk(rb, c + 32, acc, pmaxw, mask);
+                if (c == 0) {
+                    // the first 64 keys' P is complete: their P.V may run while the rest is computed
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(PFA + i));
+                    sent_a = true;
+                }
                 if (c + 64 < kKeys) tmem_wait_ld_into(ra);
             }
             float a0, a1;
@@ -469,6 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                 if (!(ok = wait_all(bar(SFULL + i), scnt & 1))) break;
                 tc_fence_after();
                 rem_c = lim - t * kKeys;
+                cur_tile = scnt;
+                sent_a = false;
                 if (__any_sync(0xffffffffu, pend > m + kSlack)) {
                     const bool up = pend > m + kSlack;
                     const float alpha = up ? exp2_fast(m - pend) : 1.f;
@@ -516,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(PFULL + i));
+                if (!sent_a) mbar_arrive(bar(PFA + i));
+                mbar_arrive(bar(PFB + i));
                 ++scnt;
                 if (i == 0 && t + 1 < T && !(ok = convert_v(gv + t + 1, t + 1))) break;
             }
@@ -662,16 +686,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                 mma_commit(bar(SFULL + i));
                 mma_commit(bar(KEMPTY + kt % NSK));       // (K(t) is free once both row tiles' S(t) ran)
             };
-            // PV_i(t): one page (16 keys = 8 columns of fp16 P_i pairs) per MMA
-            auto issue_pv = [&](int t) {
-                const int np = min(kTP, it.nb - t * kTP), vt = gvt + t;
+            // PV_i(t) over pages [pa, pz) of the tile: one page (16 keys = 8 columns of fp16 P_i pairs)
+            // per MMA
+            auto issue_pv = [&](int t, int pa, int pz) {
+                const int vt = gvt + t;
                 const uint32_t vbase = sb + K::OFF_V + (vt % NSV) * K::TILE;
                 const uint32_t o = tmem + K::COL_O + i * D;
-                for (int pg = 0; pg < np; ++pg) {
+                for (int pg = pa; pg < pz; ++pg) {
                     const uint64_t bv = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
                     mma_bf16_tmem_a(o, sfull + pg * 8, bv, idPV, (t > 0 || pg > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(VEMPTY + vt % NSV));
             };
             bool ok = true;
             int kr = k0;
@@ -685,12 +709,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                     for (int t = 0; t < T && ok; ++t) {
                         // row tile 0 converts V(t) (before it signals P_0(t)): row tile 1 waits for it
                         if (i == 1 && !(ok = wait(bar(VREADY + (gvt + t) % NSV), ((gvt + t) / NSV) & 1, ctl))) break;
-                        if (!(ok = wait(bar(PFULL + i), pcnt & 1, ctl))) break;
-                        ++pcnt;
+                        // P.V of the first 64 keys as soon as their P is written, of the rest after
+                        const int np = min(kTP, it.nb - t * kTP);
+                        if (!(ok = wait(bar(PFA + i), pcnt & 1, ctl))) break;
                         // the first PV of an item starts O_i afresh: the last item's epilogue has read it
                         if (t == 0 && ocnt > 0 && !(ok = wait(bar(OFREE + i), (ocnt - 1) & 1, ctl))) break;
                         tc_fence_after();
-                        issue_pv(t);
+                        issue_pv(t, 0, min(np, kTP / 2));
+                        mma_commit(bar(PVA + i));
+                        if (!(ok = wait(bar(PFB + i), pcnt & 1, ctl))) break;
+                        ++pcnt;
+                        tc_fence_after();
+                        issue_pv(t, kTP / 2, np);
+                        mma_commit(bar(VEMPTY + (gvt + t) % NSV));
                         if (t + 1 < T) {
                             const int kt = gk + t + 1;
                             if (!(ok = wait(bar(KFULL + kt % NSK), (kt / NSK) & 1, ctl))) break;
