@@ -109,3 +109,17 @@ def test_fp8_scales_are_absmax_over_448():
         for g in range(2):
             exp = np.float32(np.abs(allk[sel, g]).max()) / np.float32(448.0)
             assert w.k_scales[blk, g] == exp
+
+
+def test_causal_flops_counts_every_visible_pair():
+    """The prefill metric's FLOP count: 4 * D * Hq per (query, visible key),
+    against a brute-force count of the pairs the definition makes visible
+    (query i of sequence b sees positions 0 .. L_b - Q_b + i)."""
+    from paged_kv_decode_14_gb300 import workloads as wl
+    w = wl.make_workload("flops", context_lens=[1, 17, 40, 300, 0], q_lens=[1, 5, 40, 128, 0], num_q_heads=8,
+                         num_kv_heads=2, head_dim=64, seed=3)
+    pairs = 0
+    for L, Q in zip(w.context_lens.tolist(), w.q_lens.tolist()):
+        for i in range(Q):
+            pairs += sum(1 for j in range(L) if j <= L - Q + i)
+    assert wl.causal_flops(w) == 4 * 64 * 8 * pairs
