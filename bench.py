@@ -383,7 +383,7 @@ def run_prefill(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "flops_per_step": flops, "attention_us": attn_us, "append_us": step_us - attn_us,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": load_traffic(w.name),
                          "peak_kind": f"{kind} (cuBLAS bf16 GEMM burst; fp16 runs at the same rate)",
                          "kernel": "paged chunked prefill (tcgen05, two 128-row tiles per CTA)",
                          "algorithmic_flops_per_launch": flops, "avg_launch_us": attn_us,
