@@ -1421,6 +1421,13 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         *reinterpret_cast<uint4*>(pdst + (K::OFF_PLO - K::OFF_P) + cc * (16 * 128)) =
                             make_uint4(l4[0], l4[1], l4[2], l4[3]);
                 }
+                if constexpr (FP8) {
+                    // this warpgroup widens V(t) (it has time to spare between tiles; the epilogue
+                    // warpgroup keeps the piece epilogues): every thread acquires the landed pages
+                    wait_bar(bar(B::VLAND + vs), (t / NSV) & 1, ctl);
+                    widen(smem + K::OFF_V + vs * (K::TILE + K::VSLACK), tt, kBarSoft);
+                    mbar_arrive(bar(B::VFULL + vs));
+                }
                 // unwritten tail slots of the sequence's last page: zero their V rows (they may hold NaN)
                 if (k < np && pos >= L) {
                     wait_bar(bar(B::VFULL + vs), (t / NSV) & 1, ctl);
@@ -1519,64 +1526,12 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 d.pc = pc;
                 return d;
             };
-            if constexpr (!FP8) {
-                for (int pc = 0;; ++pc) {
-                    const bool okr = wait_bar(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1, ctl);
-                    if (bar_red_or(kBarEpi, kSoftThreads, !okr)) break;
-                    const PieceDesc d = take_piece(pc);
-                    piece_epilogue(d, tt, kBarEpi);
-                    if (d.last) break;
-                }
-            } else {
-                // FP8: this warpgroup also widens every V tile in place (K stays e4m3
-                // for the S MMA).  Each round takes whatever is ready: a finished
-                // piece's epilogue, the next V tile (agreed across the warpgroup by bar.red).
-                const int T = tile_count();
-                int vt = 0, pc = 0;
-                bool epi_done = false;
-                uint64_t t_prog = globaltimer_ns();
-                while (vt < T || !epi_done) {
-                    bool did = false;
-                    // (one thread probes, the warpgroup agrees; a piece is taken once its O^T
-                    // is complete too: its last V tile may still be waiting here for widening)
-                    if (!epi_done &&
-                        bar_red_or(kBarEpi, kSoftThreads,
-                                   tt == 0 && mbar_test_wait(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1) &&
-                                       mbar_test_wait(bar(B::ODONE + (pc & 1)), (pc >> 1) & 1))) {
-                        wait_bar(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1, ctl);   // (acquire in every thread)
-                        const PieceDesc d = take_piece(pc);
-                        piece_epilogue(d, tt, kBarEpi);
-                        epi_done = d.last;
-                        ++pc;
-                        did = true;
-                    }
-                    if (vt < T) {
-                        const int vs = vt % NSV;
-                        if (bar_red_or(kBarEpi, kSoftThreads, tt == 0 && mbar_test_wait(bar(B::VLAND + vs), (vt / NSV) & 1))) {
-                            wait_bar(bar(B::VLAND + vs), (vt / NSV) & 1, ctl);   // (acquire in every thread)
-                            widen(smem + K::OFF_V + vs * (K::TILE + K::VSLACK), tt, kBarEpi);
-                            mbar_arrive(bar(B::VFULL + vs));
-                            ++vt;
-                            did = true;
-                        }
-                    }
-                    if (did) {
-                        t_prog = globaltimer_ns();
-                    } else {
-                        // nothing ready: give up on an abort, or after the wait limit without progress
-                        bool stuck = false;
-                        if (tt == 0) {
-                            stuck = *abort_flag != 0;
-                            if (!stuck && globaltimer_ns() - t_prog > p.wait_limit_ns) {
-                                raise_error(p.err, PKV_DEVERR_TIMEOUT);
-                                *abort_flag = 1;
-                                stuck = true;
-                            }
-                        }
-                        if (bar_red_or(kBarEpi, kSoftThreads, stuck)) break;
-                        __nanosleep(96);
-                    }
-                }
+            for (int pc = 0;; ++pc) {
+                const bool okr = wait_bar(bar(B::PREADY + (pc & 1)), (pc >> 1) & 1, ctl);
+                if (bar_red_or(kBarEpi, kSoftThreads, !okr)) break;
+                const PieceDesc d = take_piece(pc);
+                piece_epilogue(d, tt, kBarEpi);
+                if (d.last) break;
             }
         }
     }
