@@ -6,29 +6,34 @@
 // table equals dense attention): query i of sequence b, query head h, sees
 // positions 0 .. L_b - Q_b + i of kv-head h / G.
 //
-// A CTA owns 256 query rows of one kv-head -- 256 / G consecutive query
-// positions x the G heads of the group (row r = position r / G, head r % G) --
-// as two 128-row tiles, so every K/V page it streams serves 256 rows.  It
-// walks 128-key tiles (8 pages) up to its rows' causal limit; per key tile t
-// and row tile i:
-//   S_i[128 rows, 128 keys] = Q_i . K_t^T          (M=128, N=128, K-major A and B in shared memory)
-//   softmax per row (one thread per row = TMEM lane, two reads of S: max, then P)
-//   O_i[128 rows, D] += P_hi . V_t + P_lo . V_t    (M=128, N=D, A from TMEM, B MN-major in shared memory)
-// S, P and O live in TMEM (S_0, S_1: 128 columns each; O_0, O_1: D each).
-// P = 2^(s - m) is split into a bf16 high part and the bf16 rounding of its
-// remainder, so the weights keep ~16 significant bits (one bf16 P misses the
-// 2e-3 tolerance on rows that average a handful of keys).  Each 16-key chunk
-// of S is replaced in place by its 8 columns of P_hi pairs and 8 of P_lo
-// pairs.  The cache's page layout is already the canonical no-swizzle operand
+// A work item is 256 query rows of one kv-head -- 256 / G consecutive query
+// positions x the G heads of the group (row r = position r / G, head r % G)
+// -- held as two 128-row tiles, so every K/V page a CTA streams serves 256
+// rows.  The CTAs are persistent (one per SM) and take items heavy first in
+// serpentine rounds.  An item walks 128-key tiles (8 pages) up to its rows'
+// causal limit; per key tile t and row tile i:
+//   S_i[128 rows, 128 keys] = Q_i . K_t^T     (M=128, N=128, K-major A and B in shared memory)
+//   softmax per row (one thread per row = TMEM lane), one pass against the
+//     row's running reference maximum
+//   O_i[128 rows, D] += P_i . V_t             (M=128, N=D, fp16 A from TMEM, fp16 B MN-major in shared memory)
+// S, P and O live in TMEM (S/P_0, S/P_1: 128 columns each; O_0, O_1: D each).
+// P = 2^(s - m) is written as fp16 pairs over the S columns already read
+// (fp16 keeps 11 significant bits; bf16 P misses the 2e-3 tolerance on rows
+// that average a handful of keys), and V is turned from bf16 into fp16 in
+// shared memory once per tile, since both operands of one MMA have the same
+// type.  The cache's page layout is already the canonical no-swizzle operand
 // layout: K pages are K-major B operands, V pages MN-major B operands, so
 // pages go HBM -> shared memory by 1-D bulk copies.  O is rescaled in TMEM
 // only when a row's maximum rises by more than 2^8 (exp2 units).
 //
-// Roles: warps 0-3 softmax of row tile 0, warps 4-7 of row tile 1 (thread =
-// row; they also run the epilogue), warp 8 producer (block table, bulk
-// copies), warp 9 MMA issuer, in the order
-//   S_0(0) S_1(0) | PV_0(0) S_0(1) PV_1(0) S_1(1) | PV_0(1) S_0(2) ...
-// so one row tile's softmax runs while the tensor core works for the other.
+// Roles (384 threads): warps 0-3 softmax of row tile 0, warps 4-7 of row
+// tile 1 (thread = row; they also run the epilogue, and row tile 0 converts
+// V), warp 8 the K producer and warp 9 the V producer (block table, bulk
+// copies into their own rings), warps 10 and 11 the MMA issuers of row tiles
+// 0 and 1.  Issuer i runs, per tile,
+//   PV_i(t, first 64 keys) once their P is written | PV_i(t, rest) | S_i(t + 1)
+// so one row tile's softmax runs while the tensor core works for the other,
+// and the first half of P.V overlaps the softmax of the second.
 // tcgen05.mma ops of one thread run in issue order: S_i(t + 1) overwrites P_i
 // only after PV_i(t) has read it, and when S_i(t + 1) signals, PV_i(t) has
 // completed, so the softmax may rescale O_i without another wait.  Every
