@@ -43,7 +43,8 @@
 // cp.async.
 //
 // Work partition: the balanced unit partition of common.cuh, one persistent
-// CTA per SM (for wide segments, cut by weight with a per-piece charge).  A
+// CTA per SM (for wide and FP8 segments, cut by weight with a fixed charge
+// per segment).  A
 // CTA takes its last piece first and then walks its range from the start, so
 // both pieces of every segment cut between two CTAs finish early and their
 // merge overlaps the rest of the work.
@@ -86,6 +87,9 @@ constexpr int kSeqTab = 256;                  // sequences the shared-memory tab
 
 // Online-softmax reference slack (powers of two), see the header comment.
 constexpr float kRescaleSlack = 8.f;
+// Units charged per segment in the weighted CTA cut of narrow FP8 segments
+// (wide: 24); measured best of 4-40 on the long FP8 batch
+constexpr int kNarrowCharge = 16;
 
 template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8>
 struct Cfg {
@@ -124,14 +128,14 @@ struct Cfg {
     static constexpr int SEQTAB = FP8 ? kSeqTab / 2 : kSeqTab;   // sequences the table holds
     static constexpr int OFF_GATHER = OFF_SEQ + SEQTAB * 16;
     static constexpr int GATHER = SPLIT ? RMAX * (D + 2) * 4 : 0;
-    // the weighted CTA boundaries (int [TABMAX + 1]), for wide segments
+    // the weighted CTA boundaries (int [TABMAX + 1])
     static constexpr int TABMAX = 160;
     static constexpr int OFF_BND = (OFF_GATHER + GATHER + 15) / 16 * 16;
-    static constexpr bool PTAB = !EWG && OFF_BND + (TABMAX + 1) * 4 + 128 <= kMaxSmem - 1024;
+    static constexpr bool PTAB = (FP8 || !EWG) && OFF_BND + (TABMAX + 1) * 4 + 128 <= kMaxSmem - 512;
     static constexpr int SMEM_USED = (PTAB ? OFF_BND + (TABMAX + 1) * 4 : OFF_GATHER + GATHER) + 128;  // + slack
     // One CTA per SM either way: take the whole per-block budget, so every
     // operand read the descriptors can form stays inside the allocation.
-    static constexpr int SMEM = kMaxSmem - 1024;
+    static constexpr int SMEM = kMaxSmem - 512;         // (static shared memory: < 300 bytes)
     static constexpr int COL_S = 0;                      // S^T buffers: NSB x NPAD columns
     // O^T accumulators: [piece parity][kv-head of the segment] x NPAD columns.
     // Each kv-head of a segment accumulates into its own: a P.V MMA of one
@@ -542,14 +546,16 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     Cursor cur0, curt;
     int u0, u1, W, P;
     int4* seqtab = p.num_seqs <= K::SEQTAB ? reinterpret_cast<int4*>(smem + K::OFF_SEQ) : nullptr;
-    // Wide segments (epilogue in the softmax warps, about three tiles of time
-    // per piece) cut the CTA ranges by weight, charging every segment piece 24
-    // units; narrow ones (epilogue off the softmax path) keep the equal split,
-    // which needs no table at the start.
-    int* bndtab = (K::PTAB && !EWG) ? reinterpret_cast<int*>(smem + K::OFF_BND) : nullptr;
+    // Wide and FP8 segments cut the CTA ranges by weight: every segment is
+    // charged a fixed number of units on top of its own for what a piece costs
+    // beyond its bytes (its partial last tile, which takes a whole tile's time,
+    // the piece start and, for wide segments, the epilogue in the softmax warps:
+    // about three tiles).  Narrow bf16 segments keep the equal split, which
+    // needs no table at the start (the table cost them ~2 us a launch).
+    int* bndtab = K::PTAB ? reinterpret_cast<int*>(smem + K::OFF_BND) : nullptr;
     bool tab_used = false;
     const bool has_work = plan_locate<kThreads, CASC>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt,
-                                                seqtab, bndtab, K::TABMAX, 24, &tab_used,
+                                                seqtab, bndtab, K::TABMAX, EWG ? kNarrowCharge : 24, &tab_used,
                                                 reinterpret_cast<int4*>(smem + K::OFF_P),   // (P ring unused yet)
                                                 CASC ? nullptr : &lq);
     const Part part{W, P, tab_used ? bndtab : nullptr};
