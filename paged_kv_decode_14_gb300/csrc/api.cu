@@ -23,8 +23,8 @@ int tc_heads_per_segment(int num_kv_heads, int rows);
 // Kernel choice and grid for one attention call, in virtual kv-heads (vheads
 // of group vgroup; kv_split of them per cache kv-head): the tensor-core
 // kernel for bf16 caches (R = vgroup * max_q_len <= 32 always) and for FP8
-// caches with head_dim 128 and R <= 8 (one persistent CTA per SM, all of its
-// ~227 KiB of shared memory), else the CUDA-core kernel (4 CTAs per SM).
+// caches with R <= 8 (one persistent CTA per SM, all of its ~227 KiB of
+// shared memory), else the CUDA-core kernel (4 CTAs per SM).
 // rows_pad: partial-slot rows (the tensor-core kernel keeps up to 32 columns
 // of several kv-heads per segment).  Virtual kv-heads that share cache pages
 // are never grouped in one segment (its pages are copied as one run).
@@ -32,7 +32,7 @@ AttnLaunch plan_attention(const pkv_cache* c, int vgroup, int vheads, int kv_spl
                           int num_sms) {
     AttnLaunch L;
     const int rows = vgroup * max_q_len;
-    L.tc = c->kv_dtype == PKV_KV_BF16 ? rows <= 32 : (c->head_dim == 128 && rows <= 8);
+    L.tc = c->kv_dtype == PKV_KV_BF16 ? rows <= 32 : rows <= 8;
     L.ncta = num_ctas > 0 ? num_ctas : (L.tc ? num_sms : 4 * num_sms);
     L.rows_pad = L.tc ? 32 : simt_rows_pad(rows);
     L.hg = (L.tc && kv_split == 1) ? tc_heads_per_segment(vheads, rows) : 1;

@@ -34,7 +34,7 @@
 // the CUDA cores (except zeroing the unwritten tail rows of a sequence's last
 // page, which may hold NaN).
 //
-// FP8 (e4m3) caches, head_dim 128, NCOL <= 8: the K pages stay e4m3 and S^T
+// FP8 (e4m3) caches, NCOL <= 8: the K pages stay e4m3 and S^T
 // runs on kind::f8f6f4 MMAs against the q rows, each scaled by a power of two
 // and split exactly into two e4m3 terms (columns n and 8 + n, added in the
 // softmax with the page's k scale); the V pages land in the upper half of a
@@ -589,39 +589,46 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     };
     // Widen one operand slot in place: the bulk copy left the tile's e4m3 pages
     // (layout [2][D/16][8][16] bytes) in the slot's upper half.  Each thread of
-    // a 128-thread warpgroup (named barrier bid) reads its 16-byte chunk of
-    // every page, the warpgroup syncs, then writes the bf16 operand
-    // ([2][D/8][8][8] elements per page) over the whole slot.  Codes are exact
-    // in bf16; the page scales are applied in the softmax.
+    // a 128-thread warpgroup (named barrier bid) reads its 16-byte chunk e of
+    // NPT of the pages (D = 128: chunk tt of all 8 pages; D = 64, 64 chunks a
+    // page: chunk tt % 64 of pages tt / 64, tt / 64 + 2, ...), the warpgroup
+    // syncs, then writes the bf16 operand ([2][D/8][8][8] elements per page)
+    // over the whole slot.  Codes are exact in bf16; the page scales are
+    // applied in the softmax.
     auto widen = [&](uint8_t* slot, int tt, int bid) {
-        static_assert(!FP8 || K::PAGE8 / 16 == kSoftThreads, "one chunk of every page per thread");
+        constexpr int CPP8 = K::PAGE8 / 16;                  // 16-byte chunks of an e4m3 page
+        constexpr int PSTEP = kSoftThreads / CPP8;           // pages between a thread's pages
+        constexpr int NPT = kTP / PSTEP;                     // pages a thread widens
+        static_assert(!FP8 || (kSoftThreads % CPP8 == 0 && kTP % PSTEP == 0), "widening split");
         constexpr int NC16 = D / 16;
-        uint4 v[kTP];
+        const int e = tt % CPP8, k0 = tt / CPP8;
+        uint4 v[NPT];
 #pragma unroll
-        for (int k = 0; k < kTP; ++k)
-            v[k] = *reinterpret_cast<const uint4*>(slot + K::OFF_LAND + k * K::PAGE8 + tt * 16);
+        for (int j = 0; j < NPT; ++j)
+            v[j] = *reinterpret_cast<const uint4*>(slot + K::OFF_LAND + (k0 + j * PSTEP) * K::PAGE8 + e * 16);
         named_bar_sync(bid, kSoftThreads);
         // NaN codes are rare (a NaN value stored in the cache; the unwritten slots of a
         // sequence's last page may hold anything): a cheap test over the thread's own
         // chunks, and the exact fix of the chunks it wrote only when it hits
         uint32_t nb = 0;
 #pragma unroll
-        for (int k = 0; k < kTP; ++k)
-            nb |= e4m3_nan_bits(v[k].x) | e4m3_nan_bits(v[k].y) | e4m3_nan_bits(v[k].z) | e4m3_nan_bits(v[k].w);
-        const int r = tt & 7, c = (tt >> 3) % NC16, oh = tt / (8 * NC16);
-        uint8_t* d0 = slot + ((oh * (D / 8) + 2 * c) * 8 + r) * 16;
+        for (int j = 0; j < NPT; ++j)
+            nb |= e4m3_nan_bits(v[j].x) | e4m3_nan_bits(v[j].y) | e4m3_nan_bits(v[j].z) | e4m3_nan_bits(v[j].w);
+        // chunk e of a page: token group e / (8 NC16), 16-element column block (e / 8) % NC16, token e % 8
+        const int r = e & 7, c = (e >> 3) % NC16, oh = e / (8 * NC16);
+        uint8_t* d0 = slot + ((oh * (D / 8) + 2 * c) * 8 + r) * 16 + k0 * K::PAGE;
 #pragma unroll
-        for (int k = 0; k < kTP; ++k) {
-            const uint32_t wv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+        for (int j = 0; j < NPT; ++j) {
+            const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
             uint32_t o[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) e4m3x4_to_bf16x4(wv[j], o[2 * j], o[2 * j + 1]);
-            *reinterpret_cast<uint4*>(d0 + k * K::PAGE) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(d0 + k * K::PAGE + 128) = make_uint4(o[4], o[5], o[6], o[7]);
+            for (int x = 0; x < 4; ++x) e4m3x4_to_bf16x4(wv[x], o[2 * x], o[2 * x + 1]);
+            *reinterpret_cast<uint4*>(d0 + j * PSTEP * K::PAGE) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(d0 + j * PSTEP * K::PAGE + 128) = make_uint4(o[4], o[5], o[6], o[7]);
         }
         if (nb & 0x80808080u) {      // (stale pages past the tile's page count may hit too: harmless)
 #pragma unroll 1
-            for (int i = 0; i < 2 * kTP; ++i) fix_nan_lanes(d0 + (i >> 1) * K::PAGE + (i & 1) * 128);
+            for (int i = 0; i < 2 * NPT; ++i) fix_nan_lanes(d0 + (i >> 1) * PSTEP * K::PAGE + (i & 1) * 128);
         }
         fence_proxy_async_smem();             // the MMA reads the slot through the async proxy
     };
@@ -947,7 +954,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         // brought to [128, 256)), split exactly into hi + lo e4m3 terms (a
                         // bf16 value's 8 significant bits), stored as rows n and 8 + n; the
                         // softmax adds the two columns and multiplies by 2^-E_n
-                        static_assert(!FP8 || (K::NCH == 16 && QV == 4 && RMAX == 8), "FP8 q staging: D = 128, R <= 8");
+                        static_assert(!FP8 || ((K::NCH == 16 || K::NCH == 8) && RMAX == 8), "FP8 q staging: R <= 8");
                         int ek[QV];
 #pragma unroll
                         for (int k = 0; k < QV; ++k) {
@@ -958,7 +965,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                                 mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(wq[h] << 16)),
                                                      fabsf(__uint_as_float(wq[h] & 0xFFFF0000u))));
 #pragma unroll
-                            for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                            for (int o = K::NCH / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                             const int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
                             const int E = mx > 0.f ? min(126, max(-126, 7 - e)) : 0;
                             ek[k] = E;
@@ -983,12 +990,14 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                                 *reinterpret_cast<uint2*>(rh + (D / 16) * 128) = make_uint2(lo[0], lo[1]);
                             }
                         }
-                        // column n's factor -> lane n: row n sits in lanes (n & 1) * 16 + [0, 16), step n >> 1
+                        // column n's factor -> lane n: a step holds RPS rows, row n in lanes
+                        // (n % RPS) * NCH + [0, NCH) of step n / RPS
+                        constexpr int RPS = 32 / K::NCH;
                         int en = 0;
 #pragma unroll
                         for (int k = 0; k < QV; ++k) {
-                            const int v = __shfl_sync(0xffffffffu, ek[k], (lane & 1) * 16);
-                            if ((lane >> 1) == k) en = v;
+                            const int v = __shfl_sync(0xffffffffu, ek[k], (lane % RPS) * K::NCH);
+                            if (lane / RPS == k) en = v;
                         }
                         cur_c = __uint_as_float((uint32_t)(127 - en) << 23);
                     } else {
@@ -1578,9 +1587,10 @@ int tc_heads_per_segment(int num_kv_heads, int rows) {
     return hg;
 }
 
-// bf16 cache, head_dim 64/128, R = G * max_q_len <= 32.  Narrow segments (N =
-// 16) run the epilogue in its own warpgroup; wide ones (N = 32), whose softmax
-// needs more registers than a 384-thread block leaves, in the softmax warps.
+// bf16 cache, head_dim 64/128, R = G * max_q_len <= 32; FP8 cache, head_dim
+// 64/128, R <= 8.  Narrow segments (N = 16) run the epilogue in its own
+// warpgroup; wide ones (N = 32), whose softmax needs more registers than a
+// 384-thread block leaves, in the softmax warps.
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st) {
     const bool split = tc_col_limit(p.rows) == 8;
     if (p.cascade != 0) {                      // (bf16 caches only: the host checks)
@@ -1595,8 +1605,9 @@ cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int
         return fp8     ? tc::launch_t<128, 16, true, 4, 4, true, true>(p, ncta, st)
                : split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
                        : tc::launch_t<128, 32, false, 2, 2, false>(p, ncta, st);
-    return split ? tc::launch_t<64, 16, true, 4, 6, true>(p, ncta, st)
-                 : tc::launch_t<64, 32, false, 4, 4, false>(p, ncta, st);
+    return fp8     ? tc::launch_t<64, 16, true, 6, 8, true, true>(p, ncta, st)
+           : split ? tc::launch_t<64, 16, true, 4, 6, true>(p, ncta, st)
+                   : tc::launch_t<64, 32, false, 4, 4, false>(p, ncta, st);
 }
 
 }  // namespace pkv

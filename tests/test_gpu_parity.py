@@ -73,6 +73,12 @@ SWEEP = [
     (128, 16, 2, [1, 15, 16, 17, 130, 700], [1] * 6, "fp8"),   # FP8, G = 8: one kv-head per segment
     (128, 8, 2, [5, 40, 77, 300], [2, 1, 2, 1], "fp8"),        # FP8, R = 8 with a causal window
     (128, 8, 4, [0, 33, 0, 517], [0, 1, 0, 1], "fp8"),         # FP8, empty sequences, four kv-heads per segment
+    # FP8 with head_dim 64 on the tensor cores (1 KiB e4m3 pages, widened four pages a thread)
+    (64, 32, 8, [1, 15, 16, 17, 130, 700, 2000], [1] * 7, "fp8"),   # G = 4: two kv-heads per segment
+    (64, 16, 2, [5, 40, 77, 300], [1, 1, 1, 1], "fp8"),             # G = 8: one kv-head per segment
+    (64, 8, 4, [9, 200, 33, 517], [2, 1, 4, 1], "fp8"),             # G = 2, causal windows, R <= 8
+    (64, 8, 8, [0, 33, 0, 517, 64], [0, 1, 0, 1, 1], "fp8"),        # G = 1: four kv-heads per segment
+    (64, 32, 8, np.random.default_rng(904).integers(1, 1500, 96).tolist(), [1] * 96, "fp8"),
     # verify windows (R = 20, wide segments: the weighted cut) over short and long sequences
     (128, 32, 8, [20, 700, 33, 17, 400, 90, 16, 1000], [5] * 8, "bf16"),
     # large batches: past the shared-memory sequence table (256 bf16 / 128 FP8
@@ -132,7 +138,8 @@ def test_fp8_subnormal_codes():
 
 @pytest.mark.parametrize("head_dim,group,num_kv_heads,dtype", [
     (128, 4, 2, "fp8"),     # tensor-core FP8 kernel, two kv-heads per segment
-    (64, 4, 2, "fp8"),      # CUDA-core FP8 kernel (head_dim 64)
+    (64, 4, 2, "fp8"),      # tensor-core FP8 kernel, head_dim 64
+    (64, 16, 2, "fp8"),     # CUDA-core FP8 kernel, head_dim 64 (G * Q > 8)
     (128, 16, 2, "fp8"),    # CUDA-core FP8 kernel (G * Q > 8)
     (128, 4, 2, "bf16"),    # tensor-core narrow kernel, two kv-heads per segment
     (64, 1, 4, "bf16"),     # narrow kernel, four kv-heads per segment

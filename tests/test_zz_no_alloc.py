@@ -38,12 +38,15 @@ def _case(which):
     if which == "fp8_tc":        # FP8, head_dim 128, G * Q <= 8: the tensor-core kernel
         return wl.make_workload("f8", context_lens=[900, 33, 1700, 5], q_lens=[1, 1, 1, 1], num_q_heads=32,
                                 num_kv_heads=8, head_dim=128, kv_dtype="fp8", seed=92, outlier_p=0.01)
-    # FP8, head_dim 64: the CUDA-core kernel (its own rows_pad and grid of 4 CTAs per SM)
-    return wl.make_workload("f8s", context_lens=[900, 33, 1700, 5], q_lens=[1, 2, 1, 1], num_q_heads=32,
+    if which == "fp8_tc64":      # FP8, head_dim 64, G * Q = 8: the tensor-core kernel
+        return wl.make_workload("f8t", context_lens=[900, 33, 1700, 5], q_lens=[1, 2, 1, 1], num_q_heads=32,
+                                num_kv_heads=8, head_dim=64, kv_dtype="fp8", seed=94, outlier_p=0.01)
+    # FP8, head_dim 64, G * Q = 12: the CUDA-core kernel (its own rows_pad and grid of 4 CTAs per SM)
+    return wl.make_workload("f8s", context_lens=[900, 33, 1700, 5], q_lens=[1, 3, 1, 1], num_q_heads=32,
                             num_kv_heads=8, head_dim=64, kv_dtype="fp8", seed=93, outlier_p=0.01)
 
 
-@pytest.mark.parametrize("which", ["decode", "verify", "fp8_tc", "fp8_simt"])
+@pytest.mark.parametrize("which", ["decode", "verify", "fp8_tc", "fp8_tc64", "fp8_simt"])
 def test_noalloc_matches_workspace_entry_two_calls(which):
     """Two calls in a row, each bit-identical to pkv_paged_attention with a
     caller workspace (the same kernel, grid and partition, so the same sums
