@@ -336,15 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
             m += inc;
         };
         // P of 32 keys, two keys per packed fp32 operation (MASK: keys past this row's limit weigh
-        // 0); unless FORCE, nothing is stored (false) when some P would reach 2^kBig (or is NaN).
-        // Adds the chunk's P to acc and the largest fp16 P bit pattern (P >= 0: integer order is
-        // value order) to pmaxw.
-        auto emit_fast = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, uint32_t& pmaxw, bool force,
-                             bool mask) -> bool {
+        // 0); unless FORCE, nothing is stored (false) when the chunk's sum of P reaches 2^kBig (or
+        // is NaN): P >= 0, so no P reaches it otherwise.  Adds the chunk's P to acc.
+        auto emit_fast = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, bool force, bool mask) -> bool {
             const uint64_t sc2 = f2pack(__float_as_uint(sc), __float_as_uint(sc));
             const uint64_t nm2 = f2pack(__float_as_uint(-m), __float_as_uint(-m));
             uint64_t ca = 0;                               // (+0, +0)
-            uint32_t w[16], cm = 0;
+            uint32_t w[16];
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
                 float x0, x1;
@@ -357,16 +355,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                 ca = f2add(ca, f2pack(__float_as_uint(p0), __float_as_uint(p1)));
                 const __half2 h = __floats2half2_rn(p0, p1);
                 w[k >> 1] = *reinterpret_cast<const uint32_t*>(&h);
-                cm = __vmaxu2(cm, w[k >> 1]);
             }
-            if (!force && __any_sync(0xffffffffu, (cm & 0xffffu) >= 0x7800u || (cm >> 16) >= 0x7800u)) return false;
+            if (!force) {
+                float c0, c1;
+                f2unpack(ca, c0, c1);
+                if (__any_sync(0xffffffffu, !(c0 + c1 < 32768.f))) return false;
+            }
             acc = f2add(acc, ca);
-            pmaxw = __vmaxu2(pmaxw, cm);
             tmem_st16u(scol + (c >> 1), w);
             return true;
         };
-        auto chunk = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, uint32_t& pmaxw, bool mask) {
-            if (emit_fast(rr, c, acc, pmaxw, false, mask)) return;
+        auto chunk = [&](const uint32_t (&rr)[32], int c, uint64_t& acc, bool mask) {
+            if (emit_fast(rr, c, acc, false, mask)) return;
             // (rare) a logit more than 2^kBig above the reference: raise it first
             float c0 = -INFINITY, c1 = -INFINITY;
 #pragma unroll
@@ -375,24 +375,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                 c1 = fmaxf(c1, !mask || c + x + 1 <= rem_c ? __uint_as_float(rr[x + 1]) : -INFINITY);
             }
             raise_ref(fmaxf(c0, c1) * sc, c, acc);
-            emit_fast(rr, c, acc, pmaxw, true, mask);       // (P <= 1 now, but for NaN logits)
+            emit_fast(rr, c, acc, true, mask);              // (P <= 1 now, but for NaN logits)
         };
         // one pass over a tile once the row's reference is known, loads of the next 32 columns in
-        // flight while the previous 32 are turned into P; returns the tile's sum of P, and in
-        // pmaxw its largest P
-        auto fast_pass = [&](uint32_t& pmaxw, bool mask) -> float {
+        // flight while the previous 32 are turned into P; returns the tile's sum of P
+        auto fast_pass = [&](bool mask) -> float {
             uint64_t acc = 0;
-            pmaxw = 0;
             uint32_t ra[32], rb[32];
             tmem_ld32_async(scol, ra);
             tmem_wait_ld_into(ra);
 #pragma unroll 1
             for (int c = 0; c < kKeys; c += 64) {
                 tmem_ld32_async(scol + c + 32, rb);
-                chunk(ra, c, acc, pmaxw, mask);
+                chunk(ra, c, acc, mask);
                 tmem_wait_ld_into(rb);
                 if (c + 64 < kKeys) tmem_ld32_async(scol + c + 64, ra);
-                chunk(rb, c + 32, acc, pmaxw, mask);
+                chunk(rb, c + 32, acc, mask);
                 if (c == 0) {
                     // the first 64 keys' P is complete: their P.V may run while the rest is computed
                     tmem_wait_st();
@@ -506,12 +504,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnParams p
                 }
                 pend = -INFINITY;
                 if (__all_sync(0xffffffffu, m > -INFINITY) && sc > 0.f) {
-                    // reference known: one pass (masked on the causal diagonal).  A largest P of 2^e
-                    // or more (e >= kSlack) moves the reference up by e + 1 octaves at the next tile.
-                    uint32_t pw;
-                    l += __all_sync(0xffffffffu, rem_c >= kKeys - 1) ? fast_pass(pw, false) : fast_pass(pw, true);
-                    const uint32_t pm = max(pw & 0xffffu, pw >> 16);
-                    if (pm >= 0x5c00u && pm < 0x7c00u) pend = m + (float)((int)(pm >> 10) - 15 + 1);
+                    // reference known: one pass (masked on the causal diagonal).  A tile sum of P of
+                    // 2^e or more (e >= kSlack; it bounds the largest P) moves the reference up by
+                    // e + 1 octaves at the next tile.
+                    const float ts = __all_sync(0xffffffffu, rem_c >= kKeys - 1) ? fast_pass(false) : fast_pass(true);
+                    l += ts;
+                    if (ts >= 256.f && ts < INFINITY) pend = m + (float)((int)(__float_as_uint(ts) >> 23) - 127 + 1);
                 } else {
                     // two passes (a warp's first tile with keys, rows past the window): the tile's
                     // maximum over the visible keys first, then P
