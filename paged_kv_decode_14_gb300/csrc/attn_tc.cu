@@ -785,31 +785,43 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     den[x] = 0.f;
                     num[x] = 0.f;
                 }
-                for (int c = c_first; c <= c_last; ++c) {
-                    float m[8], l[8], a[8];
-                    if (c == cta) {
+                // the partials of MB CTAs at a time: every load in flight before the first is
+                // used (at the launch's end these reads queue behind the other CTAs' streams)
+                constexpr int MB = FP8 ? 2 : 1;
+                for (int cb = c_first; cb <= c_last; cb += MB) {
+                    float m[MB][8], l[MB][8], a[MB][8];
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) {
-                            m[x] = Mx[n0 + x];
-                            l[x] = Lsum[n0 + x];
-                            a[x] = acc[n0 + x];
-                        }
-                    } else {
-                        const float* sl = slot_ptr(p, c, d.S0, part.start(c));
+                    for (int j = 0; j < MB; ++j) {
+                        const int c = cb + j;
+                        if (c == cta) {
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) {
-                            const int n = n0 + x;
-                            m[x] = n < ncol ? __ldcg(sl + n) : -INFINITY;
-                            l[x] = n < ncol ? __ldcg(sl + p.rows_pad + n) : 0.f;
-                            a[x] = (n < ncol && tt < D) ? __ldcg(sl + 2 * p.rows_pad + (size_t)n * D + tt) : 0.f;
+                            for (int x = 0; x < 8; ++x) {
+                                m[j][x] = Mx[n0 + x];
+                                l[j][x] = Lsum[n0 + x];
+                                a[j][x] = acc[n0 + x];
+                            }
+                        } else {
+                            const bool cok = c <= c_last;
+                            const float* sl = slot_ptr(p, cok ? c : cta, d.S0, part.start(cok ? c : cta));
+#pragma unroll
+                            for (int x = 0; x < 8; ++x) {
+                                const int n = n0 + x;
+                                m[j][x] = cok && n < ncol ? __ldcg(sl + n) : -INFINITY;
+                                l[j][x] = cok && n < ncol ? __ldcg(sl + p.rows_pad + n) : 0.f;
+                                a[j][x] = (cok && n < ncol && tt < D) ? __ldcg(sl + 2 * p.rows_pad + (size_t)n * D + tt) : 0.f;
+                            }
                         }
                     }
 #pragma unroll
-                    for (int x = 0; x < 8; ++x) {
-                        float wo, wn;
-                        merge_weights(M[x], m[x], wo, wn);
-                        den[x] = merge_acc(den[x], wo, l[x], wn);
-                        num[x] = merge_acc(num[x], wo, a[x], wn);
+                    for (int j = 0; j < MB; ++j) {
+                        if (cb + j > c_last) break;
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            float wo, wn;
+                            merge_weights(M[x], m[j][x], wo, wn);
+                            den[x] = merge_acc(den[x], wo, l[j][x], wn);
+                            num[x] = merge_acc(num[x], wo, a[j][x], wn);
+                        }
                     }
                 }
 #pragma unroll
