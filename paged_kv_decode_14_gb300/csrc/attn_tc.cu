@@ -94,6 +94,10 @@ constexpr int kNarrowCharge = 16;
 template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8>
 struct Cfg {
     static constexpr int RMAX = SPLIT ? NPAD / 2 : NPAD;  // logical columns
+    // MMA N: NPAD rounded up to 16 (a wide kernel with NPAD = 24 computes 32 columns, and its
+    // softmax and epilogue touch only the first 24: P columns 24-31 are never written and only
+    // reach O columns that are never read)
+    static constexpr int NM = (NPAD + 15) / 16 * 16;
     static constexpr int PAGE = kBlock * D * 2;         // a page as bf16 MMA operand
     static constexpr int PAGE8 = kBlock * D;            // an FP8 cache page
     static constexpr int NSC = 16;                      // scale ring: tiles the producer may lead by, bounded
@@ -109,9 +113,9 @@ struct Cfg {
     // FP8 scale ring: float [NSC][32]: k scales [8], v scales [8], column factors [8]
     static constexpr int OFF_SC = OFF_V + NSV * (TILE + VSLACK);
     static constexpr int OFF_Q = OFF_SC + (FP8 ? NSC * 32 * 4 : 0);
-    static constexpr int QBUF = NPAD * D * 2;
+    static constexpr int QBUF = NM * D * 2;
     static constexpr int OFF_P = OFF_Q + 2 * QBUF;
-    static constexpr int PBUF = NPAD * kTileTok * 2;
+    static constexpr int PBUF = NM * kTileTok * 2;
     // wide segments (no high/low columns) keep P's low parts in a second ring
     static constexpr int OFF_PLO = OFF_P + NSB * PBUF;
     static constexpr int OFF_RED = OFF_PLO + (SPLIT ? 0 : NSB * PBUF);  // float [8 slots][RMAX]
@@ -136,14 +140,14 @@ struct Cfg {
     // One CTA per SM either way: take the whole per-block budget, so every
     // operand read the descriptors can form stays inside the allocation.
     static constexpr int SMEM = kMaxSmem - 512;         // (static shared memory: < 300 bytes)
-    static constexpr int COL_S = 0;                      // S^T buffers: NSB x NPAD columns
-    // O^T accumulators: [piece parity][kv-head of the segment] x NPAD columns.
+    static constexpr int COL_S = 0;                      // S^T buffers: NSB x NM columns
+    // O^T accumulators: [piece parity][kv-head of the segment] x NM columns.
     // Each kv-head of a segment accumulates into its own: a P.V MMA of one
     // head's page also multiplies the zero P entries of the other heads'
     // columns, and 0 x NaN (a NaN stored in the page's V) must not reach them.
     static constexpr int HGMAX = SPLIT ? 4 : 2;          // kv-heads per segment
-    static constexpr int COL_O = NSB * NPAD;
-    static constexpr int NCOLS = NSB * NPAD + 2 * HGMAX * NPAD;
+    static constexpr int COL_O = NSB * NM;
+    static constexpr int NCOLS = NSB * NM + 2 * HGMAX * NM;
     static constexpr int TMEM_COLS = NCOLS <= 64 ? 64 : NCOLS <= 128 ? 128 : 256;
     static_assert(NCOLS <= 256, "TMEM budget");
     static_assert(OFF_BAR % 8 == 0 && OFF_SEQ % 16 == 0 && OFF_RED % 16 == 0, "shared memory alignment");
@@ -681,11 +685,11 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
 #pragma unroll
             for (int n = 0; n < RMAX; ++n) acc[n] = 0.f;
             for (int hh = 0; hh < HG; ++hh) {
-                float o[NPAD];
+                float o[K::NM];
 #pragma unroll
-                for (int c = 0; c < NPAD; c += 16) {
+                for (int c = 0; c < K::NM; c += 16) {
                     float tmp[16];
-                    tmem_ld16(tmem + lbase + K::COL_O + (par * K::HGMAX + hh) * NPAD + c, tmp);
+                    tmem_ld16(tmem + lbase + K::COL_O + (par * K::HGMAX + hh) * K::NM + c, tmp);
 #pragma unroll
                     for (int x = 0; x < 16; ++x) o[c + x] = tmp[x];
                 }
@@ -1082,7 +1086,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         // S^T of tile t once its K and its piece's q have landed and the
         // softmax has released S^T buffer t % NSB (P of tile t - NSB written).
         if (lane == 0) {
-            constexpr uint32_t idS = FP8 ? idesc_e4m3_f32(128, NPAD) : idesc_bf16_f32(128, NPAD, false, false);
+            constexpr uint32_t idS = FP8 ? idesc_e4m3_f32(128, K::NM) : idesc_bf16_f32(128, K::NM, false, false);
             constexpr int SBO = FP8 ? (D / 16) * 128 : K::NCH * 128;   // between 8-row core-matrix groups
             int t = 0, j = 0;
             bool ok = true;
@@ -1102,9 +1106,9 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         const uint64_t a = smem_desc(kbase + k * 256, 128, SBO);
                         const uint64_t b = smem_desc(qbase + k * 256, 128, SBO);
                         if constexpr (FP8)
-                            mma_f8(tmem + K::COL_S + (t % NSB) * NPAD, a, b, idS, k > 0);
+                            mma_f8(tmem + K::COL_S + (t % NSB) * K::NM, a, b, idS, k > 0);
                         else
-                            mma_bf16(tmem + K::COL_S + (t % NSB) * NPAD, a, b, idS, k > 0);
+                            mma_bf16(tmem + K::COL_S + (t % NSB) * K::NM, a, b, idS, k > 0);
                     }
                     mma_commit(bar(B::SFULL + t % NSB));
                     mma_commit(bar(B::KEMPTY + ks));
@@ -1124,11 +1128,11 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         // starts its accumulator afresh once the epilogue of the piece two
         // before has read it.
         if (lane == 0) {
-            constexpr uint32_t idPV = idesc_bf16_f32(128, NPAD, true, true);
+            constexpr uint32_t idPV = idesc_bf16_f32(128, K::NM, true, true);
             int t = 0, pc = 0;
             bool ok = true;
             while (ok && it.valid()) {
-                const uint32_t obase = tmem + K::COL_O + (pc & 1) * K::HGMAX * NPAD;
+                const uint32_t obase = tmem + K::COL_O + (pc & 1) * K::HGMAX * K::NM;
                 uint32_t started = 0;             // kv-heads whose accumulator this piece has started
                 if (EWG && pc >= 2 && !(ok = wait_bar(bar(B::OFREE + (pc & 1)), ((pc >> 1) - 1) & 1, ctl))) break;
                 for (int t0 = 0; t0 < it.npg; t0 += kTP, ++t) {
@@ -1142,7 +1146,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     // unit slot pg holds unit it.pg0 + t0 + pg of the segment: kv-head (hh0 + pg) % HG
                     const int hh0 = (it.pg0 + t0) - div_small(it.pg0 + t0, HG) * HG;
                     for (int hh = 0; hh < HG; ++hh) {
-                        const uint32_t ocol = obase + hh * NPAD;
+                        const uint32_t ocol = obase + hh * K::NM;
                         for (int pg = hh >= hh0 ? hh - hh0 : hh - hh0 + HG; pg < np; pg += HG) {
                             const uint32_t accum = (started >> hh) & 1u;
                             started |= 1u << hh;
@@ -1308,7 +1312,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 const int Q = it.cur.Q, R = G * Q, L = it.cur.L, lim0 = L - Q;
                 const int np = min(kTP, it.npg - jt * kTP);
                 const int vs = t % NSV;
-                const uint32_t obase = K::COL_O + (pc & 1) * K::HGMAX * NPAD;
+                const uint32_t obase = K::COL_O + (pc & 1) * K::HGMAX * K::NM;
                 // this thread's token: unit slot k of the tile -> (page, kv-head), position
                 const int k = tt >> 4;
                 const int qu = it.pg0 + jt * kTP + k;
@@ -1336,7 +1340,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
 #pragma unroll
                 for (int c = 0; c < RMAX; c += 16) {
                     float tmp[16];
-                    tmem_ld16(tmem + lane_base + K::COL_S + (t % NSB) * NPAD + c, tmp);
+                    tmem_ld16(tmem + lane_base + K::COL_S + (t % NSB) * K::NM + c, tmp);
 #pragma unroll
                     for (int x = 0; x < 16 && c + x < RMAX; ++x) {
                         if constexpr (FP8)
@@ -1398,12 +1402,15 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         tc_fence_after();
                         for (int h2 = 0; h2 < HG; ++h2) {
 #pragma unroll
-                            for (int c = 0; c < NPAD; c += 16) {
+                            for (int c = 0; c < K::NM; c += 16) {
                                 float o[16];
-                                tmem_ld16(tmem + lane_base + obase + h2 * NPAD + c, o);
+                                tmem_ld16(tmem + lane_base + obase + h2 * K::NM + c, o);
 #pragma unroll
-                                for (int x = 0; x < 16; ++x) o[x] *= alpha[SPLIT ? (c + x) / 2 : (c + x)];
-                                tmem_st16(tmem + lane_base + obase + h2 * NPAD + c, o);
+                                for (int x = 0; x < 16; ++x) {
+                                    const int n = SPLIT ? (c + x) / 2 : (c + x);
+                                    o[x] *= n < RMAX ? alpha[n] : 1.f;
+                                }
+                                tmem_st16(tmem + lane_base + obase + h2 * K::NM + c, o);
                             }
                         }
                     }
@@ -1491,9 +1498,14 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 }
                 float* lw = lred + (par * 4 + warp) * RMAX;
                 {
+                    // (a power-of-two width for the butterfly: RMAX = 24 is padded to 32)
+                    constexpr int RB = RMAX <= 8 ? 8 : RMAX <= 16 ? 16 : 32;
+                    float lb[RB];
+#pragma unroll
+                    for (int n = 0; n < RB; ++n) lb[n] = n < RMAX ? l_part[n] : 0.f;
                     int col = 0;
-                    Butterfly<RMAX, 16, false>::run(l_part, lane, col);   // (l_part is reset below)
-                    if ((lane & (32 / RMAX - 1)) == 0) lw[col] = l_part[0];
+                    Butterfly<RB, 16, false>::run(lb, lane, col);
+                    if ((lane & (32 / RB - 1)) == 0 && col < RMAX) lw[col] = lb[0];
                 }
 #pragma unroll
                 for (int n = 0; n < RMAX; ++n)
@@ -1602,7 +1614,9 @@ int tc_heads_per_segment(int num_kv_heads, int rows) {
 // bf16 cache, head_dim 64/128, R = G * max_q_len <= 32; FP8 cache, head_dim
 // 64/128, R <= 8.  Narrow segments (N = 16) run the epilogue in its own
 // warpgroup; wide ones (N = 32), whose softmax needs more registers than a
-// 384-thread block leaves, in the softmax warps.
+// 384-thread block leaves, in the softmax warps.  Wide head_dim 128 segments
+// of at most 24 columns (a 5-token verify window at G = 4: 20) take the
+// kernel whose softmax and epilogue handle 24 of the 32 MMA columns.
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st) {
     const bool split = tc_col_limit(p.rows) == 8;
     if (p.cascade != 0) {                      // (bf16 caches only: the host checks)
@@ -1616,7 +1630,8 @@ cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int
     if (head_dim == 128)
         return fp8     ? tc::launch_t<128, 16, true, 4, 4, true, true>(p, ncta, st)
                : split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
-                       : tc::launch_t<128, 32, false, 2, 2, false>(p, ncta, st);
+               : p.hg * p.rows <= 24 ? tc::launch_t<128, 24, false, 2, 2, false>(p, ncta, st)
+                                     : tc::launch_t<128, 32, false, 2, 2, false>(p, ncta, st);
     return fp8     ? tc::launch_t<64, 16, true, 6, 8, true, true>(p, ncta, st)
            : split ? tc::launch_t<64, 16, true, 4, 6, true>(p, ncta, st)
                    : tc::launch_t<64, 32, false, 4, 4, false>(p, ncta, st);

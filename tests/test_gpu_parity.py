@@ -79,6 +79,9 @@ SWEEP = [
     (64, 8, 4, [9, 200, 33, 517], [2, 1, 4, 1], "fp8"),             # G = 2, causal windows, R <= 8
     (64, 8, 8, [0, 33, 0, 517, 64], [0, 1, 0, 1, 1], "fp8"),        # G = 1: four kv-heads per segment
     (64, 32, 8, np.random.default_rng(904).integers(1, 1500, 96).tolist(), [1] * 96, "fp8"),
+    # wide segments of at most 24 columns (the 24-column softmax of the wide kernel)
+    (128, 16, 4, [30, 300, 77, 1000], [3, 1, 2, 3], "bf16"),      # G = 4, R = 12: two kv-heads per segment
+    (128, 16, 2, [50, 400, 9, 2000], [3, 2, 1, 3], "bf16"),       # G = 8, R = 24
     # verify windows (R = 20, wide segments: the weighted cut) over short and long sequences
     (128, 32, 8, [20, 700, 33, 17, 400, 90, 16, 1000], [5] * 8, "bf16"),
     # large batches: past the shared-memory sequence table (256 bf16 / 128 FP8
@@ -144,6 +147,7 @@ def test_fp8_subnormal_codes():
     (128, 4, 2, "bf16"),    # tensor-core narrow kernel, two kv-heads per segment
     (64, 1, 4, "bf16"),     # narrow kernel, four kv-heads per segment
     (128, 16, 2, "bf16"),   # wide kernel (N = 32), two kv-heads per segment
+    (128, 12, 2, "bf16"),   # wide kernel, 24 of its 32 columns (R = 12, two kv-heads per segment)
 ])
 def test_nan_in_cache_propagates(head_dim, group, num_kv_heads, dtype):
     """A NaN source value is stored as NaN (bf16 bits copied; an E4M3 NaN code
