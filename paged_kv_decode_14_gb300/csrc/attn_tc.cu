@@ -94,9 +94,9 @@ constexpr int kNarrowCharge = 16;
 template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8>
 struct Cfg {
     static constexpr int RMAX = SPLIT ? NPAD / 2 : NPAD;  // logical columns
-    // MMA N: NPAD rounded up to 16 (a wide kernel with NPAD = 24 computes 32 columns, and its
-    // softmax and epilogue touch only the first 24: P columns 24-31 are never written and only
-    // reach O columns that are never read)
+    // MMA N: NPAD rounded up to 16 (a wide kernel with NPAD = 20 or 24 computes 32 columns, and
+    // its softmax and epilogue touch only the first NPAD: P columns from the next multiple of 8
+    // on are never written and only reach O columns that are never read)
     static constexpr int NM = (NPAD + 15) / 16 * 16;
     static constexpr int PAGE = kBlock * D * 2;         // a page as bf16 MMA operand
     static constexpr int PAGE8 = kBlock * D;            // an FP8 cache page
@@ -799,10 +799,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         const int c = cb + j;
                         if (c == cta) {
 #pragma unroll
-                            for (int x = 0; x < 8; ++x) {
-                                m[j][x] = Mx[n0 + x];
-                                l[j][x] = Lsum[n0 + x];
-                                a[j][x] = acc[n0 + x];
+                            for (int x = 0; x < 8; ++x) {      // (RMAX may end inside a group of 8)
+                                m[j][x] = n0 + x < RMAX ? Mx[n0 + x] : -INFINITY;
+                                l[j][x] = n0 + x < RMAX ? Lsum[n0 + x] : 0.f;
+                                a[j][x] = n0 + x < RMAX ? acc[n0 + x] : 0.f;
                             }
                         } else {
                             const bool cok = c <= c_last;
@@ -1427,7 +1427,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 if (t >= NSB) wait_bar(bar(B::PEMPTY + t % NSB), ((t / NSB) - 1) & 1, ctl);
                 uint8_t* pdst = smem + K::OFF_P + (t % NSB) * K::PBUF + tt * 16;
 #pragma unroll
-                for (int cc = 0; cc < NPAD / 8; ++cc) {
+                for (int cc = 0; cc < (NPAD + 7) / 8; ++cc) {      // (a last group past RMAX is 0)
                     uint32_t w4[4], l4[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
@@ -1440,8 +1440,9 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                             b = pv - hi;
                         } else {
                             // wide: column n's high part here, its low part in the second ring
-                            a = FP8 ? pr[cc * 8 + 2 * h] * vscale : pr[cc * 8 + 2 * h];
-                            b = FP8 ? pr[cc * 8 + 2 * h + 1] * vscale : pr[cc * 8 + 2 * h + 1];
+                            const int n0 = cc * 8 + 2 * h;
+                            a = n0 < RMAX ? (FP8 ? pr[n0] * vscale : pr[n0]) : 0.f;
+                            b = n0 + 1 < RMAX ? (FP8 ? pr[n0 + 1] * vscale : pr[n0 + 1]) : 0.f;
                             const float ah = __bfloat162float(__float2bfloat16_rn(a));
                             const float bh = __bfloat162float(__float2bfloat16_rn(b));
                             l4[h] = pack_bf16x2(a - ah, b - bh);
@@ -1615,8 +1616,8 @@ int tc_heads_per_segment(int num_kv_heads, int rows) {
 // 64/128, R <= 8.  Narrow segments (N = 16) run the epilogue in its own
 // warpgroup; wide ones (N = 32), whose softmax needs more registers than a
 // 384-thread block leaves, in the softmax warps.  Wide head_dim 128 segments
-// of at most 24 columns (a 5-token verify window at G = 4: 20) take the
-// kernel whose softmax and epilogue handle 24 of the 32 MMA columns.
+// of at most 20 or 24 columns (a 5-token verify window at G = 4: 20) take a
+// kernel whose softmax and epilogue handle only those of the 32 MMA columns.
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st) {
     const bool split = tc_col_limit(p.rows) == 8;
     if (p.cascade != 0) {                      // (bf16 caches only: the host checks)
@@ -1630,6 +1631,7 @@ cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int
     if (head_dim == 128)
         return fp8     ? tc::launch_t<128, 16, true, 4, 4, true, true>(p, ncta, st)
                : split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
+               : p.hg * p.rows <= 20 ? tc::launch_t<128, 20, false, 2, 2, false>(p, ncta, st)
                : p.hg * p.rows <= 24 ? tc::launch_t<128, 24, false, 2, 2, false>(p, ncta, st)
                                      : tc::launch_t<128, 32, false, 2, 2, false>(p, ncta, st);
     return fp8     ? tc::launch_t<64, 16, true, 6, 8, true, true>(p, ncta, st)

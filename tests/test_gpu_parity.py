@@ -82,6 +82,7 @@ SWEEP = [
     # wide segments of at most 24 columns (the 24-column softmax of the wide kernel)
     (128, 16, 4, [30, 300, 77, 1000], [3, 1, 2, 3], "bf16"),      # G = 4, R = 12: two kv-heads per segment
     (128, 16, 2, [50, 400, 9, 2000], [3, 2, 1, 3], "bf16"),       # G = 8, R = 24
+    (128, 10, 2, [7, 333, 64, 1500], [2, 1, 2, 2], "bf16"),       # G = 5, R = 10: 20 columns, two kv-heads
     # verify windows (R = 20, wide segments: the weighted cut) over short and long sequences
     (128, 32, 8, [20, 700, 33, 17, 400, 90, 16, 1000], [5] * 8, "bf16"),
     # large batches: past the shared-memory sequence table (256 bf16 / 128 FP8
