@@ -90,6 +90,9 @@ constexpr float kRescaleSlack = 8.f;
 // Units charged per segment in the weighted CTA cut of narrow FP8 segments
 // (wide: 24); measured best of 4-40 on the long FP8 batch
 constexpr int kNarrowCharge = 16;
+// ... and of wide segments whose epilogue runs in the epilogue warpgroup (with it in the
+// softmax warps: 24)
+constexpr int kWideEwgCharge = 12;
 
 template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8>
 struct Cfg {
@@ -135,7 +138,7 @@ struct Cfg {
     // the weighted CTA boundaries (int [TABMAX + 1])
     static constexpr int TABMAX = 160;
     static constexpr int OFF_BND = (OFF_GATHER + GATHER + 15) / 16 * 16;
-    static constexpr bool PTAB = (FP8 || !EWG) && OFF_BND + (TABMAX + 1) * 4 + 128 <= kMaxSmem - 512;
+    static constexpr bool PTAB = (FP8 || !SPLIT) && OFF_BND + (TABMAX + 1) * 4 + 128 <= kMaxSmem - 512;
     static constexpr int SMEM_USED = (PTAB ? OFF_BND + (TABMAX + 1) * 4 : OFF_GATHER + GATHER) + 128;  // + slack
     // One CTA per SM either way: take the whole per-block budget, so every
     // operand read the descriptors can form stays inside the allocation.
@@ -559,7 +562,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     int* bndtab = K::PTAB ? reinterpret_cast<int*>(smem + K::OFF_BND) : nullptr;
     bool tab_used = false;
     const bool has_work = plan_locate<kThreads, CASC>(p, blockIdx.x, gridDim.x, scratch, &cur0, &u0, &u1, &W, &P, &curt,
-                                                seqtab, bndtab, K::TABMAX, EWG ? kNarrowCharge : 24, &tab_used,
+                                                seqtab, bndtab, K::TABMAX, SPLIT ? kNarrowCharge : EWG ? kWideEwgCharge : 24, &tab_used,
                                                 reinterpret_cast<int4*>(smem + K::OFF_P),   // (P ring unused yet)
                                                 CASC ? nullptr : &lq);
     const Part part{W, P, tab_used ? bndtab : nullptr};
@@ -1617,7 +1620,9 @@ int tc_heads_per_segment(int num_kv_heads, int rows) {
 // warpgroup; wide ones (N = 32), whose softmax needs more registers than a
 // 384-thread block leaves, in the softmax warps.  Wide head_dim 128 segments
 // of at most 20 or 24 columns (a 5-token verify window at G = 4: 20) take a
-// kernel whose softmax and epilogue handle only those of the 32 MMA columns.
+// kernel whose softmax and epilogue handle only those of the 32 MMA columns;
+// the 20-column softmax fits a 384-thread block, so that one has the epilogue
+// warpgroup too.
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st) {
     const bool split = tc_col_limit(p.rows) == 8;
     if (p.cascade != 0) {                      // (bf16 caches only: the host checks)
@@ -1631,7 +1636,7 @@ cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int
     if (head_dim == 128)
         return fp8     ? tc::launch_t<128, 16, true, 4, 4, true, true>(p, ncta, st)
                : split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
-               : p.hg * p.rows <= 20 ? tc::launch_t<128, 20, false, 2, 2, false>(p, ncta, st)
+               : p.hg * p.rows <= 20 ? tc::launch_t<128, 20, false, 2, 2, true>(p, ncta, st)
                : p.hg * p.rows <= 24 ? tc::launch_t<128, 24, false, 2, 2, false>(p, ncta, st)
                                      : tc::launch_t<128, 32, false, 2, 2, false>(p, ncta, st);
     return fp8     ? tc::launch_t<64, 16, true, 6, 8, true, true>(p, ncta, st)
