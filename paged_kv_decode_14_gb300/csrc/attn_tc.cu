@@ -127,10 +127,11 @@ struct Cfg {
     static constexpr int OFF_EM = OFF_LRED + 2 * 4 * RMAX * 4;         // float [2][RMAX]
     static constexpr int OFF_PD = OFF_EM + 2 * RMAX * 4;               // int [2][8]: piece descriptors
     static constexpr int OFF_BAR = OFF_PD + 2 * 8 * 4;
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 16 + (FP8 ? NSV + NSC : 0);   // the barriers of Bars
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 3 * NSB + 18 + (FP8 ? NSV + NSC : 0);   // the barriers of Bars
     static constexpr int OFF_MISC = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;  // tmem addr, abort, zero, gather state
     static constexpr int OFF_MQ = OFF_MISC + 16;         // merge tasks: int [4][8]
-    static constexpr int OFF_SEQ = OFF_MQ + 128;         // int4 [SEQTAB]: per-sequence (L, Q, Ub, qoff)
+    static constexpr int OFF_VOTE = OFF_MQ + 128;        // int [2][4]: the softmax warps' votes (tile parity)
+    static constexpr int OFF_SEQ = OFF_VOTE + 32;        // int4 [SEQTAB]: per-sequence (L, Q, Ub, qoff)
     // pre-merged earlier pieces of the CTA's last segment: M[RMAX], den[RMAX], num[RMAX][D]
     static constexpr int SEQTAB = FP8 ? kSeqTab / 2 : kSeqTab;   // sequences the table holds
     static constexpr int OFF_GATHER = OFF_SEQ + SEQTAB * 16;
@@ -165,9 +166,10 @@ struct Bars {
                          ODONE = MQFULL + 4,      // [2]: last P.V of a piece of that parity done
                          PREADY = ODONE + 2,      // [2]: a piece of that parity handed to the epilogue
                          OFREE = PREADY + 2,      // [2]: its epilogue has read O^T, lred and emref
+                         VOTE = OFREE + 2,        // [2]: the softmax warps' reference votes of a tile (parity)
                          // FP8 only: a V slot's e4m3 pages have landed (before their widening), scale ring
-                         VLAND = OFREE + 2, SCALE = VLAND + NSV,
-                         END = FP8 ? SCALE + 16 : OFREE + 2;
+                         VLAND = VOTE + 2, SCALE = VLAND + NSV,
+                         END = FP8 ? SCALE + 16 : VOTE + 2;
 };
 
 // A finished piece, as its epilogue needs it.
@@ -530,6 +532,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             mbar_init(bar(B::ODONE + i), 1);
             mbar_init(bar(B::PREADY + i), kSoftThreads);
             mbar_init(bar(B::OFREE + i), kSoftThreads);
+            mbar_init(bar(B::VOTE + i), 4);                 // lane 0 of each softmax warp
         }
         mbar_init(bar(B::DONE), 1);
         mbar_init(bar(B::DONE + 1), 1);
@@ -1362,7 +1365,30 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         s[n] = vis ? s[n] * p.scale_log2 : -INFINITY;
                     need |= s[n] > m_ref[n] + kRescaleSlack;
                 }
-                if (bar_red_or(kBarSoft, kSoftThreads, need || !okw)) {
+                // The FP8 kernel votes without blocking: each warp posts its vote and arrives on
+                // the tile's vote barrier, P is computed against the current reference meanwhile,
+                // and only then is the vote read (a raise recomputes P).  A vote barrier that
+                // timed out counts as a raise, whose first barrier then winds all warps down.
+                // (The bf16 kernels measured no faster this way: they keep the blocking vote.)
+                constexpr bool kSpec = SPLIT && FP8;
+                float pr[RMAX];
+                bool raise;
+                if constexpr (kSpec) {
+                    int* vote = reinterpret_cast<int*>(smem + K::OFF_VOTE) + (t & 1) * 4;
+                    const bool wneed = __any_sync(0xffffffffu, need || !okw);
+                    if (lane == 0) {
+                        vote[warp] = wneed ? 1 : 0;
+                        mbar_arrive(bar(B::VOTE + (t & 1)));
+                    }
+#pragma unroll
+                    for (int n = 0; n < RMAX; ++n) pr[n] = (s[n] == -INFINITY) ? 0.f : fast_exp2(s[n] - m_ref[n]);
+                    const bool okv = wait_bar(bar(B::VOTE + (t & 1)), (t >> 1) & 1, ctl);
+                    const volatile int* vq = vote;
+                    raise = !okv || (vq[0] | vq[1] | vq[2] | vq[3]) != 0;
+                } else {
+                    raise = bar_red_or(kBarSoft, kSoftThreads, need || !okw);
+                }
+                if (raise) {
                     // raise the reference to this tile's max (first tile of a piece, or a big jump):
                     // per (unit slot, column) maxima over the slot's 16 tokens, then per column
                     if constexpr (RMAX <= 16) {
@@ -1420,12 +1446,12 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     // keep red[] stable until every thread has read it
                     named_bar_sync(kBarSoft, kSoftThreads);
                 }
-                float pr[RMAX];
+                if (!kSpec || raise) {
 #pragma unroll
-                for (int n = 0; n < RMAX; ++n) {
-                    pr[n] = (s[n] == -INFINITY) ? 0.f : fast_exp2(s[n] - m_ref[n]);
-                    l_part[n] += pr[n];
+                    for (int n = 0; n < RMAX; ++n) pr[n] = (s[n] == -INFINITY) ? 0.f : fast_exp2(s[n] - m_ref[n]);
                 }
+#pragma unroll
+                for (int n = 0; n < RMAX; ++n) l_part[n] += pr[n];
                 // P buffer t % NSB is free once the P.V of tile t - NSB has completed
                 if (t >= NSB) wait_bar(bar(B::PEMPTY + t % NSB), ((t / NSB) - 1) & 1, ctl);
                 uint8_t* pdst = smem + K::OFF_P + (t % NSB) * K::PBUF + tt * 16;
