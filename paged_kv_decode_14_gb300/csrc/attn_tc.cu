@@ -1151,17 +1151,32 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     const uint32_t pbase = sb + K::OFF_P + (t % NSB) * K::PBUF;
                     // unit slot pg holds unit it.pg0 + t0 + pg of the segment: kv-head (hh0 + pg) % HG
                     const int hh0 = (it.pg0 + t0) - div_small(it.pg0 + t0, HG) * HG;
-                    for (int hh = 0; hh < HG; ++hh) {
-                        const uint32_t ocol = obase + hh * K::NM;
-                        for (int pg = hh >= hh0 ? hh - hh0 : hh - hh0 + HG; pg < np; pg += HG) {
+                    if constexpr (D == 64 && SPLIT && !FP8) {
+                        // head_dim 64, bf16: slot order, so consecutive MMAs go to different heads'
+                        // accumulators (one head's MMAs accumulate into the same columns one after
+                        // another); this kernel's tiles are the shortest, and its P.V issuer had
+                        // fallen ~2 tiles behind the softmax.  (The other kernels measured slower so.)
+                        int hh = hh0;
+                        for (int pg = 0; pg < np; ++pg) {
                             const uint32_t accum = (started >> hh) & 1u;
                             started |= 1u << hh;
-                            const uint64_t a = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
-                            const uint64_t b = smem_desc(pbase + pg * 256, 128, 16 * 128);
-                            mma_bf16(ocol, a, b, idPV, accum);
-                            if constexpr (!SPLIT) {      // (wide: P's low parts, same accumulator)
-                                const uint64_t bl = smem_desc(pbase + (K::OFF_PLO - K::OFF_P) + pg * 256, 128, 16 * 128);
-                                mma_bf16(ocol, a, bl, idPV, 1u);
+                            mma_bf16(obase + hh * K::NM, smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128),
+                                     smem_desc(pbase + pg * 256, 128, 16 * 128), idPV, accum);
+                            if (++hh == HG) hh = 0;
+                        }
+                    } else {
+                        for (int hh = 0; hh < HG; ++hh) {
+                            const uint32_t ocol = obase + hh * K::NM;
+                            for (int pg = hh >= hh0 ? hh - hh0 : hh - hh0 + HG; pg < np; pg += HG) {
+                                const uint32_t accum = (started >> hh) & 1u;
+                                started |= 1u << hh;
+                                const uint64_t a = smem_desc(vbase + pg * K::PAGE, K::NCH * 128, 128);
+                                const uint64_t b = smem_desc(pbase + pg * 256, 128, 16 * 128);
+                                mma_bf16(ocol, a, b, idPV, accum);
+                                if constexpr (!SPLIT) {      // (wide: P's low parts, same accumulator)
+                                    const uint64_t bl = smem_desc(pbase + (K::OFF_PLO - K::OFF_P) + pg * 256, 128, 16 * 128);
+                                    mma_bf16(ocol, a, bl, idPV, 1u);
+                                }
                             }
                         }
                     }
