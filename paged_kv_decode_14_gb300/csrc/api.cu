@@ -1,5 +1,6 @@
 // C ABI of libpagedkv: argument checks, grid planning and kernel dispatch.
 // Declarations and contracts: include/pagedkv.h.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -23,8 +24,10 @@ int tc_heads_per_segment(int num_kv_heads, int rows);
 // Kernel choice and grid for one attention call, in virtual kv-heads (vheads
 // of group vgroup; kv_split of them per cache kv-head): the tensor-core
 // kernel for bf16 caches (R = vgroup * max_q_len <= 32 always) and for FP8
-// caches with R <= 8 (one persistent CTA per SM, all of its ~227 KiB of
-// shared memory), else the CUDA-core kernel (4 CTAs per SM).
+// caches with R <= 8 (always so for windows of up to 8 tokens: the split
+// makes it), one persistent CTA per SM with all of its ~227 KiB of shared
+// memory; else (FP8, windows of 9-16 tokens) the CUDA-core kernel (4 CTAs
+// per SM).
 // rows_pad: partial-slot rows (the tensor-core kernel keeps up to 32 columns
 // of several kv-heads per segment).  Virtual kv-heads that share cache pages
 // are never grouped in one segment (its pages are copied as one run).
@@ -115,7 +118,7 @@ pkv_status attention_setup(const pkv_cache* cache, const void* q, int num_q_head
     if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
     if (max_q_len > max_q_limit) return PKV_ERR_UNSUPPORTED;
     const int group = num_q_heads / cache->num_kv_heads;
-    const int ks = kv_split_for(group, max_q_len);
+    const int ks = kv_split_for(group, max_q_len, kv_split_limit(cache->kv_dtype == PKV_KV_FP8_E4M3, max_q_len));
     const int vgroup = group / ks, vheads = cache->num_kv_heads * ks;
     if ((int64_t)max_blocks_per_seq * vheads >= (1 << 20)) return PKV_ERR_UNSUPPORTED;   // unit indices stay below 2^20
     if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
@@ -241,9 +244,15 @@ PKV_API size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_q_head
     if (head_dim <= 0 || max_q_len < 1) return 0;
     if (num_ctas <= 0) num_ctas = default_ctas(num_sms_current());
     if (num_ctas <= 0) return 0;
-    const int group = num_q_heads / num_kv_heads, ks = kv_split_for(group, max_q_len);
-    const int rows_pad = max(32, simt_rows_pad((group / ks) * max_q_len));
-    return workspace_layout(num_seqs, num_kv_heads * ks, head_dim, rows_pad, num_ctas).total;
+    // (the cache's dtype is not an argument: the larger of the bf16 and FP8 plans)
+    const int group = num_q_heads / num_kv_heads;
+    size_t need = 0;
+    for (int fp8 = 0; fp8 < 2; ++fp8) {
+        const int ks = kv_split_for(group, max_q_len, kv_split_limit(fp8 != 0, max_q_len));
+        const int rows_pad = max(32, simt_rows_pad((group / ks) * max_q_len));
+        need = std::max(need, workspace_layout(num_seqs, num_kv_heads * ks, head_dim, rows_pad, num_ctas).total);
+    }
+    return need;
 }
 
 PKV_API pkv_status pkv_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {

@@ -63,10 +63,11 @@ SWEEP = [
     (128, 8, 2, [5, 40, 77, 300], [5, 3, 8, 2], "bf16"),
     (128, 16, 2, [5, 40, 77, 300], [5, 3, 8, 2], "bf16"),  # G = 8, R up to 64: two virtual kv-heads per kv-head
     (64, 32, 2, [9, 130, 33], [4, 2, 3], "bf16"),          # G = 16, R up to 64
-    (128, 32, 4, [20, 300], [5, 2], "fp8"),                # FP8, G = 8, R = 40 (CUDA-core kernel)
+    (128, 32, 4, [20, 300], [5, 2], "fp8"),                # FP8, G = 8, Q = 5: eight virtual groups (tensor cores)
     (64, 4, 4, [9, 10, 11], [8, 4, 2], "bf16"),
     (128, 32, 8, [600, 3, 1200], [1, 1, 1], "fp8"),
-    (64, 8, 1, [33, 17, 129], [4, 1, 2], "fp8"),
+    (64, 8, 1, [33, 17, 129], [4, 1, 2], "fp8"),           # FP8, G = 8, Q = 4: virtual groups of 2 heads
+    (128, 8, 2, [50, 300, 700, 16], [9, 12, 16, 1], "fp8"),  # FP8 windows of 9-16 tokens: the CUDA-core kernel
     (128, 16, 1, [40, 250], [2, 2], "bf16"),          # G = 16, R = 32
     (128, 8, 2, [0, 20, 0, 45], [0, 1, 0, 2], "bf16"),  # empty sequences
     (64, 16, 2, [20, 50], [0, 3], "bf16"),             # a sequence with no query rows
@@ -107,6 +108,21 @@ def test_sweep(case):
         assert_attention_close(got, ref, f"sweep {case} ncta {ncta}")
 
 
+def test_fp8_verify_q5_full_size():
+    """FP8 cache, 5-token verify windows on the verify batch's shape (32
+    sequences, lengths U[512, 4096], G = 4): R = 20 rows per kv-head run as
+    four virtual groups of 5 on the FP8 tensor-core kernel."""
+    rng = np.random.Generator(np.random.PCG64(1005))
+    L = rng.integers(512, 4097, size=32).astype(np.int32)
+    w = wl.make_workload("verify_fp8", context_lens=L, q_lens=np.full(32, 5, np.int32), num_q_heads=32,
+                         num_kv_heads=8, head_dim=128, kv_dtype="fp8", seed=105, outlier_p=0.01)
+    kc, vc = oracle.build_cache(w)
+    ref, _ = oracle.attend(w, kc, vc)
+    dw, got = run_gpu(w)
+    assert_attention_close(got, ref, "FP8 verify Q=5")
+    assert dw.errors() == (0, 0)
+
+
 def test_verify_g8_q5_full_size():
     """A 64 / 8-head model verifying 5 draft tokens on the verify batch's shape
     (32 sequences, lengths U[512, 4096]): R = G * Q = 40 rows per kv-head, so
@@ -143,8 +159,8 @@ def test_fp8_subnormal_codes():
 @pytest.mark.parametrize("head_dim,group,num_kv_heads,dtype", [
     (128, 4, 2, "fp8"),     # tensor-core FP8 kernel, two kv-heads per segment
     (64, 4, 2, "fp8"),      # tensor-core FP8 kernel, head_dim 64
-    (64, 16, 2, "fp8"),     # CUDA-core FP8 kernel, head_dim 64 (G * Q > 8)
-    (128, 16, 2, "fp8"),    # CUDA-core FP8 kernel (G * Q > 8)
+    (64, 16, 2, "fp8"),     # FP8, head_dim 64, G = 16: two virtual groups
+    (128, 16, 2, "fp8"),    # FP8, G = 16: two virtual groups of 8 on the tensor cores
     (128, 4, 2, "bf16"),    # tensor-core narrow kernel, two kv-heads per segment
     (64, 1, 4, "bf16"),     # narrow kernel, four kv-heads per segment
     (128, 16, 2, "bf16"),   # wide kernel (N = 32), two kv-heads per segment

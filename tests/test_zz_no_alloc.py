@@ -41,8 +41,8 @@ def _case(which):
     if which == "fp8_tc64":      # FP8, head_dim 64, G * Q = 8: the tensor-core kernel
         return wl.make_workload("f8t", context_lens=[900, 33, 1700, 5], q_lens=[1, 2, 1, 1], num_q_heads=32,
                                 num_kv_heads=8, head_dim=64, kv_dtype="fp8", seed=94, outlier_p=0.01)
-    # FP8, head_dim 64, G * Q = 12: the CUDA-core kernel (its own rows_pad and grid of 4 CTAs per SM)
-    return wl.make_workload("f8s", context_lens=[900, 33, 1700, 5], q_lens=[1, 3, 1, 1], num_q_heads=32,
+    # FP8, head_dim 64, a 9-token window: the CUDA-core kernel (its own rows_pad and grid of 4 CTAs per SM)
+    return wl.make_workload("f8s", context_lens=[900, 33, 1700, 9], q_lens=[1, 9, 1, 1], num_q_heads=32,
                             num_kv_heads=8, head_dim=64, kv_dtype="fp8", seed=93, outlier_p=0.01)
 
 
