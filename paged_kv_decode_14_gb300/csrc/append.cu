@@ -10,8 +10,12 @@
 
 namespace pkv {
 
+// At most 32 registers a thread, so that a 32-thread CTA fits beside a resident
+// attention CTA (384 threads x 168 registers leave 1024 of an SM's 65536): a
+// decode step's append is then already waiting on the SMs when the attention
+// before it ends.
 template <int E>
-__global__ void __launch_bounds__(256) append_kernel(const uint8_t* __restrict__ k_new, const uint8_t* __restrict__ v_new,
+__global__ void __maxnreg__(32) append_kernel(const uint8_t* __restrict__ k_new, const uint8_t* __restrict__ v_new,
                                                      const int64_t* __restrict__ slots, int64_t num_tokens, int Hkv,
                                                      int D, int64_t num_blocks, uint8_t* k_cache, uint8_t* v_cache,
                                                      const float* __restrict__ k_scales,
@@ -111,9 +115,13 @@ cudaError_t launch_append(const pkv_cache& c, const void* k_new, const void* v_n
                           int64_t num_tokens, int* err, cudaStream_t st, int num_sms) {
     const int E = c.kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2;
     const int64_t total = num_tokens * c.num_kv_heads * (c.head_dim * E / 16) * 2;
-    const int threads = 256;
+    // a decode step's few bf16 tokens: 32-thread CTAs, one chunk a thread (one of them fits
+    // beside each resident attention CTA); FP8 (whose encode divides every value) and larger
+    // appends (a prefill's prompt): 256-thread CTAs, up to 8 per SM
+    const bool small = E == 2 && total <= (int64_t)num_sms * 32 * 2;
+    const int threads = small ? 32 : 256;
     int64_t blocks = (total + threads - 1) / threads;
-    const int64_t cap = (int64_t)num_sms * 8;
+    const int64_t cap = (int64_t)num_sms * (small ? 2 : 8);
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     // A programmatic dependent launch: the kernel may be scheduled while the
