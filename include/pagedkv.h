@@ -165,8 +165,8 @@ PKV_API pkv_status pkv_paged_kv_append_rope(const pkv_cache* cache, const void* 
  * left merge tickets set: zero the workspace again before reusing it.
  * num_ctas = 0 means the library's default grid for the current device.
  * The size does not depend on the cache's dtype: it covers the larger of
- * the bf16 and FP8 plans (an FP8 cache with windows of up to 8 tokens splits
- * each kv-head's query heads into groups of at most 8 rows, one ticket each).
+ * the bf16 and FP8 plans (an FP8 cache splits each kv-head's query heads
+ * into groups of at most 16 or 8 rows, one ticket each).
  */
 PKV_API size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                             int32_t num_kv_heads, int32_t head_dim,
@@ -196,9 +196,10 @@ PKV_API pkv_status pkv_workspace_init(void* workspace, size_t workspace_bytes, v
  *   context_lens,  device int32 [num_seqs]; 0 <= q_lens[b] <= context_lens[b].
  *   q_lens
  *   max_q_len      host-known upper bound of q_lens (1..16), picks the kernel
- *                  (FP8 caches: up to 8 runs on the tensor cores, the GQA group
- *                  split into virtual groups of at most 8 query rows; 9..16 on
- *                  the CUDA cores).
+ *                  (FP8 caches run on the tensor cores with the GQA group split
+ *                  into virtual groups of at most 16 query rows at head_dim
+ *                  128, of 8 at head_dim 64 up to 8 tokens; head_dim 64 with
+ *                  9..16 tokens on the CUDA cores).
  *   scale          softmax scale (e.g. 1/sqrt(head_dim)).
  *   num_ctas       grid size (0 = default); it sets how the batch's KV is
  *                  split, so results of different grids differ by rounding only.

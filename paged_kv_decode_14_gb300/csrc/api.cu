@@ -19,15 +19,15 @@ cudaError_t launch_attention_simt(const AttnParams& p, int head_dim, int elem_by
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int ncta, cudaStream_t st);
 cudaError_t launch_prefill(const AttnParams& p, int head_dim, int num_sms, cudaStream_t st);
 int simt_rows_pad(int rows);
-int tc_heads_per_segment(int num_kv_heads, int rows);
+int tc_heads_per_segment(int num_kv_heads, int rows, bool fp8);
 
 // Kernel choice and grid for one attention call, in virtual kv-heads (vheads
 // of group vgroup; kv_split of them per cache kv-head): the tensor-core
 // kernel for bf16 caches (R = vgroup * max_q_len <= 32 always) and for FP8
-// caches with R <= 8 (always so for windows of up to 8 tokens: the split
-// makes it), one persistent CTA per SM with all of its ~227 KiB of shared
-// memory; else (FP8, windows of 9-16 tokens) the CUDA-core kernel (4 CTAs
-// per SM).
+// caches with R <= 8, or R <= 16 at head_dim 128 (the split makes it so for
+// every window at head_dim 128 and for windows of up to 8 tokens at 64), one
+// persistent CTA per SM with all of its ~227 KiB of shared memory; else (FP8,
+// head_dim 64, windows of 9-16 tokens) the CUDA-core kernel (4 CTAs per SM).
 // rows_pad: partial-slot rows (the tensor-core kernel keeps up to 32 columns
 // of several kv-heads per segment).  Virtual kv-heads that share cache pages
 // are never grouped in one segment (its pages are copied as one run).
@@ -35,10 +35,11 @@ AttnLaunch plan_attention(const pkv_cache* c, int vgroup, int vheads, int kv_spl
                           int num_sms) {
     AttnLaunch L;
     const int rows = vgroup * max_q_len;
-    L.tc = c->kv_dtype == PKV_KV_BF16 ? rows <= 32 : rows <= 8;
+    const bool fp8 = c->kv_dtype == PKV_KV_FP8_E4M3;
+    L.tc = !fp8 ? rows <= 32 : (rows <= 8 || (c->head_dim == 128 && rows <= 16));
     L.ncta = num_ctas > 0 ? num_ctas : (L.tc ? num_sms : 4 * num_sms);
     L.rows_pad = L.tc ? 32 : simt_rows_pad(rows);
-    L.hg = (L.tc && kv_split == 1) ? tc_heads_per_segment(vheads, rows) : 1;
+    L.hg = (L.tc && kv_split == 1) ? tc_heads_per_segment(vheads, rows, fp8) : 1;
     return L;
 }
 
@@ -118,7 +119,8 @@ pkv_status attention_setup(const pkv_cache* cache, const void* q, int num_q_head
     if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
     if (max_q_len > max_q_limit) return PKV_ERR_UNSUPPORTED;
     const int group = num_q_heads / cache->num_kv_heads;
-    const int ks = kv_split_for(group, max_q_len, kv_split_limit(cache->kv_dtype == PKV_KV_FP8_E4M3, max_q_len));
+    const int ks = kv_split_for(group, max_q_len,
+                                kv_split_limit(cache->kv_dtype == PKV_KV_FP8_E4M3, cache->head_dim, max_q_len));
     const int vgroup = group / ks, vheads = cache->num_kv_heads * ks;
     if ((int64_t)max_blocks_per_seq * vheads >= (1 << 20)) return PKV_ERR_UNSUPPORTED;   // unit indices stay below 2^20
     if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
@@ -248,7 +250,7 @@ PKV_API size_t pkv_attention_workspace_size(int32_t num_seqs, int32_t num_q_head
     const int group = num_q_heads / num_kv_heads;
     size_t need = 0;
     for (int fp8 = 0; fp8 < 2; ++fp8) {
-        const int ks = kv_split_for(group, max_q_len, kv_split_limit(fp8 != 0, max_q_len));
+        const int ks = kv_split_for(group, max_q_len, kv_split_limit(fp8 != 0, head_dim, max_q_len));
         const int rows_pad = max(32, simt_rows_pad((group / ks) * max_q_len));
         need = std::max(need, workspace_layout(num_seqs, num_kv_heads * ks, head_dim, rows_pad, num_ctas).total);
     }

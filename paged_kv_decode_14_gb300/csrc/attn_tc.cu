@@ -96,7 +96,9 @@ constexpr int kWideEwgCharge = 12;
 
 template <int D, int NPAD, bool SPLIT, int NSK, int NSV, bool EWG, bool FP8>
 struct Cfg {
-    static constexpr int RMAX = SPLIT ? NPAD / 2 : NPAD;  // logical columns
+    // logical columns: SPLIT, P's high and low parts on adjacent columns; FP8, S^T holds each q row
+    // as two e4m3 terms on columns n and RMAX + n
+    static constexpr int RMAX = (SPLIT || FP8) ? NPAD / 2 : NPAD;
     // MMA N: NPAD rounded up to 16 (a wide kernel with NPAD = 20 or 24 computes 32 columns, and
     // its softmax and epilogue touch only the first NPAD: P columns from the next multiple of 8
     // on are never written and only reach O columns that are never read)
@@ -113,7 +115,7 @@ struct Cfg {
     static constexpr int OFF_K = 0;                     // + st * KSLOT
     static constexpr int OFF_V = NSK * KSLOT;           // + st * (TILE + VSLACK)
     static constexpr int OFF_LAND = TILE - kTP * PAGE8;
-    // FP8 scale ring: float [NSC][32]: k scales [8], v scales [8], column factors [8]
+    // FP8 scale ring: float [NSC][32]: k scales [8], v scales [8], column factors [RMAX <= 16]
     static constexpr int OFF_SC = OFF_V + NSV * (TILE + VSLACK);
     static constexpr int OFF_Q = OFF_SC + (FP8 ? NSC * 32 * 4 : 0);
     static constexpr int QBUF = NM * D * 2;
@@ -857,7 +859,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         constexpr bool kQAhead = QV <= 4;         // wide pieces load their q at the piece start
         int t = 0, j = 0, kcount = 0, vcount = 0;
         bool ok = true;
-        float cur_c = 1.f;                // (FP8) lane n < 8: column n's factor 2^-E_n in the current piece
+        float cur_c = 1.f;                // (FP8) lane n < RMAX: column n's factor 2^-E_n in the current piece
         // q rows of piece `pi` in column order, 16 bytes per lane and step
         auto load_q = [&](const PieceIter<CASC>& pi, uint4 (&v)[QV]) {
             const int R = G * pi.cur.Q, ncol = HG * R;
@@ -976,7 +978,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         // brought to [128, 256)), split exactly into hi + lo e4m3 terms (a
                         // bf16 value's 8 significant bits), stored as rows n and 8 + n; the
                         // softmax adds the two columns and multiplies by 2^-E_n
-                        static_assert(!FP8 || ((K::NCH == 16 || K::NCH == 8) && RMAX == 8), "FP8 q staging: R <= 8");
+                        static_assert(!FP8 || ((K::NCH == 16 || K::NCH == 8) && (RMAX == 8 || RMAX == 16)),
+                                      "FP8 q staging: R <= 16");
                         int ek[QV];
 #pragma unroll
                         for (int k = 0; k < QV; ++k) {
@@ -1007,9 +1010,10 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                                     lo[h >> 1] |= (c2 & 0xFFFFu) << ((h & 1) * 16);
                                 }
                                 const int n = idx / K::NCH, c = idx % K::NCH;    // row, 8-element chunk
-                                uint8_t* rh = qdst + (c >> 1) * 128 + n * 16 + (c & 1) * 8;
+                                // (8-row core-matrix groups (D / 16) * 128 bytes apart: rows n, then RMAX + n)
+                                uint8_t* rh = qdst + (n >> 3) * ((D / 16) * 128) + (c >> 1) * 128 + (n & 7) * 16 + (c & 1) * 8;
                                 *reinterpret_cast<uint2*>(rh) = make_uint2(hi[0], hi[1]);
-                                *reinterpret_cast<uint2*>(rh + (D / 16) * 128) = make_uint2(lo[0], lo[1]);
+                                *reinterpret_cast<uint2*>(rh + (RMAX / 8) * ((D / 16) * 128)) = make_uint2(lo[0], lo[1]);
                             }
                         }
                         // column n's factor -> lane n: a step holds RPS rows, row n in lanes
@@ -1048,7 +1052,7 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         cp_async_4(scs + 32 + lane * 4, p.v_scales + unit);
                     }
                     cp_async_mbar_arrive_noinc(bar(B::SCALE + ssl));
-                    if (lane < 8) reinterpret_cast<float*>(smem + K::OFF_SC)[ssl * 32 + 16 + lane] = cur_c;
+                    if (lane < RMAX) reinterpret_cast<float*>(smem + K::OFF_SC)[ssl * 32 + 16 + lane] = cur_c;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B::SCALE + ssl));
                 }
@@ -1362,12 +1366,20 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                 for (int c = 0; c < RMAX; c += 16) {
                     float tmp[16];
                     tmem_ld16(tmem + lane_base + K::COL_S + (t % NSB) * K::NM + c, tmp);
+                    if constexpr (FP8 && RMAX > 8) {
+                        // hi + lo q terms: columns c + x and RMAX + c + x
+                        float tl[16];
+                        tmem_ld16(tmem + lane_base + K::COL_S + (t % NSB) * K::NM + RMAX + c, tl);
 #pragma unroll
-                    for (int x = 0; x < 16 && c + x < RMAX; ++x) {
-                        if constexpr (FP8)
-                            s[c + x] = tmp[x] + tmp[x + RMAX];   // hi + lo q terms (RMAX = 8)
-                        else
-                            s[c + x] = tmp[x];
+                        for (int x = 0; x < 16 && c + x < RMAX; ++x) s[c + x] = tmp[x] + tl[x];
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 16 && c + x < RMAX; ++x) {
+                            if constexpr (FP8)
+                                s[c + x] = tmp[x] + tmp[x + RMAX];   // hi + lo q terms (RMAX = 8)
+                            else
+                                s[c + x] = tmp[x];
+                        }
                     }
                 }
                 bool need = false;
@@ -1648,8 +1660,9 @@ static int tc_col_limit(int rows) { return rows <= 8 ? 8 : 32; }
 // (heads x G x max_q_len) fit the column limit.
 // At most 4 (narrow) or 2 (wide): each kv-head of a segment has its own O^T
 // accumulator in TMEM.
-int tc_heads_per_segment(int num_kv_heads, int rows) {
-    const int lim = tc_col_limit(rows), cap = rows <= 8 ? 4 : 2;
+int tc_heads_per_segment(int num_kv_heads, int rows, bool fp8) {
+    // (FP8 wide segments: 16 columns, each q row split over two)
+    const int lim = fp8 && rows > 8 ? 16 : tc_col_limit(rows), cap = rows <= 8 ? 4 : 2;
     int hg = 1;
     for (int h = 1; h <= min(num_kv_heads, cap); ++h)
         if (num_kv_heads % h == 0 && h * rows <= lim) hg = h;
@@ -1675,8 +1688,9 @@ cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int
                      : tc::launch_t<64, 32, false, 4, 4, false, false, true>(p, ncta, st);
     }
     if (head_dim == 128)
-        return fp8     ? tc::launch_t<128, 16, true, 4, 4, true, true>(p, ncta, st)
-               : split ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
+        return fp8 && split ? tc::launch_t<128, 16, true, 4, 4, true, true>(p, ncta, st)
+               : fp8        ? tc::launch_t<128, 32, false, 2, 3, true, true>(p, ncta, st)
+               : split      ? tc::launch_t<128, 16, true, 2, 4, true>(p, ncta, st)
                : p.hg * p.rows <= 20 ? tc::launch_t<128, 20, false, 2, 2, true>(p, ncta, st)
                : p.hg * p.rows <= 24 ? tc::launch_t<128, 24, false, 2, 2, false>(p, ncta, st)
                                      : tc::launch_t<128, 32, false, 2, 2, false>(p, ncta, st);

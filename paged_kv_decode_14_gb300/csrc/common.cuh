@@ -174,15 +174,18 @@ struct AttnParams {
 
 // Virtual kv-heads per cache kv-head: the smallest divisor of the GQA group
 // that leaves at most `limit` query rows per virtual head (32 for bf16 caches;
-// 8 for FP8 caches with windows of up to 8 tokens, the rows of the FP8
-// tensor-core kernel: each virtual head's segment re-reads the cache kv-head's
-// pages, mostly from L2, which still beats the CUDA-core kernel by ~4x).
+// for FP8 caches the rows of the FP8 tensor-core kernel: 16 at head_dim 128,
+// 8 at 64 for windows of up to 8 tokens; each virtual head's segment re-reads
+// the cache kv-head's pages, mostly from L2, which still beats the CUDA-core
+// kernel severalfold).
 __host__ inline int kv_split_for(int group, int max_q_len, int limit = 32) {
     for (int ks = 1; ks < group; ++ks)
         if (group % ks == 0 && (group / ks) * max_q_len <= limit) return ks;
     return group;
 }
-__host__ inline int kv_split_limit(bool fp8, int max_q_len) { return fp8 && max_q_len <= 8 ? 8 : 32; }
+__host__ inline int kv_split_limit(bool fp8, int head_dim, int max_q_len) {
+    return !fp8 ? 32 : head_dim == 128 ? 16 : max_q_len <= 8 ? 8 : 32;
+}
 
 // Cache kv-head of virtual kv-head vh.
 __device__ __forceinline__ int cache_head(const AttnParams& p, int vh);

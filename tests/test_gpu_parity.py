@@ -63,11 +63,13 @@ SWEEP = [
     (128, 8, 2, [5, 40, 77, 300], [5, 3, 8, 2], "bf16"),
     (128, 16, 2, [5, 40, 77, 300], [5, 3, 8, 2], "bf16"),  # G = 8, R up to 64: two virtual kv-heads per kv-head
     (64, 32, 2, [9, 130, 33], [4, 2, 3], "bf16"),          # G = 16, R up to 64
-    (128, 32, 4, [20, 300], [5, 2], "fp8"),                # FP8, G = 8, Q = 5: eight virtual groups (tensor cores)
+    (128, 32, 4, [20, 300], [5, 2], "fp8"),                # FP8, G = 8, Q = 5: four virtual groups of 10 rows
     (64, 4, 4, [9, 10, 11], [8, 4, 2], "bf16"),
     (128, 32, 8, [600, 3, 1200], [1, 1, 1], "fp8"),
     (64, 8, 1, [33, 17, 129], [4, 1, 2], "fp8"),           # FP8, G = 8, Q = 4: virtual groups of 2 heads
-    (128, 8, 2, [50, 300, 700, 16], [9, 12, 16, 1], "fp8"),  # FP8 windows of 9-16 tokens: the CUDA-core kernel
+    (64, 8, 2, [50, 300, 700, 16], [9, 12, 16, 1], "fp8"),   # FP8, head_dim 64, 9-16 tokens: the CUDA-core kernel
+    (128, 8, 2, [50, 300, 700, 16], [9, 12, 16, 1], "fp8"),  # FP8, head_dim 128, 16-token windows: 16-row segments
+    (128, 32, 2, [1, 40, 333, 1030], [1, 1, 1, 1], "fp8"),   # FP8, G = 16: one 16-row segment per kv-head
     (128, 16, 1, [40, 250], [2, 2], "bf16"),          # G = 16, R = 32
     (128, 8, 2, [0, 20, 0, 45], [0, 1, 0, 2], "bf16"),  # empty sequences
     (64, 16, 2, [20, 50], [0, 3], "bf16"),             # a sequence with no query rows
@@ -111,7 +113,7 @@ def test_sweep(case):
 def test_fp8_verify_q5_full_size():
     """FP8 cache, 5-token verify windows on the verify batch's shape (32
     sequences, lengths U[512, 4096], G = 4): R = 20 rows per kv-head run as
-    four virtual groups of 5 on the FP8 tensor-core kernel."""
+    two virtual groups of 10 on the wide FP8 tensor-core kernel."""
     rng = np.random.Generator(np.random.PCG64(1005))
     L = rng.integers(512, 4097, size=32).astype(np.int32)
     w = wl.make_workload("verify_fp8", context_lens=L, q_lens=np.full(32, 5, np.int32), num_q_heads=32,
@@ -160,7 +162,7 @@ def test_fp8_subnormal_codes():
     (128, 4, 2, "fp8"),     # tensor-core FP8 kernel, two kv-heads per segment
     (64, 4, 2, "fp8"),      # tensor-core FP8 kernel, head_dim 64
     (64, 16, 2, "fp8"),     # FP8, head_dim 64, G = 16: two virtual groups
-    (128, 16, 2, "fp8"),    # FP8, G = 16: two virtual groups of 8 on the tensor cores
+    (128, 16, 2, "fp8"),    # FP8, G = 16: 16-row segments (the wide FP8 kernel)
     (128, 4, 2, "bf16"),    # tensor-core narrow kernel, two kv-heads per segment
     (64, 1, 4, "bf16"),     # narrow kernel, four kv-heads per segment
     (128, 16, 2, "bf16"),   # wide kernel (N = 32), two kv-heads per segment
