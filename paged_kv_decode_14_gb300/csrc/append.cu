@@ -10,29 +10,50 @@
 
 namespace pkv {
 
-// At most 32 registers a thread, so that a 32-thread CTA fits beside a resident
+// At most 32 registers a thread (bf16), so that a 32-thread CTA fits beside a resident
 // attention CTA (384 threads x 168 registers leave 1024 of an SM's 65536): a
 // decode step's append is then already waiting on the SMs when the attention
 // before it ends.
 template <int E>
-__global__ void __maxnreg__(32) append_kernel(const uint8_t* __restrict__ k_new, const uint8_t* __restrict__ v_new,
+__global__ void __maxnreg__(E == 2 ? 32 : 48) append_kernel(const uint8_t* __restrict__ k_new, const uint8_t* __restrict__ v_new,
                                                      const int64_t* __restrict__ slots, int64_t num_tokens, int Hkv,
                                                      int D, int64_t num_blocks, uint8_t* k_cache, uint8_t* v_cache,
                                                      const float* __restrict__ k_scales,
                                                      const float* __restrict__ v_scales, int* err) {
     griddep_launch();                            // the attention that follows may start its set-up
-    griddep_wait();                              // the previous kernel's reads and writes are done
     const int NCH = D * E / 16;                  // 16-byte chunks per token row in the cache
     const int64_t per_tok = (int64_t)Hkv * NCH * 2;
     const int64_t total = num_tokens * per_tok;
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t idx0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    // The thread's first chunk (a decode step's only one): its slot and source are read before
+    // the dependency wait (the previous kernel -- the last step's attention -- does not write
+    // them), so that only the stores follow the wait.  Scales are read after it.
+    int64_t s0 = -1;
+    uint4 a0 = make_uint4(0, 0, 0, 0), b0 = a0;
+    if (idx0 < total) {
+        const int64_t t = idx0 / per_tok;
+        int rem = (int)(idx0 % per_tok);
+        const int which = rem & 1;
+        rem >>= 1;
+        const int g = rem / NCH, ch = rem % NCH;
+        s0 = slots[t];
+        const uint8_t* src = (which ? v_new : k_new) + (((size_t)t * Hkv + g) * D) * 2;
+        if constexpr (E == 2) {
+            a0 = __ldg(reinterpret_cast<const uint4*>(src + ch * 16));
+        } else {
+            a0 = __ldg(reinterpret_cast<const uint4*>(src + ch * 32));
+            b0 = __ldg(reinterpret_cast<const uint4*>(src + ch * 32 + 16));
+        }
+    }
+    griddep_wait();                              // the previous kernel's reads and writes are done
+    for (int64_t idx = idx0; idx < total; idx += (int64_t)gridDim.x * blockDim.x) {
+        const bool first = idx == idx0;
         const int64_t t = idx / per_tok;
         int rem = (int)(idx % per_tok);
         const int which = rem & 1;               // 0 = K, 1 = V
         rem >>= 1;
         const int g = rem / NCH, ch = rem % NCH;
-        const int64_t s = slots[t];
+        const int64_t s = first ? s0 : slots[t];
         if (s < 0) continue;
         const int64_t blk = s / kBlock;
         const int off = (int)(s % kBlock);
@@ -44,11 +65,11 @@ __global__ void __maxnreg__(32) append_kernel(const uint8_t* __restrict__ k_new,
         uint8_t* page = (which ? v_cache : k_cache) + ((size_t)blk * Hkv + g) * (size_t)(kBlock * D * E);
         uint4* dst = reinterpret_cast<uint4*>(page + ((off >> 3) * NCH + ch) * 128 + (off & 7) * 16);
         if constexpr (E == 2) {
-            *dst = __ldg(reinterpret_cast<const uint4*>(src + ch * 16));
+            *dst = first ? a0 : __ldg(reinterpret_cast<const uint4*>(src + ch * 16));
         } else {
             const float sc = (which ? v_scales : k_scales)[(size_t)blk * Hkv + g];
-            const uint4 a = __ldg(reinterpret_cast<const uint4*>(src + ch * 32));
-            const uint4 b = __ldg(reinterpret_cast<const uint4*>(src + ch * 32 + 16));
+            const uint4 a = first ? a0 : __ldg(reinterpret_cast<const uint4*>(src + ch * 32));
+            const uint4 b = first ? b0 : __ldg(reinterpret_cast<const uint4*>(src + ch * 32 + 16));
             const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
             uint32_t packed[4];
 #pragma unroll
