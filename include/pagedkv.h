@@ -116,6 +116,13 @@ typedef struct pkv_cache {
  * its (block, kv-head) scale in IEEE fp32 and encoded to E4M3 with round to
  * nearest even and saturation to +-448 (NaN stays NaN).
  * num_tokens = 0 is a no-op.
+ *
+ * Launch (programmatic dependent launch): the kernel lets the next kernel on
+ * the stream launch at once, and reads slot_mapping, k_new and v_new (its
+ * threads' first chunks) before waiting for the previous kernel on the
+ * stream; the cache and the scales are touched only after that wait.  So a
+ * kernel that lets its dependents start early must not write those three
+ * inputs (none of this library's kernels writes them).
  */
 PKV_API pkv_status pkv_paged_kv_append(const pkv_cache* cache, const void* k_new, const void* v_new,
                                        const int64_t* slot_mapping, int64_t num_tokens,
@@ -147,7 +154,10 @@ PKV_API pkv_status pkv_paged_kv_append(const pkv_cache* cache, const void* k_new
  *                  v_scales arrays are written.  A block continued by a later call
  *                  keeps its scale (values beyond it saturate).  0: the scales are
  *                  inputs, as for pkv_paged_kv_append.
- * Other arguments and the slot rules as for pkv_paged_kv_append.  Supported
+ * Other arguments and the slot rules as for pkv_paged_kv_append.  Unlike it,
+ * the last of its launches lets the next kernel on the stream launch only
+ * once it has completed: it rotates q in place, and an attention that
+ * follows reads q before its own dependency wait.  Supported
  * up to 32 kv-heads (else PKV_ERR_UNSUPPORTED).  Launches one CTA per token
  * (plus two short kernels when FP8 scales are chosen here).
  */

@@ -143,7 +143,8 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(
     extern __shared__ __align__(16) uint8_t rope_smem[];
     __shared__ double2 cs[kMaxHalf];
     __shared__ float sc[2][32];                         // this token's (K, V) scale per kv-head (FP8)
-    griddep_launch();
+    // No early trigger here: this kernel rotates q in place, and the attention that follows reads
+    // its q rows before its own dependency wait, so it may launch only once this grid has ended.
     griddep_wait();
     const int64_t t = blockIdx.x;
     const int half = D / 2, tid = threadIdx.x;

@@ -96,3 +96,13 @@ def test_fp8_scales_from_values_without_rotation():
 
 def test_rope_append_fp8_given_scales():
     _run(_workload("fp8", 205), 10000.0, rotate=True, autoscale=False)
+
+
+def test_rope_append_then_attention_large_batch():
+    """300 sequences: the RoPE append (one CTA per token) runs long enough
+    that an attention launched before it ended would read q rows not yet
+    rotated; the attention must see every rotated row."""
+    rng = np.random.default_rng(206)
+    lens = rng.integers(4, 400, 300).tolist()
+    ql = [int(min(L, 1 + (i % 3))) for i, L in enumerate(lens)]
+    _run(_workload("bf16", 206, lens=lens, ql=ql), 10000.0, rotate=True, autoscale=False)
