@@ -58,10 +58,10 @@
 // quarter), warp 4 producer (bulk copies, q staging, one piece ahead on q and
 // the block table), warp 5 the S^T issuer, warp 6 the merge warp, warp 7 the
 // P.V issuer (the two issuers block on their own barriers, so a P.V never
-// waits behind the next tiles' S^T), and for narrow segments warps 8-11, the
-// epilogue warpgroup: piece epilogues run there, off the softmax's path
-// (wide segments run them in the softmax warps, after the next piece's first
-// tile).  Every mbarrier wait is bounded (2 s); a timeout sets
+// waits behind the next tiles' S^T), and warps 8-11, the epilogue warpgroup:
+// piece epilogues run there, off the softmax's path (the bf16 wide instances
+// of more than 20 columns, whose softmax needs the registers of a 256-thread
+// block, run them in the softmax warps, after the next piece's first tile).  Every mbarrier wait is bounded (2 s); a timeout sets
 // PKV_DEVERR_TIMEOUT and an abort flag, all roles wind down, in-flight copies
 // are drained and TMEM is freed before the CTA exits.
 #include "common.cuh"
