@@ -10,7 +10,9 @@
 // sit on the MMA's N side ("swap AB"): column n = hh * R + r for kv-head
 // hh of the group and row r = i * G + hl of that head's GQA group, R = G * Q,
 // NCOL = HG * R <= 8 (P split into a bf16 high and low part on adjacent
-// columns, N = 16) or <= 32 (N = 32).  A 128-token tile holds 8 (page,
+// columns, N = 16) or <= 32 (N = 32; P's low parts in a second ring, and
+// instances whose softmax handles only the first 20 or 24 columns).  A
+// 128-token tile holds 8 (page,
 // kv-head) units in page-major order; each token row only sees the columns of
 // its own kv-head.
 //
@@ -34,18 +36,18 @@
 // the CUDA cores (except zeroing the unwritten tail rows of a sequence's last
 // page, which may hold NaN).
 //
-// FP8 (e4m3) caches, NCOL <= 8: the K pages stay e4m3 and S^T
-// runs on kind::f8f6f4 MMAs against the q rows, each scaled by a power of two
-// and split exactly into two e4m3 terms (columns n and 8 + n, added in the
-// softmax with the page's k scale); the V pages land in the upper half of a
-// bf16 operand slot and the epilogue warpgroup widens them in place; P
-// carries the page's v scale.  Page scales reach a ring in shared memory by
-// cp.async.
+// FP8 (e4m3) caches, NCOL <= 8 (N = 16) or, at head_dim 128, <= 16 (N = 32):
+// the K pages stay e4m3 and S^T runs on kind::f8f6f4 MMAs against the q
+// rows, each scaled by a power of two and split exactly into two e4m3 terms
+// (columns n and NCOL-max + n, added in the softmax with the page's k scale);
+// the V pages land in the upper half of a bf16 operand slot and the softmax
+// warpgroup widens them in place after writing each tile's P; P carries the
+// page's v scale.  Page scales reach a ring in shared memory by cp.async.
 //
 // Work partition: the balanced unit partition of common.cuh, one persistent
 // CTA per SM (for wide and FP8 segments, cut by weight with a fixed charge
-// per segment).  A
-// CTA takes its last piece first and then walks its range from the start, so
+// per segment).  A CTA takes its last piece first and then walks its range
+// from the start, so
 // both pieces of every segment cut between two CTAs finish early and their
 // merge overlaps the rest of the work.
 //
