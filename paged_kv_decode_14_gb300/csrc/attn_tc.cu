@@ -266,43 +266,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Four e4m3 codes (bytes of w, lowest first) -> four bf16 (lo: codes 0, 1;
-// hi: codes 2, 3), exact, on the integer and bf16x2 pipes instead of the
-// conversion unit.  A code's 4 exponent and 3 mantissa bits are placed in the
-// low exponent bits and the top mantissa bits of a bf16, which then reads as
-// the code's value times 2^-120 (its bf16 subnormals are the e4m3 subnormals);
-// a bf16x2 multiply by 2^120 restores the value.  The NaN codes (0x7f, 0xff;
-// the append keeps a NaN source value NaN) come out as +-480 (magnitude
-// 0x43f0), a value no finite code reaches (the largest is 448): see
-// fix_nan_lanes.
-__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t hb = ((w >> 4) & 0x07070707u) | (w & 0x80808080u);   // per byte: sign, 3 high exponent bits
-    const uint32_t lb = (w << 4) & 0xF0F0F0F0u;                          // per byte: low exponent bit, mantissa
-    const uint32_t a = __byte_perm(lb, hb, 0x5140), b = __byte_perm(lb, hb, 0x7362);
-    const __nv_bfloat162 k2 = __halves2bfloat162(__ushort_as_bfloat16(0x7B80), __ushort_as_bfloat16(0x7B80));
-    const __nv_bfloat162 ra = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), k2);
-    const __nv_bfloat162 rb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), k2);
-    lo = *reinterpret_cast<const uint32_t*>(&ra);
-    hi = *reinterpret_cast<const uint32_t*>(&rb);
+// Four e4m3 codes (bytes of w, lowest first) -> four fp16 (lo: codes 0, 1;
+// hi: codes 2, 3) by CUDA's conversion: exact (every e4m3 value is an fp16
+// value), NaN codes to NaN.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+    const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
+    hi = (uint32_t)b.x | ((uint32_t)b.y << 16);
 }
 
-// The rare path of the V widening: turns the +-480 lanes that NaN codes
-// produced in the 16-byte chunk at c into bf16 NaN of the same sign.
-__device__ __forceinline__ void fix_nan_lanes(uint8_t* c) {
-    uint4 w = *reinterpret_cast<const uint4*>(c);
-    uint32_t x[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if ((x[j] & 0x7FFFu) == 0x43F0u) x[j] |= 0x7FC0u;
-        if ((x[j] & 0x7FFF0000u) == 0x43F00000u) x[j] |= 0x7FC00000u;
-    }
-    *reinterpret_cast<uint4*>(c) = make_uint4(x[0], x[1], x[2], x[3]);
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
-
-// Bit 7 of byte i of the result is set iff byte i of w is an E4M3 NaN code
-// (low seven bits all ones): (b & 0x7f) + 1 reaches 0x80 only for those, and
-// never carries into the next byte.
-__device__ __forceinline__ uint32_t e4m3_nan_bits(uint32_t w) { return (w & 0x7F7F7F7Fu) + 0x01010101u; }
 
 // Pieces of a CTA's unit range [u0, u1), in processing order: the piece
 // holding u1 - 1 first (when it does not start at u0), then [u0, start of
@@ -606,9 +583,9 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
     // a 128-thread warpgroup (named barrier bid) reads its 16-byte chunk e of
     // NPT of the pages (D = 128: chunk tt of all 8 pages; D = 64, 64 chunks a
     // page: chunk tt % 64 of pages tt / 64, tt / 64 + 2, ...), the warpgroup
-    // syncs, then writes the bf16 operand ([2][D/8][8][8] elements per page)
-    // over the whole slot.  Codes are exact in bf16; the page scales are
-    // applied in the softmax.
+    // syncs, then writes the fp16 operand ([2][D/8][8][8] elements per page)
+    // over the whole slot.  Codes are exact in fp16 (NaN codes become NaN);
+    // the page scales are applied in the softmax (P carries the v scale).
     auto widen = [&](uint8_t* slot, int tt, int bid) {
         constexpr int CPP8 = K::PAGE8 / 16;                  // 16-byte chunks of an e4m3 page
         constexpr int PSTEP = kSoftThreads / CPP8;           // pages between a thread's pages
@@ -621,13 +598,6 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         for (int j = 0; j < NPT; ++j)
             v[j] = *reinterpret_cast<const uint4*>(slot + K::OFF_LAND + (k0 + j * PSTEP) * K::PAGE8 + e * 16);
         named_bar_sync(bid, kSoftThreads);
-        // NaN codes are rare (a NaN value stored in the cache; the unwritten slots of a
-        // sequence's last page may hold anything): a cheap test over the thread's own
-        // chunks, and the exact fix of the chunks it wrote only when it hits
-        uint32_t nb = 0;
-#pragma unroll
-        for (int j = 0; j < NPT; ++j)
-            nb |= e4m3_nan_bits(v[j].x) | e4m3_nan_bits(v[j].y) | e4m3_nan_bits(v[j].z) | e4m3_nan_bits(v[j].w);
         // chunk e of a page: token group e / (8 NC16), 16-element column block (e / 8) % NC16, token e % 8
         const int r = e & 7, c = (e >> 3) % NC16, oh = e / (8 * NC16);
         uint8_t* d0 = slot + ((oh * (D / 8) + 2 * c) * 8 + r) * 16 + k0 * K::PAGE;
@@ -636,13 +606,9 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
             const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
             uint32_t o[8];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) e4m3x4_to_bf16x4(wv[x], o[2 * x], o[2 * x + 1]);
+            for (int x = 0; x < 4; ++x) e4m3x4_to_f16x4(wv[x], o[2 * x], o[2 * x + 1]);
             *reinterpret_cast<uint4*>(d0 + j * PSTEP * K::PAGE) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(d0 + j * PSTEP * K::PAGE + 128) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        if (nb & 0x80808080u) {      // (stale pages past the tile's page count may hit too: harmless)
-#pragma unroll 1
-            for (int i = 0; i < 2 * NPT; ++i) fix_nan_lanes(d0 + (i >> 1) * PSTEP * K::PAGE + (i & 1) * 128);
         }
         fence_proxy_async_smem();             // the MMA reads the slot through the async proxy
     };
@@ -1140,7 +1106,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
         // starts its accumulator afresh once the epilogue of the piece two
         // before has read it.
         if (lane == 0) {
-            constexpr uint32_t idPV = idesc_bf16_f32(128, K::NM, true, true);
+            // (FP8: fp16 operands, V widened to fp16)
+            constexpr uint32_t idPV = FP8 ? idesc_f16_f32(128, K::NM, true, true) : idesc_bf16_f32(128, K::NM, true, true);
             int t = 0, pc = 0;
             bool ok = true;
             while (ok && it.valid()) {
@@ -1359,6 +1326,9 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                     const float* sc = reinterpret_cast<const float*>(smem + K::OFF_SC) + (t % K::NSC) * 32;
                     kscale = sc[k];
                     vscale = sc[8 + k];
+                    // P carries the v scale into fp16 operands: P < 2^8 keeps P * vscale finite for
+                    // scales up to 255 (|v| below ~114,000 before encoding)
+                    if (vscale > 255.f) raise_error(p.err, PKV_DEVERR_RANGE);
 #pragma unroll
                     for (int n = 0; n < RMAX; ++n) cf[n] = sc[16 + n] * (p.scale_log2 * kscale);
                 }
@@ -1493,7 +1463,8 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                         if constexpr (SPLIT) {
                             const int n = cc * 4 + h;          // physical columns 2n (high) and 2n+1 (low)
                             const float pv = FP8 ? pr[n] * vscale : pr[n];
-                            const float hi = __bfloat162float(__float2bfloat16_rn(pv));
+                            // (FP8: fp16 parts, the type of the widened V)
+                            const float hi = FP8 ? __half2float(__float2half_rn(pv)) : __bfloat162float(__float2bfloat16_rn(pv));
                             a = hi;
                             b = pv - hi;
                         } else {
@@ -1501,13 +1472,13 @@ __global__ void __launch_bounds__(threads_of<EWG>(), 1) attn_tc_kernel(const Att
                             const int n0 = cc * 8 + 2 * h;
                             a = n0 < RMAX ? (FP8 ? pr[n0] * vscale : pr[n0]) : 0.f;
                             b = n0 + 1 < RMAX ? (FP8 ? pr[n0 + 1] * vscale : pr[n0 + 1]) : 0.f;
-                            const float ah = __bfloat162float(__float2bfloat16_rn(a));
-                            const float bh = __bfloat162float(__float2bfloat16_rn(b));
-                            l4[h] = pack_bf16x2(a - ah, b - bh);
+                            const float ah = FP8 ? __half2float(__float2half_rn(a)) : __bfloat162float(__float2bfloat16_rn(a));
+                            const float bh = FP8 ? __half2float(__float2half_rn(b)) : __bfloat162float(__float2bfloat16_rn(b));
+                            l4[h] = FP8 ? pack_f16x2(a - ah, b - bh) : pack_bf16x2(a - ah, b - bh);
                             a = ah;
                             b = bh;
                         }
-                        w4[h] = pack_bf16x2(a, b);
+                        w4[h] = FP8 ? pack_f16x2(a, b) : pack_bf16x2(a, b);
                     }
                     *reinterpret_cast<uint4*>(pdst + cc * (16 * 128)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     if constexpr (!SPLIT)
