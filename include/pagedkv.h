@@ -86,7 +86,9 @@ typedef enum pkv_kv_dtype { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
 #define PKV_DEVERR_LENGTH 2     /* q_len > context_len, or a negative length */
 #define PKV_DEVERR_SLOT 4       /* slot >= num_blocks * 16 in an append */
 #define PKV_DEVERR_TIMEOUT 8    /* a bounded wait inside a kernel expired */
-#define PKV_DEVERR_RANGE 16     /* pkv_paged_prefill: a finite V value of magnitude >= 65536 */
+#define PKV_DEVERR_RANGE 16     /* pkv_paged_prefill: a finite V value of magnitude >= 65536;
+                                   pkv_paged_attention, FP8 cache on the tensor cores: a V scale
+                                   above 255 */
 
 /* One paged cache ("startup policy": fixed for its lifetime). */
 typedef struct pkv_cache {
@@ -226,6 +228,11 @@ PKV_API pkv_status pkv_workspace_init(void* workspace, size_t workspace_bytes, v
  * hit L2).
  * Results are deterministic and depend only
  * on logical positions (not on which physical blocks hold them).
+ *
+ * FP8 caches on the tensor cores take P.V in fp16 (V's e4m3 codes are exact
+ * in fp16; P carries the page's v scale): a v scale above 255 (values beyond
+ * ~114,000 before encoding) sets PKV_DEVERR_RANGE and the affected outputs
+ * are unspecified.
  *
  * NaN in the cache: a NaN stored in K makes every element of the rows that
  * see it NaN, and a NaN in V the matching dimension of those rows, as in the
