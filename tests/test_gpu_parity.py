@@ -381,3 +381,22 @@ def test_append_skips_negative_slots_and_flags_out_of_range():
     oracle.paged_kv_append(0, kc, vc, None, None, NB, Hkv, D, w_k, w_k, slots.cpu().numpy())
     got = cache.k.view(torch.int16).cpu().numpy().reshape(-1).view(np.uint16)
     assert np.array_equal(got, kc)
+
+
+def test_fp8_v_scale_range():
+    """FP8 caches take P.V in fp16 with P carrying the page's v scale: a
+    scale of 255 (P < 2^8 keeps P * scale inside fp16) matches the oracle
+    with no error; 256 sets PKV_DEVERR_RANGE."""
+    w = wl.make_workload("f8range", context_lens=[300, 77], q_lens=[1, 1], num_q_heads=32, num_kv_heads=8,
+                         head_dim=128, kv_dtype="fp8", seed=950)
+    blk = int(w.block_tables[0, 3])
+    w.v_scales[blk, 2] = 255.0
+    kc, vc = oracle.build_cache(w)
+    ref, _ = oracle.attend(w, kc, vc)
+    dw, got = run_gpu(w)
+    assert_attention_close(got, ref, "v scale 255")
+    assert dw.errors() == (0, 0)
+    w.v_scales[blk, 2] = 256.0
+    dw, _ = run_gpu(w)
+    a, _ = dw.errors()
+    assert a == nat.DEVERR_RANGE
