@@ -281,7 +281,7 @@ def dense_sdpa_reference(w, kc, vc):
     return out.numpy()
 
 
-@pytest.mark.parametrize("case", ["tiny", "verify", "prefix", "fp8", "d128"])
+@pytest.mark.parametrize("case", ["tiny", "verify", "prefix", "fp8", "d128", "prefill"])
 def test_attention_equals_dense_sdpa(case):
     if case == "tiny":
         w = wl.tiny_decode()
@@ -294,9 +294,13 @@ def test_attention_equals_dense_sdpa(case):
     elif case == "fp8":
         w = wl.make_workload("f", context_lens=[20, 130, 1], q_lens=[1, 2, 1], num_q_heads=8,
                              num_kv_heads=2, head_dim=128, kv_dtype="fp8", seed=23, outlier_p=0.01)
-    else:
+    elif case == "d128":
         w = wl.make_workload("d", context_lens=[100, 3], q_lens=[1, 1], num_q_heads=8,
                              num_kv_heads=1, head_dim=128, seed=24)
+    else:
+        # whole prompts: every token is a query, the first one sees only itself
+        w = wl.make_workload("c", context_lens=[17, 33, 1], q_lens=[17, 33, 1], num_q_heads=8,
+                             num_kv_heads=2, head_dim=64, seed=25)
     kc, vc = oracle.build_cache(w)
     out, outb = oracle.attend(w, kc, vc)
     ref = dense_sdpa_reference(w, kc, vc)
